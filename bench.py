@@ -1,0 +1,448 @@
+#!/usr/bin/env python
+"""Benchmark of the GDN layer hot path on GB300.
+
+Headline step: one fused GDN decode step (conv roll + conv + SiLU + L2 norm +
+gates + gated delta rule) in the Qwen3-Next geometry (Hk=16, Hv=32, dk=dv=128,
+8192 conv channels, width 4, bf16 conv cache, fp32 state) for B=256 rows
+through a shuffled slot table over 512 slots. Metric: algorithmic HBM GB/s of
+that step. Also reported: the decode batch sweep, the B=1024-over-2048-slot
+case, and chunked-prefill tokens/s on one 4096-token sequence and on ~32k
+packed varlen tokens.
+
+Timing: W untimed warm-up steps, then exactly K timed steps. Each step is
+bracketed by CUDA events on the stream the library launches on; L2 is flushed
+(a 512 MiB buffer is overwritten) between timed steps, outside the events.
+Multi-GPU (torchrun): every rank runs its own workload on its own GPU (weak
+scaling, no data-path collective); the step time is the max over ranks.
+
+--impl reference times the fp64 CPU oracle (the only reference this build
+has) on the host cores on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = ("GDN decode HBM GB/s (% of peak) and chunked-prefill tokens/s per layer, 1 GB300")
+HEADLINE_B = 256
+NUM_SLOTS = 512
+FALLBACK_HBM_GBS = 6800.0
+# fp32 CUDA-core peak: 152 SMs x 128 FMA/clk x 2 FLOP x 2.07 GHz
+FP32_ALU_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
+
+
+def decode_bytes(B, geo, conv_f32=False, bias=True, out_bytes=2):
+    """Algorithmic bytes of one decode step: per row the fp32 state read + write, x, the
+    conv window read + write, the output and the gate inputs and slot; per call the conv
+    weight and bias and the per-head gate parameters."""
+    s = 4 if conv_f32 else 2
+    D = geo.D
+    per_row = (2 * geo.Hv * geo.dv * geo.dk * 4 + 2 * D + 2 * D * (geo.W - 1) * s
+               + out_bytes * geo.Hv * geo.dv + 2 * 2 * geo.Hv + 4)
+    per_call = 2 * D * geo.W + (2 * D if bias else 0) + 8 * geo.Hv
+    return B * per_row + per_call
+
+
+def prefill_flops_per_token(geo, C=64):
+    """Dense-tile FLOPs per token of the chunked form (Gram and QK^T shared per k-head)."""
+    dk, dv, r = geo.dk, geo.dv, geo.Hv // geo.Hk
+    per_chunk_head = 2 * (C * C * dk / r * 2 + C * C * dv + C * C * dk + 2 * C * dk * dv
+                          + C * C * dv + dv * C * dk)
+    return per_chunk_head * geo.Hv / C
+
+
+def prefill_bytes(T, N, geo, conv=True, conv_s=2):
+    D = geo.D
+    per_tok = 2 * D + 2 * 2 * geo.Hv + 2 * geo.Hv * geo.dv
+    per_seq = 2 * geo.Hv * geo.dv * geo.dk * 4 + (2 * D * (geo.W - 1) * conv_s if conv else 0)
+    return T * per_tok + N * per_seq
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            j = json.load(f)
+        return float(j["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_digest():
+    h = hashlib.sha256()
+    for f in ("gdn_decode.cu", "gdn_common.cuh"):
+        with open(os.path.join(ROOT, "gated_deltanet_linear_gdn_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic():
+    """Per-launch DRAM bytes of the decode kernel from the committed ncu summary, if it was
+    taken on the current kernel source (else None)."""
+    p = os.path.join(ROOT, "profiles", "decode_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        j = json.load(f)
+    if j.get("source_digest") != kernel_source_digest():
+        return None
+    return j
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join(ROOT, f".clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.fh,
+                stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.remove(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
+        return {"sm_mhz": float(np.median(sm)) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+# --------------------------------------------------------------------------- our arm
+
+def run_ours(args, rank, world):
+    import torch
+
+    import gated_deltanet_linear_gdn_gb300 as gdn
+    from gated_deltanet_linear_gdn_gb300 import inputs as gi
+
+    gdn.lib()  # fails loudly if the CUDA library is missing
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+    geo = gi.QWEN3_NEXT
+    dims = gdn.Dims(geo.Hk, geo.Hv, geo.dk, geo.dv, geo.W)
+    flush_buf = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+
+    def flush():
+        flush_buf.fill_(1)
+
+    def b16(x):
+        return torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).view(torch.bfloat16)
+
+    def decode_setup(B, num_slots, seed, conv_f32=False, bias=True, silu=True):
+        inp = gi.make_inputs(geo, [1] * B, num_slots, seed, state_pool=False, conv_f32=conv_f32,
+                             bias=bias, silu=silu)
+        t = dict(
+            mixed=b16(inp.mixed).to(dev), a=b16(inp.a).to(dev), b=b16(inp.b).to(dev),
+            A_log=torch.from_numpy(inp.A_log).to(dev), dt_bias=torch.from_numpy(inp.dt_bias).to(dev),
+            conv_w=b16(inp.conv_w).to(dev), conv_b=None if inp.conv_b is None else b16(inp.conv_b).to(dev),
+            conv=(torch.from_numpy(inp.conv_state) if conv_f32 else b16(inp.conv_state)).to(dev),
+            ssm=gi.device_state_pool(num_slots, geo, 0.05, seed + 7, dev),
+            slot=torch.from_numpy(inp.slot).to(dev),
+            out=torch.empty(B, geo.Hv, geo.dv, dtype=torch.bfloat16, device=dev),
+            silu=silu, inp=inp)
+        return t
+
+    def decode_call(t):
+        gdn.gdn_decode_step(t["mixed"], t["a"], t["b"], t["A_log"], t["dt_bias"], t["conv_w"],
+                            t["conv_b"], t["conv"], t["ssm"], t["slot"], t["out"], dims,
+                            silu=t["silu"], stream=stream)
+
+    def timed(fn, steps, warmup, do_flush=True):
+        for _ in range(warmup):
+            fn()
+        torch.cuda.synchronize()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(steps)]
+        for e0, e1 in ev:
+            if do_flush:
+                flush()
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        return [e0.elapsed_time(e1) for e0, e1 in ev]
+
+    result = {}
+    clocks = ClockSampler(dev.index).start() if rank == 0 else None
+
+    # ---- decode sweep (context) ----
+    sweep = {}
+    if not args.no_sweep:
+        for B in (1, 2, 4, 8, 16, 64, 256):
+            t = decode_setup(B, NUM_SLOTS, seed=B)
+            ms = float(np.median(timed(lambda: decode_call(t), 20, 3)))
+            nb = decode_bytes(B, geo)
+            sweep[str(B)] = {"us": round(ms * 1e3, 2), "GBps": round(nb / ms / 1e6, 1)}
+            del t
+        for conv_f32 in (False, True):
+            t = decode_setup(1024, 2048, seed=5, conv_f32=conv_f32)
+            ms = float(np.median(timed(lambda: decode_call(t), 10, 2)))
+            nb = decode_bytes(1024, geo, conv_f32=conv_f32)
+            key = "1024_of_2048_" + ("f32cache" if conv_f32 else "bf16cache")
+            sweep[key] = {"us": round(ms * 1e3, 2), "GBps": round(nb / ms / 1e6, 1)}
+            del t
+        torch.cuda.empty_cache()
+
+    # ---- chunked prefill ----
+    prefill = {}
+    if not args.no_prefill:
+        for name, inp in (("single_4096_bypass", gi.prefill_single(4096, seed=0)),
+                          ("varlen_8seq_conv", gi.prefill_varlen(8, 8192, seed=0))):
+            T, N = inp.total_tokens, inp.slot.size
+            tt = dict(
+                mixed=b16(inp.mixed).to(dev), a=b16(inp.a).to(dev), b=b16(inp.b).to(dev),
+                A_log=torch.from_numpy(inp.A_log).to(dev),
+                dt_bias=torch.from_numpy(inp.dt_bias).to(dev),
+                conv_w=None if inp.conv_w is None else b16(inp.conv_w).to(dev),
+                conv_b=None if inp.conv_b is None else b16(inp.conv_b).to(dev),
+                conv=None if inp.conv_state is None else b16(inp.conv_state).to(dev),
+                ssm=torch.from_numpy(inp.ssm_state).to(dev),
+                cu=torch.from_numpy(inp.cu_seqlens).to(dev), slot=torch.from_numpy(inp.slot).to(dev),
+                hi=None if inp.has_init is None else torch.from_numpy(inp.has_init).to(dev),
+                out=torch.empty(T, geo.Hv, geo.dv, dtype=torch.bfloat16, device=dev))
+            ws = torch.empty(gdn.gdn_chunked_prefill_workspace_size(T, N, dims, 64),
+                             dtype=torch.uint8, device=dev)
+
+            def pcall(tt=tt, ws=ws):
+                gdn.gdn_chunked_prefill(tt["mixed"], tt["a"], tt["b"], tt["A_log"], tt["dt_bias"],
+                                        tt["conv_w"], tt["conv_b"], tt["conv"], tt["ssm"], tt["cu"],
+                                        tt["slot"], tt["hi"], tt["out"], ws, dims, chunk=64,
+                                        stream=stream)
+            ms = float(np.median(timed(pcall, 5, 2)))
+            fl = prefill_flops_per_token(geo) * T
+            prefill[name] = {"tokens": T, "seqs": N, "ms": round(ms, 3),
+                             "tokens_per_s": round(T / ms * 1e3, 1),
+                             "TFLOPs": round(fl / ms / 1e9, 2),
+                             "alu_frac_fp32": round(fl / ms / 1e9 / FP32_ALU_TFLOPS, 4),
+                             "GBps": round(prefill_bytes(T, N, geo, conv=inp.conv_w is not None) / ms / 1e6, 1)}
+            del tt, ws
+        torch.cuda.empty_cache()
+
+    # ---- e2e through the public API with pinned host buffers ----
+    t = decode_setup(HEADLINE_B, NUM_SLOTS, seed=HEADLINE_B)
+    h_mixed = t["mixed"].cpu().pin_memory()
+    h_a, h_b = t["a"].cpu().pin_memory(), t["b"].cpu().pin_memory()
+    h_slot = t["slot"].cpu().pin_memory()
+    h_out = torch.empty_like(t["out"], device="cpu").pin_memory()
+
+    def e2e_call():
+        t["mixed"].copy_(h_mixed, non_blocking=True)
+        t["a"].copy_(h_a, non_blocking=True)
+        t["b"].copy_(h_b, non_blocking=True)
+        t["slot"].copy_(h_slot, non_blocking=True)
+        decode_call(t)
+        h_out.copy_(t["out"], non_blocking=True)
+
+    e2e_ms = float(np.mean(timed(e2e_call, max(5, args.steps // 2), 3)))
+    h2d = sum(x.numel() * x.element_size() for x in (h_mixed, h_a, h_b, h_slot))
+    d2h = h_out.numel() * h_out.element_size()
+
+    # ---- headline: exactly K timed decode steps ----
+    nbytes = decode_bytes(HEADLINE_B, geo)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+    step_ms = timed(lambda: decode_call(t), args.steps, args.warmup)
+    torch.cuda.synchronize()
+    mean_ms = float(np.mean(step_ms))
+    if world > 1:
+        import torch.distributed as dist
+        x = torch.tensor([mean_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(x, op=dist.ReduceOp.MAX)
+        dist.barrier()
+        mean_ms = float(x.item())
+    clk = clocks.stop() if clocks else None
+
+    if rank != 0:
+        return None
+    peak, peak_kind = load_peaks()
+    achieved = nbytes / (mean_ms * 1e-3) / 1e9
+    traffic = ncu_traffic()
+    value = nbytes * world / (mean_ms * 1e-3) / 1e9
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(mean_ms, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": "GDN decode step, Qwen3-Next geometry Hk=16 Hv=32 dk=dv=128 "
+                               "D=8192 W=4, B=256 rows over 512 shuffled slots, bf16 conv cache, "
+                               "fp32 state, bf16 I/O",
+                   "batch": HEADLINE_B, "num_slots": NUM_SLOTS,
+                   "bytes_per_step": nbytes, "l2": "flushed between timed steps (512 MiB write)"},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
+                     "frac_of_8TBps_nominal": round(achieved / 8000.0, 4),
+                     "traffic": None if traffic is None else traffic["dram_bytes_per_launch"],
+                     "traffic_note": None if traffic is None else traffic.get("note")},
+        "e2e": {"value": round(nbytes * world / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": round(e2e_ms, 5)},
+        "gpu_launches": args.steps,
+        "clocks": clk,
+        "decode_sweep": sweep,
+        "prefill": prefill,
+        "context": {"pages_gb10_c16_GBps": 175.14,
+                    "note": "GB10 (SM121) whole GDN transition incl. W4A4 projections; context only"},
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(seconds=args.cpu_seconds)
+    return line
+
+
+# --------------------------------------------------------------------------- oracle arm
+
+def oracle_decode_sample(rows, seed=HEADLINE_B):
+    """Host inputs of a `rows`-row sample of the headline decode workload (compact pool)."""
+    from gated_deltanet_linear_gdn_gb300 import inputs as gi
+
+    geo = gi.QWEN3_NEXT
+    inp = gi.make_inputs(geo, [1] * rows, rows + 1, seed, slots=np.arange(1, rows + 1))
+    return inp
+
+
+def _oracle_call(inp, conv, ssm, nthreads):
+    import oracle
+
+    g = inp.geo
+    return oracle.layer(inp.mixed, inp.a, inp.b, False, inp.A_log, inp.dt_bias, inp.conv_w,
+                        inp.conv_b, True, conv, False, 0, ssm, inp.cu_seqlens, inp.slot, None,
+                        g.Hk, g.Hv, g.dk, g.dv, g.W, inp.scale, True, None, nthreads)
+
+
+def cpu_baseline(seconds=10.0, rows=32):
+    import oracle
+
+    oracle.lib()
+    nthreads = os.cpu_count() or 1
+    inp = oracle_decode_sample(rows)
+    conv = inp.conv_state.copy()
+    ssm = inp.ssm_state.astype(np.float64)
+    runs = 0
+    t0 = time.perf_counter()
+    while True:
+        _oracle_call(inp, conv, ssm, nthreads)
+        runs += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    nb = decode_bytes(rows, inp.geo) * runs
+    return {"value": round(nb / el / 1e9, 4), "unit": "GB/s", "cores": nthreads, "kind": "oracle",
+            "sample": f"{rows} rows of the B=256 decode workload (Qwen3-Next geometry), "
+                      f"{runs} oracle calls in {el:.1f} s, fp64, {nthreads} threads"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    import oracle
+
+    oracle.lib()
+    nthreads = os.cpu_count() or 1
+    rows = 16
+    inp = oracle_decode_sample(rows)
+    conv = inp.conv_state.copy()
+    ssm = inp.ssm_state.astype(np.float64)
+    for _ in range(args.warmup):
+        _oracle_call(inp, conv, ssm, nthreads)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        _oracle_call(inp, conv, ssm, nthreads)
+        times.append(time.perf_counter() - t0)
+    nb = decode_bytes(rows, inp.geo)
+    mean_s = float(np.mean(times))
+    value = nb / mean_s / 1e9
+    sample = (f"{rows} rows of the B=256 decode workload per step (Qwen3-Next geometry), fp64 "
+              f"oracle, {nthreads} host threads")
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(mean_s * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "GDN decode step, Qwen3-Next geometry Hk=16 Hv=32 dk=dv=128 "
+                               "D=8192 W=4, B=256 rows over 512 shuffled slots, bf16 conv cache, "
+                               "fp32 state, bf16 I/O", "batch": HEADLINE_B,
+                   "num_slots": NUM_SLOTS, "sampled_rows_per_step": rows},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": nthreads,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        dist.init_process_group("nccl")
+    line = run_ours(args, rank, world)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,1 +1,184 @@
-"""GB300-native Gated DeltaNet layer hot path (conv update, fused decode step, chunked prefill)."""
+"""GB300-native Gated DeltaNet (GDN) layer hot path.
+
+A thin ctypes binding over ``libgdn.so`` (the C ABI of ``include/gdn.h``):
+the functions below carry the C entry points' names and only marshal
+arguments -- torch tensors in, device pointers and sizes out. Every step of
+the layer runs in the library's CUDA kernels; there is no Python or CPU
+fallback. If the library is missing or fails to load, every call raises.
+
+torch is used only for device memory, streams and dtypes.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libgdn.so")
+
+GDN_OK, GDN_ERR_INVALID_ARG, GDN_ERR_UNSUPPORTED, GDN_ERR_CUDA = 0, 1, 2, 3
+GDN_BF16, GDN_F32 = 0, 1
+GDN_CONV_DIM_FIRST, GDN_CONV_TAP_FIRST = 0, 1
+GDN_GATE_FUSED, GDN_GATE_DIRECT = 0, 1
+GDN_DEVERR_SLOT_RANGE, GDN_DEVERR_SEQLENS = 1, 2
+
+
+class GDNError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(msg)
+        self.status = status
+
+
+class gdn_dims(ctypes.Structure):
+    _fields_ = [("num_k_heads", ctypes.c_int32), ("num_v_heads", ctypes.c_int32),
+                ("head_k_dim", ctypes.c_int32), ("head_v_dim", ctypes.c_int32),
+                ("conv_width", ctypes.c_int32)]
+
+
+@dataclass(frozen=True)
+class Dims:
+    Hk: int
+    Hv: int
+    dk: int
+    dv: int
+    W: int = 4
+
+    @property
+    def D(self) -> int:
+        return 2 * self.Hk * self.dk + self.Hv * self.dv
+
+    def c(self) -> gdn_dims:
+        return gdn_dims(self.Hk, self.Hv, self.dk, self.dv, self.W)
+
+
+_lib = None
+
+
+def lib():
+    """Load libgdn.so (raises if it is absent: build it with build.build_library())."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: the CUDA library must be built "
+                               "(gated_deltanet_linear_gdn_gb300.build.build_library())")
+        L = ctypes.CDLL(LIB_PATH)
+        P, I32, F = ctypes.c_void_p, ctypes.c_int32, ctypes.c_float
+        L.gdn_conv_update.restype = I32
+        L.gdn_conv_update.argtypes = [P, P, I32, I32, P, P, I32, P, I32, I32, I32, I32, P, P, P]
+        L.gdn_decode_step.restype = I32
+        L.gdn_decode_step.argtypes = [P, P, P, I32, P, P, P, P, I32, P, I32, I32, P, P, I32, I32,
+                                      gdn_dims, F, I32, P, I32, P, P]
+        L.gdn_chunked_prefill_workspace_size.restype = ctypes.c_size_t
+        L.gdn_chunked_prefill_workspace_size.argtypes = [I32, I32, gdn_dims, I32]
+        L.gdn_chunked_prefill.restype = I32
+        L.gdn_chunked_prefill.argtypes = [P, P, P, I32, P, P, P, P, I32, P, I32, I32, P, P, P, P,
+                                          I32, I32, I32, gdn_dims, F, I32, I32, P, I32, P,
+                                          ctypes.c_size_t, P, P]
+        L.gdn_validate_slots.restype = I32
+        L.gdn_validate_slots.argtypes = [P, I32, I32]
+        L.gdn_status_string.restype = ctypes.c_char_p
+        L.gdn_status_string.argtypes = [I32]
+        _lib = L
+    return _lib
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, torch.Tensor):
+        if t.numel() and not t.is_cuda:
+            raise ValueError("device tensors expected")
+        if t.numel() and not t.is_contiguous():
+            raise ValueError("contiguous tensors expected")
+        return ctypes.c_void_p(t.data_ptr()) if t.numel() else None
+    return ctypes.c_void_p(int(t))
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _dt(t) -> int:
+    if t.dtype == torch.bfloat16:
+        return GDN_BF16
+    if t.dtype == torch.float32:
+        return GDN_F32
+    raise ValueError(f"unsupported dtype {t.dtype}")
+
+
+def _check(status: int):
+    if status != GDN_OK:
+        raise GDNError(status, lib().gdn_status_string(status).decode())
+
+
+def status_string(status: int) -> str:
+    return lib().gdn_status_string(int(status)).decode()
+
+
+# --------------------------------------------------------------------------- entry points
+
+def gdn_conv_update(x, conv_state, weight, bias, slot, out, *, silu=True,
+                    conv_layout=GDN_CONV_DIM_FIRST, err=None, stream=None):
+    """Decode conv update (in place on conv_state). x, out: [B, D] bf16."""
+    B, D = x.shape
+    _check(lib().gdn_conv_update(_ptr(x), _ptr(conv_state), _dt(conv_state), int(conv_layout),
+                                 _ptr(weight), _ptr(bias), int(bool(silu)), _ptr(slot), B, D,
+                                 weight.shape[1], conv_state.shape[0], _ptr(out), _ptr(err),
+                                 _stream(stream)))
+
+
+def _gate_mode(a):
+    return GDN_GATE_DIRECT if a.dtype == torch.float32 else GDN_GATE_FUSED
+
+
+def gdn_decode_step(mixed_qkv, a, b, A_log, dt_bias, conv_weight, conv_bias, conv_state,
+                    ssm_state, slot, out, dims: Dims, *, silu=True,
+                    conv_layout=GDN_CONV_DIM_FIRST, scale=None, qk_l2norm=True, err=None,
+                    stream=None):
+    """One fused decode step (conv state and ssm_state updated in place).
+
+    a, b: bf16 [B, Hv] (fused gates with A_log, dt_bias) or f32 g, beta (direct)."""
+    B = mixed_qkv.shape[0]
+    scale = dims.dk ** -0.5 if scale is None else scale
+    conv_dt = _dt(conv_state) if conv_state is not None else GDN_BF16
+    _check(lib().gdn_decode_step(
+        _ptr(mixed_qkv), _ptr(a), _ptr(b), _gate_mode(a), _ptr(A_log), _ptr(dt_bias),
+        _ptr(conv_weight), _ptr(conv_bias), int(bool(silu)), _ptr(conv_state), conv_dt,
+        int(conv_layout), _ptr(ssm_state), _ptr(slot), B, ssm_state.shape[0], dims.c(),
+        float(scale), int(bool(qk_l2norm)), _ptr(out), _dt(out), _ptr(err), _stream(stream)))
+
+
+def gdn_chunked_prefill_workspace_size(total_tokens, num_seqs, dims: Dims, chunk=64) -> int:
+    return int(lib().gdn_chunked_prefill_workspace_size(int(total_tokens), int(num_seqs),
+                                                        dims.c(), int(chunk)))
+
+
+def gdn_chunked_prefill(mixed_qkv, a, b, A_log, dt_bias, conv_weight, conv_bias, conv_state,
+                        ssm_state, cu_seqlens, slot, has_initial_state, out, workspace,
+                        dims: Dims, *, chunk=64, silu=True, conv_layout=GDN_CONV_DIM_FIRST,
+                        scale=None, qk_l2norm=True, err=None, stream=None):
+    """Chunked prefill over packed sequences (states updated in place by slot)."""
+    T = mixed_qkv.shape[0]
+    N = slot.shape[0]
+    scale = dims.dk ** -0.5 if scale is None else scale
+    conv_dt = _dt(conv_state) if conv_state is not None else GDN_BF16
+    _check(lib().gdn_chunked_prefill(
+        _ptr(mixed_qkv), _ptr(a), _ptr(b), _gate_mode(a), _ptr(A_log), _ptr(dt_bias),
+        _ptr(conv_weight), _ptr(conv_bias), int(bool(silu)), _ptr(conv_state), conv_dt,
+        int(conv_layout), _ptr(ssm_state), _ptr(cu_seqlens), _ptr(slot),
+        _ptr(has_initial_state), N, T, ssm_state.shape[0], dims.c(), float(scale),
+        int(bool(qk_l2norm)), int(chunk), _ptr(out), _dt(out), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _ptr(err), _stream(stream)))
+
+
+def gdn_validate_slots(host_slot, num_slots) -> int:
+    """Host-side duplicate / range check of a host slot table (0 ok, 1 range, 2 repeat)."""
+    import numpy as np
+    s = np.ascontiguousarray(host_slot, dtype=np.int32)
+    return int(lib().gdn_validate_slots(s.ctypes.data_as(ctypes.c_void_p), s.size,
+                                        int(num_slots)))

@@ -1,0 +1,73 @@
+// gdn_internal.h -- launcher declarations shared between the C-ABI layer and
+// the kernel translation units. Host-only types; no torch.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "gdn.h"
+
+namespace gdn {
+
+constexpr int kConvWidth = 4;  // the only conv width with kernels
+
+struct ConvUpdateArgs {
+  const void* x;
+  void* conv_state;
+  int f32_cache;
+  int layout;
+  const void* weight;
+  const void* bias;
+  int silu;
+  const int32_t* slot;
+  int B, D, num_slots;
+  void* out;
+  int32_t* err;
+};
+
+struct LayerArgs {
+  const void* mixed;  // [T, D] bf16
+  const void* a;
+  const void* b;
+  int gate_mode;
+  const float* A_log;
+  const float* dt_bias;
+  const void* conv_w;  // null = conv bypass
+  const void* conv_b;
+  int silu;
+  void* conv_state;
+  int conv_f32;
+  int conv_layout;
+  float* ssm;  // [num_slots, Hv, dv, dk]
+  const int32_t* slot;
+  int num_slots;
+  int Hk, Hv, dk, dv, D;
+  float scale;
+  int qk_l2norm;
+  void* out;
+  int out_f32;
+  int32_t* err;
+};
+
+struct PrefillExtra {
+  const int32_t* cu_seqlens;
+  const uint8_t* has_init;
+  int num_seqs;
+  int total_tokens;
+  int chunk;
+  void* workspace;
+  size_t workspace_bytes;
+};
+
+cudaError_t launch_conv_update(const ConvUpdateArgs& a, cudaStream_t s);
+cudaError_t launch_decode(const LayerArgs& a, int B, cudaStream_t s);
+cudaError_t launch_prefill(const LayerArgs& a, const PrefillExtra& p, cudaStream_t s);
+size_t prefill_workspace_bytes(int total_tokens, int num_seqs, int Hk, int Hv, int dk, int dv,
+                               int chunk, int conv);
+
+// prefill helpers implemented in gdn_conv.cu
+cudaError_t launch_prefill_conv(const LayerArgs& a, const PrefillExtra& p, const int32_t* seq_ok,
+                                uint16_t* y, cudaStream_t s);
+
+}  // namespace gdn

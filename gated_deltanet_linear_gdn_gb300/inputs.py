@@ -209,3 +209,15 @@ def correlated_keys(T=64, seed=0, geo: Geometry = QWEN3_NEXT, eps=0.01) -> Layer
                        np.zeros(geo.Hv, np.float32), None, None, False, None, False, 0, ssm,
                        np.array([1], np.int32), cu, np.zeros(1, np.uint8),
                        float(geo.dk ** -0.5), True, {"seed": seed, "lengths": [T]})
+
+
+def device_state_pool(num_slots: int, geo: Geometry, std: float, seed: int, device="cuda"):
+    """fp32 state pool [num_slots, Hv, dv, dk] ~ N(0, std) drawn on the device (seeded torch
+    generator): for benchmark pools too large to draw on the host quickly."""
+    import torch
+
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed))
+    pool = torch.empty((num_slots, geo.Hv, geo.dv, geo.dk), dtype=torch.float32, device=device)
+    pool.normal_(0.0, float(std), generator=g)
+    return pool
