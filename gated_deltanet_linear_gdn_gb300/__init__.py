@@ -20,6 +20,8 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libgdn.so")
 
 GDN_OK, GDN_ERR_INVALID_ARG, GDN_ERR_UNSUPPORTED, GDN_ERR_CUDA = 0, 1, 2, 3
+GDN_ERR_SCRATCH_LIMIT = 4
+GDN_NOALLOC_SCRATCH_BYTES = 64 << 20
 GDN_BF16, GDN_F32 = 0, 1
 GDN_CONV_DIM_FIRST, GDN_CONV_TAP_FIRST = 0, 1
 GDN_GATE_FUSED, GDN_GATE_DIRECT = 0, 1
@@ -77,6 +79,10 @@ def lib():
         L.gdn_chunked_prefill.argtypes = [P, P, P, I32, P, P, P, P, I32, P, I32, I32, P, P, P, P,
                                           I32, I32, I32, gdn_dims, F, I32, I32, P, I32, P,
                                           ctypes.c_size_t, P, P]
+        L.gdn_chunked_prefill_noalloc.restype = I32
+        L.gdn_chunked_prefill_noalloc.argtypes = [P, P, P, I32, P, P, P, P, I32, P, I32, I32, P,
+                                                  P, P, P, I32, I32, I32, gdn_dims, F, I32, I32,
+                                                  P, I32, P, P]
         L.gdn_validate_slots.restype = I32
         L.gdn_validate_slots.argtypes = [P, I32, I32]
         L.gdn_status_string.restype = ctypes.c_char_p
@@ -174,6 +180,28 @@ def gdn_chunked_prefill(mixed_qkv, a, b, A_log, dt_bias, conv_weight, conv_bias,
         _ptr(has_initial_state), N, T, ssm_state.shape[0], dims.c(), float(scale),
         int(bool(qk_l2norm)), int(chunk), _ptr(out), _dt(out), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _ptr(err), _stream(stream)))
+
+
+def gdn_chunked_prefill_noalloc(mixed_qkv, a, b, A_log, dt_bias, conv_weight, conv_bias,
+                                conv_state, ssm_state, cu_seqlens, slot, has_initial_state, out,
+                                dims: Dims, *, chunk=64, silu=True,
+                                conv_layout=GDN_CONV_DIM_FIRST, scale=None, qk_l2norm=True,
+                                err=None, stream=None):
+    """gdn_chunked_prefill without a caller workspace, for callers that cannot allocate device
+    memory: the library's fixed GDN_NOALLOC_SCRATCH_BYTES array serves as the workspace.
+    Raises GDNError(GDN_ERR_SCRATCH_LIMIT) when the call needs more than that. Calls that may
+    overlap on the GPU share the array and race; make the first call on a device before any
+    stream capture."""
+    T = mixed_qkv.shape[0]
+    N = slot.shape[0]
+    scale = dims.dk ** -0.5 if scale is None else scale
+    conv_dt = _dt(conv_state) if conv_state is not None else GDN_BF16
+    _check(lib().gdn_chunked_prefill_noalloc(
+        _ptr(mixed_qkv), _ptr(a), _ptr(b), _gate_mode(a), _ptr(A_log), _ptr(dt_bias),
+        _ptr(conv_weight), _ptr(conv_bias), int(bool(silu)), _ptr(conv_state), conv_dt,
+        int(conv_layout), _ptr(ssm_state), _ptr(cu_seqlens), _ptr(slot),
+        _ptr(has_initial_state), N, T, ssm_state.shape[0], dims.c(), float(scale),
+        int(bool(qk_l2norm)), int(chunk), _ptr(out), _dt(out), _ptr(err), _stream(stream)))
 
 
 def gdn_validate_slots(host_slot, num_slots) -> int:

@@ -183,6 +183,9 @@ const char* gdn_status_string(gdn_status status) {
     case GDN_ERR_INVALID_ARG: return "GDN_ERR_INVALID_ARG: null pointer, bad size or misaligned buffer";
     case GDN_ERR_UNSUPPORTED: return "GDN_ERR_UNSUPPORTED: no kernel for this shape";
     case GDN_ERR_CUDA: return "GDN_ERR_CUDA: kernel launch failed";
+    case GDN_ERR_SCRATCH_LIMIT:
+      return "GDN_ERR_SCRATCH_LIMIT: the call needs more than the library's fixed scratch "
+             "(GDN_NOALLOC_SCRATCH_BYTES); use gdn_chunked_prefill with a workspace";
     default: return "unknown gdn_status";
   }
 }

@@ -55,7 +55,9 @@ typedef enum {
   GDN_OK = 0,
   GDN_ERR_INVALID_ARG = 1, /* a null pointer, a bad size or an inconsistent shape */
   GDN_ERR_UNSUPPORTED = 2, /* a valid shape this build has no kernel for */
-  GDN_ERR_CUDA = 3         /* the launch failed (cudaGetLastError != success) */
+  GDN_ERR_CUDA = 3,        /* the launch failed (cudaGetLastError != success) */
+  GDN_ERR_SCRATCH_LIMIT = 4 /* gdn_chunked_prefill_noalloc: the call needs more scratch
+                               than GDN_NOALLOC_SCRATCH_BYTES */
 } gdn_status;
 
 typedef enum { GDN_BF16 = 0, GDN_F32 = 1 } gdn_dtype;
@@ -192,6 +194,47 @@ gdn_status gdn_chunked_prefill(const void* mixed_qkv, const void* a, const void*
                                float scale, int32_t qk_l2norm, int32_t chunk, void* out,
                                gdn_dtype out_dtype, void* workspace, size_t workspace_bytes,
                                int32_t* err, void* stream);
+
+/*
+ * gdn_chunked_prefill_noalloc -- gdn_chunked_prefill for callers that cannot
+ * allocate device memory. The pages have no counterpart: this is a library
+ * convenience, not part of the method.
+ *
+ * Who needs it: code that may not call an allocator (cudaMalloc can
+ * synchronise the device, which a latency-critical host thread must not do), a
+ * plug-in inside a runtime that owns every device allocation, or a process
+ * that must keep a fixed device-memory footprint after start-up.
+ *
+ * It takes the same arguments as gdn_chunked_prefill minus the workspace: the
+ * workspace lives in a fixed array of GDN_NOALLOC_SCRATCH_BYTES bytes in the
+ * library's own device memory. The caller still owns and passes every input and
+ * output. Limits:
+ *   - every GPU on which the library is loaded holds that array until the
+ *     process exits;
+ *   - a call whose workspace (gdn_chunked_prefill_workspace_size) exceeds
+ *     GDN_NOALLOC_SCRATCH_BYTES returns GDN_ERR_SCRATCH_LIMIT and enqueues
+ *     nothing (64 MiB covers about 1100 tokens of the Qwen3-Next geometry
+ *     at chunk 64);
+ *   - all calls on a device share the array: calls that may run at the same
+ *     time on the GPU (streams without ordering between them) race on it;
+ *   - the first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress), which may load the module: make that first call
+ *     before any stream capture.
+ * Allocates nothing: no cudaMalloc, no cudaFree, no allocating library call.
+ */
+#define GDN_NOALLOC_SCRATCH_BYTES (64u << 20)
+
+gdn_status gdn_chunked_prefill_noalloc(const void* mixed_qkv, const void* a, const void* b,
+                                       gdn_gate_mode gate_mode, const float* A_log,
+                                       const float* dt_bias, const void* conv_weight,
+                                       const void* conv_bias, int32_t silu, void* conv_state,
+                                       gdn_dtype conv_dtype, gdn_conv_layout conv_layout,
+                                       float* ssm_state, const int32_t* cu_seqlens,
+                                       const int32_t* slot, const uint8_t* has_initial_state,
+                                       int32_t num_seqs, int32_t total_tokens, int32_t num_slots,
+                                       gdn_dims dims, float scale, int32_t qk_l2norm,
+                                       int32_t chunk, void* out, gdn_dtype out_dtype,
+                                       int32_t* err, void* stream);
 
 /*
  * gdn_validate_slots -- host-side check of a HOST slot table ([P1] Notes,
