@@ -225,9 +225,13 @@ def run_ours(args, rank, world):
 
     # ---- chunked prefill ----
     prefill = {}
+    cases = [(f"single_{args.prefill_tokens}_bypass",
+              lambda: gi.prefill_single(args.prefill_tokens, seed=0))]
+    if not args.no_varlen:
+        cases.append(("varlen_8seq_conv", lambda: gi.prefill_varlen(8, 8192, seed=0)))
     if not args.no_prefill:
-        for name, inp in (("single_4096_bypass", gi.prefill_single(4096, seed=0)),
-                          ("varlen_8seq_conv", gi.prefill_varlen(8, 8192, seed=0))):
+        for name, make in cases:
+            inp = make()
             T, N = inp.total_tokens, inp.slot.size
             tt = dict(
                 mixed=b16(inp.mixed).to(dev), a=b16(inp.a).to(dev), b=b16(inp.b).to(dev),
@@ -259,7 +263,7 @@ def run_ours(args, rank, world):
         torch.cuda.empty_cache()
 
     # ---- e2e through the public API with pinned host buffers ----
-    t = decode_setup(HEADLINE_B, NUM_SLOTS, seed=HEADLINE_B)
+    t = decode_setup(args.batch, args.num_slots, seed=args.batch)
     h_mixed = t["mixed"].cpu().pin_memory()
     h_a, h_b = t["a"].cpu().pin_memory(), t["b"].cpu().pin_memory()
     h_slot = t["slot"].cpu().pin_memory()
@@ -278,7 +282,7 @@ def run_ours(args, rank, world):
     d2h = h_out.numel() * h_out.element_size()
 
     # ---- headline: exactly K timed decode steps ----
-    nbytes = decode_bytes(HEADLINE_B, geo)
+    nbytes = decode_bytes(args.batch, geo)
     if world > 1:
         import torch.distributed as dist
         dist.barrier()
@@ -306,9 +310,9 @@ def run_ours(args, rank, world):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic",
         "config": {"workload": "GDN decode step, Qwen3-Next geometry Hk=16 Hv=32 dk=dv=128 "
-                               "D=8192 W=4, B=256 rows over 512 shuffled slots, bf16 conv cache, "
-                               "fp32 state, bf16 I/O",
-                   "batch": HEADLINE_B, "num_slots": NUM_SLOTS,
+                               f"D=8192 W=4, B={args.batch} rows over {args.num_slots} shuffled "
+                               "slots, bf16 conv cache, fp32 state, bf16 I/O",
+                   "batch": args.batch, "num_slots": args.num_slots,
                    "bytes_per_step": nbytes, "l2": "flushed between timed steps (512 MiB write)"},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
@@ -421,6 +425,11 @@ def main():
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--batch", type=int, default=HEADLINE_B, help="headline decode rows")
+    ap.add_argument("--num-slots", type=int, default=NUM_SLOTS, help="headline slot pool size")
+    ap.add_argument("--prefill-tokens", type=int, default=4096,
+                    help="length of the single-sequence prefill case")
+    ap.add_argument("--no-varlen", action="store_true", help="skip the ~32k-token varlen case")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
