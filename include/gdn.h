@@ -85,6 +85,8 @@ typedef struct {
  * bits into it with plain stores). */
 #define GDN_DEVERR_SLOT_RANGE 1 /* an active slot >= num_slots */
 #define GDN_DEVERR_SEQLENS 2    /* cu_seqlens not non-decreasing or not ending at total_tokens */
+#define GDN_DEVERR_TIMEOUT 4    /* a bounded wait for an asynchronous copy gave up (the
+                                   affected rows are left unprocessed) */
 
 /*
  * gdn_conv_update -- one decode step of the causal depthwise conv1d ([P1]
