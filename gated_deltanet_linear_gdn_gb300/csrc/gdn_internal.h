@@ -66,6 +66,15 @@ cudaError_t launch_prefill(const LayerArgs& a, const PrefillExtra& p, cudaStream
 size_t prefill_workspace_bytes(int total_tokens, int num_seqs, int Hk, int Hv, int dk, int dv,
                                int chunk, int conv);
 
+// chunk table + sequence checks (gdn_prefill.cu): meta[0] = number of chunks,
+// seq_ok[i], chunk_off[N+1] (first chunk of each sequence), chunk_seq[chunk]
+cudaError_t launch_prefill_prep(const LayerArgs& a, const PrefillExtra& p, int32_t* meta,
+                                int32_t* seq_ok, int32_t* chunk_off, int32_t* chunk_seq,
+                                cudaStream_t s);
+// tensor-core path for dk = dv = 128 (gdn_prefill_tc.cu)
+size_t prefill_tc_workspace_bytes(int total_tokens, int num_seqs, int Hk, int Hv, int chunk);
+cudaError_t launch_prefill_tc(const LayerArgs& a, const PrefillExtra& p, cudaStream_t s);
+
 // prefill helpers implemented in gdn_conv.cu
 cudaError_t launch_prefill_conv(const LayerArgs& a, const PrefillExtra& p, const int32_t* seq_ok,
                                 uint16_t* y, cudaStream_t s);

@@ -454,8 +454,16 @@ cudaError_t launch_prefill_dk(const LayerArgs& a, const PrefillExtra& p, cudaStr
 
 }  // namespace
 
+cudaError_t launch_prefill_prep(const LayerArgs& a, const PrefillExtra& p, int32_t* meta,
+                                int32_t* seq_ok, int32_t* chunk_off, int32_t* chunk_seq,
+                                cudaStream_t s) {
+  prep_kernel<<<1, 256, 0, s>>>(a, p, meta, seq_ok, chunk_off, chunk_seq);
+  return cudaGetLastError();
+}
+
 size_t prefill_workspace_bytes(int total_tokens, int num_seqs, int Hk, int Hv, int dk, int dv,
                                int chunk, int conv) {
+  if (dk == 128 && dv == 128) return prefill_tc_workspace_bytes(total_tokens, num_seqs, Hk, Hv, chunk);
   const int D = 2 * Hk * dk + Hv * dv;
   return ws_layout(total_tokens, num_seqs, Hv, dk, dv, chunk, conv, D).total;
 }
@@ -464,7 +472,7 @@ cudaError_t launch_prefill(const LayerArgs& a, const PrefillExtra& p, cudaStream
   switch (a.dk) {
     case 32: return launch_prefill_dk<32>(a, p, s);
     case 64: return launch_prefill_dk<64>(a, p, s);
-    case 128: return launch_prefill_dk<128>(a, p, s);
+    case 128: return a.dv == 128 ? launch_prefill_tc(a, p, s) : launch_prefill_dk<128>(a, p, s);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -1,0 +1,777 @@
+// gdn_prefill_tc.cu -- chunked (UT/WY) prefill of the gated delta rule on the
+// 5th-generation tensor cores (tcgen05, accumulators in tensor memory), for
+// dk = dv = 128 (the Qwen3-Next head size).
+//
+// Source: vLLM PR #53864 (CuteDSL GDN prefill), "Numerical root cause and
+// fix": the prefill forms the per-chunk KK^T block and inverts the unit
+// lower-triangular matrix built from it; a bf16 Newton-Schulz inverse fails on
+// correlated keys. Here that inverse is solved EXACTLY in fp32 (forward
+// substitution, one column per thread), and every contraction runs on the
+// tensor cores with fp32 accumulation.
+//
+// Algebra per chunk of C tokens starting from state S0 (G_t = running sum of g
+// inside the chunk, raw bf16 q, k, v, inverse norms iq_t, ik_t):
+//   A_tj = beta_t e^(G_t - G_j) ik_t ik_j (k_t . k_j),  j < t;  T = (I + A)^-1
+//   U = T diag(beta) V                    W = T diag(beta e^G ik) K
+//   P_tj = e^(G_t - G_j) iq_t scale ik_j (q_t . k_j),  j <= t
+//   D = U - W S0^T,   O = diag(e^G iq scale) Q S0^T + P D
+//   S_end = e^(G_last) S0 + D^T diag(e^(G_last - G_j) ik_j) K
+// (the same identity as the CUDA-core path; unrolling the rule inside a chunk).
+//
+// Precision: raw q, k, v are bf16 and enter the tensor cores exactly. Every
+// fp32 operand (T diag(beta), the state S, W, P, D) is split into bf16 hi + lo
+// (x = hi + lo to ~2^-17) and a product of two split operands takes three MMAs
+// (hi*hi + hi*lo + lo*hi), one split and one exact operand two. The error per
+// product is ~1e-5 relative, well inside the prefill bound.
+//
+// Kernels (after the shared prep and conv):
+//   intra (chunks packed 128/C per CTA, k-head): KK^T and QK^T for 128 token
+//       rows at once (M = N = 128; the diagonal CxC blocks are the chunks'),
+//       then per value head: gates, A and P rows from tensor memory, the fp32
+//       triangular solve, U and W as MMAs with a block-diagonal T. Writes the
+//       pass's operand tiles, already in tensor-core layout, to workspace.
+//   pass (sequence, value head): the state S lives in registers (a thread owns
+//       half a row); per chunk, bulk copies bring the chunk's tiles into shared
+//       memory, MMA group 1 forms D^T (= U^T - S W^T) and S Q^T, MMA group 2
+//       forms D^T P^T and the state update D'^T K; M = dv = 128 throughout.
+// Every wait is bounded (GDN_DEVERR_TIMEOUT on expiry, the CTA stops cleanly
+// and frees its tensor memory).
+#include "gdn_common.cuh"
+#include "gdn_internal.h"
+#include "gdn_ptx.cuh"
+#include "gdn_tc.cuh"
+
+namespace gdn {
+
+namespace {
+
+constexpr int kD = 128;          // dk = dv
+constexpr int kThreadsTc = 256;  // 8 warps: warp w reads tensor-memory lanes 32 (w % 4) ..
+constexpr uint32_t kTmemCols = 512;
+constexpr int kVecFloats = 256;  // per (chunk, head): f[C], dd[C], g_last
+
+struct TcLayout {
+  size_t meta, seq_ok, chunk_off, chunk_seq, ybuf, Qt, Kt, Wt, Pt, Ut, vec, total;
+  int max_chunks;
+  // per-tile byte sizes
+  size_t q_tile, w_tile, p_tile, u_tile;
+};
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+TcLayout tc_layout(int T, int N, int Hk, int Hv, int C, int D) {
+  TcLayout L;
+  const int64_t mc = (static_cast<int64_t>(T) + static_cast<int64_t>(N) * (C - 1)) / C;
+  L.max_chunks = static_cast<int>(mc);
+  L.q_tile = static_cast<size_t>(C) * kD * 2;  // bf16 [C x 128] (also K^T [128 x C])
+  L.w_tile = static_cast<size_t>(C) * kD * 2;  // one of hi / lo
+  L.p_tile = static_cast<size_t>(C) * C * 2;   // one of hi / lo
+  L.u_tile = static_cast<size_t>(kD) * C * 4;  // fp32 U^T [128 x C]
+  size_t off = 0;
+  L.meta = off; off = align256(off + 16 * sizeof(int32_t));
+  L.seq_ok = off; off = align256(off + static_cast<size_t>(N) * sizeof(int32_t));
+  L.chunk_off = off; off = align256(off + static_cast<size_t>(N + 1) * sizeof(int32_t));
+  L.chunk_seq = off; off = align256(off + static_cast<size_t>(mc + 1) * sizeof(int32_t));
+  L.ybuf = off; off = align256(off + static_cast<size_t>(T) * D * sizeof(uint16_t));
+  L.Qt = off; off = align256(off + static_cast<size_t>(mc) * Hk * L.q_tile);
+  L.Kt = off; off = align256(off + static_cast<size_t>(mc) * Hk * L.q_tile);
+  L.Wt = off; off = align256(off + static_cast<size_t>(mc) * Hv * 2 * L.w_tile);
+  L.Pt = off; off = align256(off + static_cast<size_t>(mc) * Hv * 2 * L.p_tile);
+  L.Ut = off; off = align256(off + static_cast<size_t>(mc) * Hv * L.u_tile);
+  L.vec = off; off = align256(off + static_cast<size_t>(mc) * Hv * kVecFloats * 4);
+  L.total = off;
+  return L;
+}
+
+struct TcBufs {
+  unsigned char* Qt;  // [chunk][Hk] bf16 q tile, K-major [C x 128]
+  unsigned char* Kt;  // [chunk][Hk] bf16 k^T tile, K-major [128 x C]
+  unsigned char* Wt;  // [chunk][Hv][hi, lo] bf16 W tile, K-major [C x 128]
+  unsigned char* Pt;  // [chunk][Hv][hi, lo] bf16 P tile, K-major [C x C]
+  float* Ut;          // [chunk][Hv] fp32 U^T, [128][C]
+  float* vec;         // [chunk][Hv][256]: f[0..C), dd[64..64+C), g_last at [128]
+  size_t q_tile, w_tile, p_tile;
+};
+
+__device__ __forceinline__ void split8(const float (&x)[8], uint4& hi, uint4& lo) {
+  uint16_t h[8], l[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) tc::split_bf16(x[i], h[i], l[i]);
+  hi = pack8(h);
+  lo = pack8(l);
+}
+
+template <int N>
+__device__ __forceinline__ void tmem_load(uint32_t addr, float (&v)[N]);
+template <>
+__device__ __forceinline__ void tmem_load<8>(uint32_t addr, float (&v)[8]) { tc::tmem_ld8(addr, v); }
+template <>
+__device__ __forceinline__ void tmem_load<16>(uint32_t addr, float (&v)[16]) { tc::tmem_ld16(addr, v); }
+
+// sync point between tensor-core work and threads: smem writes -> async proxy,
+// tensor-memory reads done, CTA barrier. Returns true if any thread flagged `bad`.
+__device__ __forceinline__ bool tc_sync(bool bad) {
+  tc::fence_async_smem();
+  tc::fence_before_sync();
+  const int any = __syncthreads_or(bad ? 1 : 0);
+  tc::fence_after_sync();
+  return any != 0;
+}
+
+// ============================================================== intra kernel
+template <int C>
+struct IntraSmem {
+  static constexpr int CPC = 128 / C;                // chunks per CTA
+  static constexpr int kTile = 128 * 128 * 2;        // bf16 [128 x 128]
+  // phase 1: sQ, sK (MMA operands), sKtw (k^T tiles for the workspace)
+  // phase 2: sKh, sKl (alias sQ, sK), sTh (aliases sKtw), sTl, sVt, sA
+  static constexpr int oQ = 0, oK = kTile, oKtw = 2 * kTile;
+  static constexpr int oTh = 2 * kTile, oTl = 3 * kTile, oVt = 4 * kTile;
+  static constexpr int oA = 5 * kTile;               // fp32 [128][C+1]
+  static constexpr int oVec = oA + 128 * (C + 1) * 4;  // iq, ik, g/G, beta: 4 x 128 floats
+  static constexpr int kBytes = oVec + 4 * 128 * 4;
+};
+
+template <int C>
+__global__ void __launch_bounds__(kThreadsTc, 1)
+    intra_tc_kernel(LayerArgs a, PrefillExtra p, const uint16_t* __restrict__ y,
+                    const int32_t* meta, const int32_t* chunk_off, const int32_t* chunk_seq,
+                    TcBufs wb) {
+  using S = IntraSmem<C>;
+  constexpr int CPC = S::CPC;
+  extern __shared__ __align__(1024) unsigned char sm[];
+  float* sA = reinterpret_cast<float*>(sm + S::oA);
+  float* s_iq = reinterpret_cast<float*>(sm + S::oVec);
+  float* s_ik = s_iq + 128;
+  float* s_G = s_ik + 128;
+  float* s_beta = s_G + 128;
+  __shared__ int s_t0[CPC], s_L[CPC];
+  __shared__ uint32_t s_tmem;
+  __shared__ __align__(8) uint64_t s_bar;
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int kh = blockIdx.y;
+  const int nchunks = meta[0];
+  const int c_first = blockIdx.x * CPC;
+  if (c_first >= nchunks) return;  // no chunk of this CTA exists
+  if (tid < CPC) {
+    const int c = c_first + tid;
+    int t0 = 0, L = 0;
+    if (c < nchunks) {
+      const int i = chunk_seq[c];
+      t0 = p.cu_seqlens[i] + (c - chunk_off[i]) * C;
+      L = min(C, p.cu_seqlens[i + 1] - t0);
+    }
+    s_t0[tid] = t0;
+    s_L[tid] = L;
+  }
+  __syncthreads();
+
+  // ---- phase 1: raw q, k rows -> tensor-core tiles; norms; k^T tiles ----
+  {
+    const int tok = tid & 127, which = tid >> 7;  // 0: q, 1: k
+    const int ci = tok / C, tl = tok % C;
+    const bool valid = tl < s_L[ci];
+    const int col0 = which ? (a.Hk + kh) * kD : kh * kD;
+    unsigned char* tile = sm + (which ? S::oK : S::oQ);
+    const uint16_t* row = y + static_cast<int64_t>(s_t0[ci] + tl) * a.D + col0;
+    float ss = 0.0f;
+#pragma unroll 4
+    for (int k8 = 0; k8 < kD / 8; ++k8) {
+      uint4 v = make_uint4(0u, 0u, 0u, 0u);
+      if (valid) v = __ldg(reinterpret_cast<const uint4*>(row) + k8);
+      float f[8];
+      unpack8(v, f);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) ss = fmaf(f[e], f[e], ss);
+      *reinterpret_cast<uint4*>(tile + tc::kmajor_offset(tok, 8 * k8, kD)) = v;
+      if (which) {  // k^T tile of this chunk: element (channel, tl)
+        const uint16_t* hv = reinterpret_cast<const uint16_t*>(&v);
+        unsigned char* kt = sm + S::oKtw + ci * (kD * C * 2);
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+          *reinterpret_cast<uint16_t*>(kt + tc::kmajor_offset(8 * k8 + e, tl, C)) = hv[e];
+      }
+    }
+    const float inv = a.qk_l2norm ? 1.0f / sqrtf(ss + 1e-6f) : 1.0f;
+    (which ? s_ik : s_iq)[tok] = inv;
+  }
+  if (warp == 0) tc::tmem_alloc(&s_tmem, kTmemCols);
+  if (tid == 0) {
+    mbar_init(smem_addr(&s_bar), 1);
+    fence_mbar_init();
+  }
+  tc_sync(false);
+  const uint32_t tb = s_tmem;
+  uint32_t phase = 0;
+  bool bad = false;
+
+  if (tid == 0) {  // G = K K^T (cols 0..127), QK = Q K^T (cols 128..255)
+    const uint32_t id = tc::idesc_bf16_f32(128, 128);
+    const uint32_t aq = smem_addr(sm + S::oQ), ak = smem_addr(sm + S::oK);
+    for (int ks = 0; ks < kD / 16; ++ks)
+      tc::mma_bf16(tb, tc::kmajor_desc(ak, kD, ks), tc::kmajor_desc(ak, kD, ks), id, ks > 0);
+    for (int ks = 0; ks < kD / 16; ++ks)
+      tc::mma_bf16(tb + 128, tc::kmajor_desc(aq, kD, ks), tc::kmajor_desc(ak, kD, ks), id, ks > 0);
+    tc::mma_commit(smem_addr(&s_bar));
+  }
+  // q and k^T tiles of each chunk -> workspace (read-only use of the smem tiles)
+  for (int ci = 0; ci < CPC; ++ci) {
+    const int c = c_first + ci;
+    if (c >= nchunks) break;
+    const size_t slice = static_cast<size_t>(C) * kD * 2;  // bytes of one chunk's tile
+    const uint4* srcq = reinterpret_cast<const uint4*>(sm + S::oQ + ci * slice);
+    const uint4* srck = reinterpret_cast<const uint4*>(sm + S::oKtw + ci * slice);
+    uint4* dq = reinterpret_cast<uint4*>(wb.Qt + (static_cast<size_t>(c) * a.Hk + kh) * wb.q_tile);
+    uint4* dk = reinterpret_cast<uint4*>(wb.Kt + (static_cast<size_t>(c) * a.Hk + kh) * wb.q_tile);
+    for (int i = tid; i < static_cast<int>(slice / 16); i += kThreadsTc) {
+      dq[i] = srcq[i];
+      dk[i] = srck[i];
+    }
+  }
+  if (!mbar_wait_bounded(smem_addr(&s_bar), phase)) bad = true;
+  phase ^= 1;
+  bad = tc_sync(bad);
+
+  // ---- phase 2: per value head ----
+  if (!bad) {
+    for (int i = tid; i < 2 * S::kTile / 16; i += kThreadsTc)  // block-diagonal T: zero all
+      reinterpret_cast<uint4*>(sm + S::oTh)[i] = make_uint4(0u, 0u, 0u, 0u);
+  }
+  const int R = a.Hv / a.Hk;
+  for (int hr = 0; hr < R && !bad; ++hr) {
+    const int h = kh * R + hr;
+    // gates of the 128 token rows, then the running sums per chunk
+    if (tid < 128) {
+      const int ci = tid / C, tl = tid % C;
+      float g = 0.0f, be = 0.0f;
+      if (tl < s_L[ci])
+        gate_log(a.a, a.b, a.gate_mode, a.A_log, a.dt_bias,
+                 static_cast<int64_t>(s_t0[ci] + tl) * a.Hv + h, h, g, be);
+      s_G[tid] = g;
+      s_beta[tid] = be;
+    }
+    __syncthreads();
+    if (tid < CPC) {
+      float run = 0.0f;
+      for (int t = 0; t < C; ++t) { run += s_G[tid * C + t]; s_G[tid * C + t] = run; }
+    }
+    __syncthreads();
+
+    // A and P rows from tensor memory. Thread: row t, column half `half`.
+    {
+      const int t = 32 * (warp & 3) + lane, half = warp >> 2;
+      const int ci = t / C, tl = t % C;
+      const int c = c_first + ci;
+      const bool live = c < nchunks && tl < s_L[ci];
+      const float Gt = s_G[t], bt = s_beta[t], ikt = s_ik[t], iqt = s_iq[t] * a.scale;
+      constexpr int NH = C / 2;  // columns per thread
+      // tcgen05.ld is warp-collective with one column address per warp, so the
+      // columns must not depend on the lane: for C >= 32 the warp's 32 rows lie
+      // in one chunk; for C = 16 they span two chunks, both are loaded and each
+      // lane keeps its own.
+      float gv[NH], qv[NH];
+      if constexpr (C >= 32) {
+        const int cw = (32 * (warp & 3)) / C;  // the warp's chunk
+#pragma unroll
+        for (int b0 = 0; b0 < NH; b0 += 16) {
+          float tg[16], tq[16];
+          tmem_load<16>(tc::taddr(tb, 32 * (warp & 3), cw * C + half * NH + b0), tg);
+          tmem_load<16>(tc::taddr(tb, 32 * (warp & 3), 128 + cw * C + half * NH + b0), tq);
+#pragma unroll
+          for (int e = 0; e < 16; ++e) { gv[b0 + e] = tg[e]; qv[b0 + e] = tq[e]; }
+        }
+      } else {
+        const int col0 = 32 * (warp & 3) + half * NH;  // chunk 2q's half; +16: chunk 2q+1
+        float ga[8], gb[8], qa[8], qb[8];
+        tmem_load<8>(tc::taddr(tb, 32 * (warp & 3), col0), ga);
+        tmem_load<8>(tc::taddr(tb, 32 * (warp & 3), col0 + 16), gb);
+        tmem_load<8>(tc::taddr(tb, 32 * (warp & 3), 128 + col0), qa);
+        tmem_load<8>(tc::taddr(tb, 32 * (warp & 3), 128 + col0 + 16), qb);
+        const bool second = lane >= 16;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          gv[e] = second ? gb[e] : ga[e];
+          qv[e] = second ? qb[e] : qa[e];
+        }
+      }
+      tc::tmem_wait_ld();
+      float pv[NH];
+#pragma unroll
+      for (int e = 0; e < NH; ++e) {
+        const int j = half * NH + e;
+        const int tj = ci * C + j;
+        const float dec = (live && j <= tl) ? expf(Gt - s_G[tj]) : 0.0f;
+        sA[t * (C + 1) + j] = (j < tl) ? bt * dec * ikt * s_ik[tj] * gv[e] : 0.0f;
+        pv[e] = dec * iqt * s_ik[tj] * qv[e];
+      }
+      if (c < nchunks) {
+        unsigned char* ph = wb.Pt + (static_cast<size_t>(c) * a.Hv + h) * 2 * wb.p_tile;
+#pragma unroll
+        for (int e8 = 0; e8 < NH; e8 += 8) {
+          float x[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) x[e] = pv[e8 + e];
+          uint4 hi, lo;
+          split8(x, hi, lo);
+          const uint32_t o = tc::kmajor_offset(tl, half * NH + e8, C);
+          *reinterpret_cast<uint4*>(ph + o) = hi;
+          *reinterpret_cast<uint4*>(ph + wb.p_tile + o) = lo;
+        }
+        if (half == 0) {
+          float* vec = wb.vec + (static_cast<size_t>(c) * a.Hv + h) * kVecFloats;
+          const float Glast = s_G[ci * C + max(s_L[ci] - 1, 0)];
+          vec[tl] = live ? expf(Gt) * iqt : 0.0f;            // f_t
+          vec[64 + tl] = live ? expf(Glast - Gt) * ikt : 0.0f;  // dd_t
+          if (tl == 0) vec[128] = expf(Glast);               // g_last
+        }
+      }
+    }
+    __syncthreads();
+
+    if (tid < 128) {
+      // exact fp32 forward substitution for column j of T = (I + A)^-1 (one chunk)
+      const int ci = tid / C, j = tid % C;
+      const float* Ab = sA + ci * C * (C + 1);
+      float Tc[C];
+#pragma unroll
+      for (int r = 0; r < C; ++r) {
+        float s0 = 0.0f, s1 = 0.0f;
+#pragma unroll
+        for (int l = 0; l < r; l += 2) {
+          s0 = fmaf(Ab[r * (C + 1) + l], Tc[l], s0);
+          if (l + 1 < r) s1 = fmaf(Ab[r * (C + 1) + l + 1], Tc[l + 1], s1);
+        }
+        Tc[r] = (r < j) ? 0.0f : (r == j ? 1.0f : -(s0 + s1));
+      }
+      // T' = T diag(beta) into the block-diagonal bf16 hi / lo tiles
+      const float bj = s_beta[ci * C + j];
+#pragma unroll
+      for (int r = 0; r < C; ++r) {
+        uint16_t hi, lo;
+        tc::split_bf16(Tc[r] * bj, hi, lo);
+        const uint32_t o = tc::kmajor_offset(ci * C + r, ci * C + j, 128);
+        *reinterpret_cast<uint16_t*>(sm + S::oTh + o) = hi;
+        *reinterpret_cast<uint16_t*>(sm + S::oTl + o) = lo;
+      }
+    } else {
+      // V^T (raw bf16) and K'^T = (diag(e^G ik) K)^T (split) as [128 x 128 tokens] operands
+      const int u = tid - 128;
+      const int vc = 2 * a.Hk * kD + h * kD, kc = (a.Hk + kh) * kD;
+      for (int item = u; item < 128 * 16; item += 128) {
+        const int r = item & 127, tg = item >> 7;  // channel r, tokens 8 tg .. 8 tg + 7
+        uint16_t hv[8];
+        float kx[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const int tok = 8 * tg + e, ci = tok / C, tl = tok % C;
+          const bool valid = tl < s_L[ci];
+          const uint16_t* rowp = y + static_cast<int64_t>(s_t0[ci] + tl) * a.D;
+          hv[e] = valid ? rowp[vc + r] : static_cast<uint16_t>(0);
+          kx[e] = valid ? bf2f(rowp[kc + r]) * (expf(s_G[tok]) * s_ik[tok]) : 0.0f;
+        }
+        const uint32_t o = tc::kmajor_offset(r, 8 * tg, 128);
+        *reinterpret_cast<uint4*>(sm + S::oVt + o) = pack8(hv);
+        uint4 hi, lo;
+        split8(kx, hi, lo);
+        *reinterpret_cast<uint4*>(sm + S::oQ + o) = hi;  // sKh (aliases sQ)
+        *reinterpret_cast<uint4*>(sm + S::oK + o) = lo;  // sKl (aliases sK)
+      }
+    }
+    bad = tc_sync(bad);
+    if (bad) break;
+
+    if (tid == 0) {  // U = T' V (cols 256..383), W = T' K' (cols 384..511)
+      const uint32_t id = tc::idesc_bf16_f32(128, 128);
+      const uint32_t th = smem_addr(sm + S::oTh), tl = smem_addr(sm + S::oTl);
+      const uint32_t vt = smem_addr(sm + S::oVt);
+      const uint32_t kh_ = smem_addr(sm + S::oQ), kl = smem_addr(sm + S::oK);
+      for (int ks = 0; ks < 8; ++ks)
+        tc::mma_bf16(tb + 256, tc::kmajor_desc(th, 128, ks), tc::kmajor_desc(vt, 128, ks), id, ks > 0);
+      for (int ks = 0; ks < 8; ++ks)
+        tc::mma_bf16(tb + 256, tc::kmajor_desc(tl, 128, ks), tc::kmajor_desc(vt, 128, ks), id, 1);
+      for (int ks = 0; ks < 8; ++ks)
+        tc::mma_bf16(tb + 384, tc::kmajor_desc(th, 128, ks), tc::kmajor_desc(kh_, 128, ks), id, ks > 0);
+      for (int ks = 0; ks < 8; ++ks)
+        tc::mma_bf16(tb + 384, tc::kmajor_desc(th, 128, ks), tc::kmajor_desc(kl, 128, ks), id, 1);
+      for (int ks = 0; ks < 8; ++ks)
+        tc::mma_bf16(tb + 384, tc::kmajor_desc(tl, 128, ks), tc::kmajor_desc(kh_, 128, ks), id, 1);
+      tc::mma_commit(smem_addr(&s_bar));
+    }
+    if (!mbar_wait_bounded(smem_addr(&s_bar), phase)) bad = true;
+    bad = __any_sync(0xffffffffu, bad);  // warp-uniform before the aligned loads
+    phase ^= 1;
+    tc::fence_after_sync();
+    if (!bad) {
+      // U^T -> workspace (fp32 [128][C]); W -> hi / lo tiles [C x 128]. Every lane
+      // executes the (warp-collective) loads; only rows of existing chunks store.
+      const int t = 32 * (warp & 3) + lane, half = warp >> 2;
+      const int ci = t / C, tl = t % C;
+      const int c = c_first + ci;
+      const bool store = c < nchunks;
+      {
+        float* ut = wb.Ut + (static_cast<size_t>(store ? c : 0) * a.Hv + h) * (kD * C);
+        unsigned char* wt = wb.Wt + (static_cast<size_t>(store ? c : 0) * a.Hv + h) * 2 * wb.w_tile;
+#pragma unroll 1
+        for (int b0 = 0; b0 < 64; b0 += 16) {
+          const int col = half * 64 + b0;
+          float uv[16], wv[16];
+          tmem_load<16>(tc::taddr(tb, 32 * (warp & 3), 256 + col), uv);
+          tmem_load<16>(tc::taddr(tb, 32 * (warp & 3), 384 + col), wv);
+          tc::tmem_wait_ld();
+          if (!store) continue;
+#pragma unroll
+          for (int e = 0; e < 16; ++e) ut[(col + e) * C + tl] = uv[e];
+#pragma unroll
+          for (int e8 = 0; e8 < 16; e8 += 8) {
+            float x[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) x[e] = wv[e8 + e];
+            uint4 hi, lo;
+            split8(x, hi, lo);
+            const uint32_t o = tc::kmajor_offset(tl, col + e8, 128);
+            *reinterpret_cast<uint4*>(wt + o) = hi;
+            *reinterpret_cast<uint4*>(wt + wb.w_tile + o) = lo;
+          }
+        }
+      }
+    }
+    bad = tc_sync(bad);
+  }
+  if (bad && tid == 0 && a.err) atomicOr(a.err, GDN_DEVERR_TIMEOUT);
+  tc_sync(false);
+  if (warp == 0) tc::tmem_dealloc(tb, kTmemCols);
+}
+
+// ============================================================== pass kernel
+template <int C>
+struct PassSmem {
+  static constexpr int kS = 128 * 128 * 2;      // S hi / lo  [128 x 128] bf16
+  static constexpr int kD_ = 128 * C * 2;       // D^T tiles  [128 x C]   bf16
+  static constexpr int kW = C * 128 * 2;        // W, Q tiles [C x 128]   bf16
+  static constexpr int kP = C * C * 2;          // P tiles    [C x C]     bf16
+  static constexpr int oSh = 0, oSl = kS;
+  static constexpr int oDh = 2 * kS, oDl = oDh + kD_, oEh = oDl + kD_, oEl = oEh + kD_;
+  static constexpr int oWh = oEl + kD_, oWl = oWh + kW, oQ = oWl + kW;
+  static constexpr int oPh = oQ + kW, oPl = oPh + kP, oKt = oPl + kP;
+  static constexpr int oVec = oKt + kD_;        // two vec buffers of kVecFloats
+  static constexpr int kBytes = oVec + 2 * kVecFloats * 4;
+};
+
+template <int C>
+__global__ void __launch_bounds__(kThreadsTc, 1)
+    pass_tc_kernel(LayerArgs a, PrefillExtra p, const int32_t* seq_ok, const int32_t* chunk_off,
+                   TcBufs wb) {
+  using S = PassSmem<C>;
+  extern __shared__ __align__(1024) unsigned char sm[];
+  __shared__ uint32_t s_tmem;
+  __shared__ __align__(8) uint64_t s_bar[4];  // fullA, fullB, mma1, mma2
+
+  const int i = blockIdx.x, h = blockIdx.y;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int bos = p.cu_seqlens[i], eos = p.cu_seqlens[i + 1];
+  if (!seq_ok[i]) {  // inactive / invalid sequence (or bad cu_seqlens): zero outputs
+    int64_t n = static_cast<int64_t>(max(eos - bos, 0));
+    if (bos < 0 || eos > p.total_tokens) n = 0;
+    for (int64_t idx = tid; idx < n * kD; idx += kThreadsTc) {
+      const int64_t o = ((bos + idx / kD) * a.Hv + h) * kD + idx % kD;
+      if (a.out_f32) static_cast<float*>(a.out)[o] = 0.0f;
+      else static_cast<uint16_t*>(a.out)[o] = 0;
+    }
+    return;
+  }
+  const int c0 = chunk_off[i], nch = chunk_off[i + 1] - c0;
+  const int32_t slot = a.slot[i];
+  const bool init = (p.has_init == nullptr) || (p.has_init[i] != 0);
+  const int q = warp & 3, half = warp >> 2;
+  const int r = 32 * q + lane;  // state row (dv index) = tensor-memory lane
+  const uint32_t fullA = smem_addr(&s_bar[0]), fullB = smem_addr(&s_bar[1]);
+  const uint32_t mma1 = smem_addr(&s_bar[2]), mma2 = smem_addr(&s_bar[3]);
+  const size_t wtile = wb.w_tile, ptile = wb.p_tile;
+
+  auto issue_A = [&](int it) {  // W hi/lo, q tile, vec of chunk c0 + it
+    const int c = c0 + it;
+    const int kh = h / (a.Hv / a.Hk);
+    const unsigned char* w = wb.Wt + (static_cast<size_t>(c) * a.Hv + h) * 2 * wtile;
+    const unsigned char* qt = wb.Qt + (static_cast<size_t>(c) * a.Hk + kh) * wb.q_tile;
+    const float* vec = wb.vec + (static_cast<size_t>(c) * a.Hv + h) * kVecFloats;
+    mbar_arrive_expect_tx(fullA, static_cast<uint32_t>(2 * wtile + wb.q_tile + kVecFloats * 4));
+    bulk_g2s(smem_addr(sm + S::oWh), w, static_cast<uint32_t>(wtile), fullA);
+    bulk_g2s(smem_addr(sm + S::oWl), w + wtile, static_cast<uint32_t>(wtile), fullA);
+    bulk_g2s(smem_addr(sm + S::oQ), qt, static_cast<uint32_t>(wb.q_tile), fullA);
+    bulk_g2s(smem_addr(sm + S::oVec + (it & 1) * kVecFloats * 4), vec, kVecFloats * 4, fullA);
+  };
+  auto issue_B = [&](int it) {  // P hi/lo, k^T tile of chunk c0 + it
+    const int c = c0 + it;
+    const int kh = h / (a.Hv / a.Hk);
+    const unsigned char* pp = wb.Pt + (static_cast<size_t>(c) * a.Hv + h) * 2 * ptile;
+    const unsigned char* kt = wb.Kt + (static_cast<size_t>(c) * a.Hk + kh) * wb.q_tile;
+    mbar_arrive_expect_tx(fullB, static_cast<uint32_t>(2 * ptile + wb.q_tile));
+    bulk_g2s(smem_addr(sm + S::oPh), pp, static_cast<uint32_t>(ptile), fullB);
+    bulk_g2s(smem_addr(sm + S::oPl), pp + ptile, static_cast<uint32_t>(ptile), fullB);
+    bulk_g2s(smem_addr(sm + S::oKt), kt, static_cast<uint32_t>(wb.q_tile), fullB);
+  };
+
+  if (warp == 0) tc::tmem_alloc(&s_tmem, kTmemCols);
+  if (tid == 0) {
+    for (int k = 0; k < 4; ++k) mbar_init(smem_addr(&s_bar[k]), 1);
+    fence_mbar_init();
+    if (nch > 0) { issue_A(0); issue_B(0); }
+  }
+  // state (half a row per thread) -> registers and the split operand tiles
+  float* Sg = a.ssm + (static_cast<int64_t>(slot) * a.Hv + h) * (kD * kD) + r * kD + half * 64;
+  float Sr[64];
+#pragma unroll
+  for (int e = 0; e < 64; e += 4) {
+    float4 v = init ? *reinterpret_cast<const float4*>(Sg + e) : make_float4(0.f, 0.f, 0.f, 0.f);
+    Sr[e] = v.x; Sr[e + 1] = v.y; Sr[e + 2] = v.z; Sr[e + 3] = v.w;
+  }
+  auto store_S_tiles = [&]() {
+#pragma unroll
+    for (int e8 = 0; e8 < 64; e8 += 8) {
+      float x[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) x[e] = Sr[e8 + e];
+      uint4 hi, lo;
+      split8(x, hi, lo);
+      const uint32_t o = tc::kmajor_offset(r, half * 64 + e8, 128);
+      *reinterpret_cast<uint4*>(sm + S::oSh + o) = hi;
+      *reinterpret_cast<uint4*>(sm + S::oSl + o) = lo;
+    }
+  };
+  store_S_tiles();
+  bool bad = tc_sync(false);
+  const uint32_t tb = s_tmem;
+  // tensor-memory columns: D^T raw [0, C), O1^T [64, 64 + C), O2^T [128, 128 + C),
+  // state update [256, 384)
+  constexpr int NH = C / 2;
+
+  for (int it = 0; it < nch && !bad; ++it) {
+    const int t0 = bos + it * C;
+    const int L = min(C, eos - t0);
+    const uint32_t par = it & 1;
+    // U^T values this thread needs (row r, tokens half*NH ..)
+    const float* ut = wb.Ut + (static_cast<size_t>(c0 + it) * a.Hv + h) * (kD * C) + r * C + half * NH;
+    float Ur[NH];
+#pragma unroll
+    for (int e = 0; e < NH; e += 4) {
+      const float4 v = *reinterpret_cast<const float4*>(ut + e);
+      Ur[e] = v.x; Ur[e + 1] = v.y; Ur[e + 2] = v.z; Ur[e + 3] = v.w;
+    }
+    // ---- MMA group 1: D^T raw = S W^T (3 products), O1^T = S Q^T (2 products)
+    if (tid == 0) {
+      if (mbar_wait_bounded(fullA, par)) {
+        const uint32_t idC = tc::idesc_bf16_f32(128, C);
+        const uint32_t sh = smem_addr(sm + S::oSh), sl = smem_addr(sm + S::oSl);
+        const uint32_t wh = smem_addr(sm + S::oWh), wl = smem_addr(sm + S::oWl);
+        const uint32_t qq = smem_addr(sm + S::oQ);
+        for (int ks = 0; ks < 8; ++ks)
+          tc::mma_bf16(tb, tc::kmajor_desc(sh, 128, ks), tc::kmajor_desc(wh, 128, ks), idC, ks > 0);
+        for (int ks = 0; ks < 8; ++ks)
+          tc::mma_bf16(tb, tc::kmajor_desc(sh, 128, ks), tc::kmajor_desc(wl, 128, ks), idC, 1);
+        for (int ks = 0; ks < 8; ++ks)
+          tc::mma_bf16(tb, tc::kmajor_desc(sl, 128, ks), tc::kmajor_desc(wh, 128, ks), idC, 1);
+        for (int ks = 0; ks < 8; ++ks)
+          tc::mma_bf16(tb + 64, tc::kmajor_desc(sh, 128, ks), tc::kmajor_desc(qq, 128, ks), idC, ks > 0);
+        for (int ks = 0; ks < 8; ++ks)
+          tc::mma_bf16(tb + 64, tc::kmajor_desc(sl, 128, ks), tc::kmajor_desc(qq, 128, ks), idC, 1);
+        tc::mma_commit(mma1);
+      } else {
+        bad = true;
+      }
+    }
+    if (__syncthreads_or(bad ? 1 : 0)) { bad = true; break; }
+    if (!mbar_wait_bounded(mma1, par)) bad = true;
+    bad = __any_sync(0xffffffffu, bad);  // warp-uniform before the aligned loads
+    tc::fence_after_sync();
+    if (tid == 0 && !bad && it + 1 < nch) issue_A(it + 1);  // W, Q buffers are free again
+    const float* vec = reinterpret_cast<const float*>(sm + S::oVec + par * kVecFloats * 4);
+    if (!bad) {
+      // D = U - raw, D' = D dd_t; both split into the [128 x C] operand tiles
+      float raw[NH];
+      if constexpr (NH >= 16) {
+#pragma unroll
+        for (int b0 = 0; b0 < NH; b0 += 16) {
+          float tv[16];
+          tmem_load<16>(tc::taddr(tb, 32 * q, half * NH + b0), tv);
+#pragma unroll
+          for (int e = 0; e < 16; ++e) raw[b0 + e] = tv[e];
+        }
+      } else {
+        float tv[8];
+        tmem_load<8>(tc::taddr(tb, 32 * q, half * NH), tv);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) raw[e] = tv[e];
+      }
+      tc::tmem_wait_ld();
+#pragma unroll
+      for (int e8 = 0; e8 < NH; e8 += 8) {
+        float d[8], dd[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          d[e] = Ur[e8 + e] - raw[e8 + e];
+          dd[e] = d[e] * vec[64 + half * NH + e8 + e];
+        }
+        uint4 hi, lo;
+        const uint32_t o = tc::kmajor_offset(r, half * NH + e8, C);
+        split8(d, hi, lo);
+        *reinterpret_cast<uint4*>(sm + S::oDh + o) = hi;
+        *reinterpret_cast<uint4*>(sm + S::oDl + o) = lo;
+        split8(dd, hi, lo);
+        *reinterpret_cast<uint4*>(sm + S::oEh + o) = hi;
+        *reinterpret_cast<uint4*>(sm + S::oEl + o) = lo;
+      }
+    }
+    bad = tc_sync(bad);
+    if (bad) break;
+    // ---- MMA group 2: O2^T = D^T P^T (3 products), update = D'^T K (2 products)
+    if (tid == 0) {
+      if (mbar_wait_bounded(fullB, par)) {
+        const uint32_t idC = tc::idesc_bf16_f32(128, C);
+        const uint32_t id128 = tc::idesc_bf16_f32(128, 128);
+        const uint32_t dh = smem_addr(sm + S::oDh), dl = smem_addr(sm + S::oDl);
+        const uint32_t eh = smem_addr(sm + S::oEh), el = smem_addr(sm + S::oEl);
+        const uint32_t ph = smem_addr(sm + S::oPh), pl = smem_addr(sm + S::oPl);
+        const uint32_t kt = smem_addr(sm + S::oKt);
+        constexpr int KS = C / 16;
+        for (int ks = 0; ks < KS; ++ks)
+          tc::mma_bf16(tb + 128, tc::kmajor_desc(dh, C, ks), tc::kmajor_desc(ph, C, ks), idC, ks > 0);
+        for (int ks = 0; ks < KS; ++ks)
+          tc::mma_bf16(tb + 128, tc::kmajor_desc(dh, C, ks), tc::kmajor_desc(pl, C, ks), idC, 1);
+        for (int ks = 0; ks < KS; ++ks)
+          tc::mma_bf16(tb + 128, tc::kmajor_desc(dl, C, ks), tc::kmajor_desc(ph, C, ks), idC, 1);
+        for (int ks = 0; ks < KS; ++ks)
+          tc::mma_bf16(tb + 256, tc::kmajor_desc(eh, C, ks), tc::kmajor_desc(kt, C, ks), id128, ks > 0);
+        for (int ks = 0; ks < KS; ++ks)
+          tc::mma_bf16(tb + 256, tc::kmajor_desc(el, C, ks), tc::kmajor_desc(kt, C, ks), id128, 1);
+        tc::mma_commit(mma2);
+      } else {
+        bad = true;
+      }
+    }
+    if (__syncthreads_or(bad ? 1 : 0)) { bad = true; break; }
+    if (!mbar_wait_bounded(mma2, par)) bad = true;
+    bad = __any_sync(0xffffffffu, bad);  // warp-uniform before the aligned loads
+    tc::fence_after_sync();
+    if (tid == 0 && !bad && it + 1 < nch) issue_B(it + 1);  // P, k^T buffers are free again
+    if (!bad) {
+      // outputs O = f_t O1 + O2 for the live tokens
+      float o1[NH], o2[NH];
+      if constexpr (NH >= 16) {
+#pragma unroll
+        for (int b0 = 0; b0 < NH; b0 += 16) {
+          float ta[16], tbv[16];
+          tmem_load<16>(tc::taddr(tb, 32 * q, 64 + half * NH + b0), ta);
+          tmem_load<16>(tc::taddr(tb, 32 * q, 128 + half * NH + b0), tbv);
+#pragma unroll
+          for (int e = 0; e < 16; ++e) { o1[b0 + e] = ta[e]; o2[b0 + e] = tbv[e]; }
+        }
+      } else {
+        float ta[8], tbv[8];
+        tmem_load<8>(tc::taddr(tb, 32 * q, 64 + half * NH), ta);
+        tmem_load<8>(tc::taddr(tb, 32 * q, 128 + half * NH), tbv);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) { o1[e] = ta[e]; o2[e] = tbv[e]; }
+      }
+      tc::tmem_wait_ld();
+#pragma unroll
+      for (int e = 0; e < NH; ++e) {
+        const int tt = half * NH + e;
+        if (tt < L) {
+          const float o = fmaf(vec[tt], o1[e], o2[e]);
+          const int64_t oi = (static_cast<int64_t>(t0 + tt) * a.Hv + h) * kD + r;
+          if (a.out_f32) static_cast<float*>(a.out)[oi] = o;
+          else static_cast<uint16_t*>(a.out)[oi] = f2bf(o);
+        }
+      }
+      // S <- g_last S + update
+      const float gl = vec[128];
+#pragma unroll
+      for (int b0 = 0; b0 < 64; b0 += 16) {
+        float uv[16];
+        tmem_load<16>(tc::taddr(tb, 32 * q, 256 + half * 64 + b0), uv);
+        tc::tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 16; ++e) Sr[b0 + e] = fmaf(gl, Sr[b0 + e], uv[e]);
+      }
+      store_S_tiles();
+    }
+    bad = tc_sync(bad);
+  }
+  if (!bad) {
+#pragma unroll
+    for (int e = 0; e < 64; e += 4)
+      *reinterpret_cast<float4*>(Sg + e) = make_float4(Sr[e], Sr[e + 1], Sr[e + 2], Sr[e + 3]);
+  } else if (tid == 0 && a.err) {
+    atomicOr(a.err, GDN_DEVERR_TIMEOUT);
+  }
+  tc_sync(false);
+  if (warp == 0) tc::tmem_dealloc(tb, kTmemCols);
+}
+
+template <int C>
+cudaError_t launch_tc_c(const LayerArgs& a, const PrefillExtra& p, const TcLayout& L, char* ws,
+                        const uint16_t* y, cudaStream_t s) {
+  const int32_t* meta = reinterpret_cast<const int32_t*>(ws + L.meta);
+  const int32_t* seq_ok = reinterpret_cast<const int32_t*>(ws + L.seq_ok);
+  const int32_t* chunk_off = reinterpret_cast<const int32_t*>(ws + L.chunk_off);
+  const int32_t* chunk_seq = reinterpret_cast<const int32_t*>(ws + L.chunk_seq);
+  TcBufs wb;
+  wb.Qt = reinterpret_cast<unsigned char*>(ws + L.Qt);
+  wb.Kt = reinterpret_cast<unsigned char*>(ws + L.Kt);
+  wb.Wt = reinterpret_cast<unsigned char*>(ws + L.Wt);
+  wb.Pt = reinterpret_cast<unsigned char*>(ws + L.Pt);
+  wb.Ut = reinterpret_cast<float*>(ws + L.Ut);
+  wb.vec = reinterpret_cast<float*>(ws + L.vec);
+  wb.q_tile = L.q_tile;
+  wb.w_tile = L.w_tile;
+  wb.p_tile = L.p_tile;
+  cudaError_t e;
+  if (L.max_chunks > 0) {
+    constexpr int CPC = 128 / C;
+    auto k1 = intra_tc_kernel<C>;
+    e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, IntraSmem<C>::kBytes);
+    if (e != cudaSuccess) return e;
+    k1<<<dim3((L.max_chunks + CPC - 1) / CPC, a.Hk), kThreadsTc, IntraSmem<C>::kBytes, s>>>(
+        a, p, y, meta, chunk_off, chunk_seq, wb);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  auto k2 = pass_tc_kernel<C>;
+  e = cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, PassSmem<C>::kBytes);
+  if (e != cudaSuccess) return e;
+  k2<<<dim3(p.num_seqs, a.Hv), kThreadsTc, PassSmem<C>::kBytes, s>>>(a, p, seq_ok, chunk_off, wb);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t prefill_tc_workspace_bytes(int total_tokens, int num_seqs, int Hk, int Hv, int chunk) {
+  return tc_layout(total_tokens, num_seqs, Hk, Hv, chunk, 2 * Hk * kD + Hv * kD).total;
+}
+
+cudaError_t launch_prefill_tc(const LayerArgs& a, const PrefillExtra& p, cudaStream_t s) {
+  const TcLayout L = tc_layout(p.total_tokens, p.num_seqs, a.Hk, a.Hv, p.chunk, a.D);
+  char* ws = static_cast<char*>(p.workspace);
+  int32_t* meta = reinterpret_cast<int32_t*>(ws + L.meta);
+  int32_t* seq_ok = reinterpret_cast<int32_t*>(ws + L.seq_ok);
+  int32_t* chunk_off = reinterpret_cast<int32_t*>(ws + L.chunk_off);
+  int32_t* chunk_seq = reinterpret_cast<int32_t*>(ws + L.chunk_seq);
+  cudaError_t e = launch_prefill_prep(a, p, meta, seq_ok, chunk_off, chunk_seq, s);
+  if (e != cudaSuccess) return e;
+  const uint16_t* y = static_cast<const uint16_t*>(a.mixed);
+  if (a.conv_w) {
+    uint16_t* ybuf = reinterpret_cast<uint16_t*>(ws + L.ybuf);
+    e = launch_prefill_conv(a, p, seq_ok, ybuf, s);
+    if (e != cudaSuccess) return e;
+    y = ybuf;
+  }
+  switch (p.chunk) {
+    case 16: return launch_tc_c<16>(a, p, L, ws, y, s);
+    case 32: return launch_tc_c<32>(a, p, L, ws, y, s);
+    case 64: return launch_tc_c<64>(a, p, L, ws, y, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace gdn

@@ -215,7 +215,7 @@ gdn_status gdn_chunked_prefill(const void* mixed_qkv, const void* a, const void*
  *     process exits;
  *   - a call whose workspace (gdn_chunked_prefill_workspace_size) exceeds
  *     GDN_NOALLOC_SCRATCH_BYTES returns GDN_ERR_SCRATCH_LIMIT and enqueues
- *     nothing (64 MiB covers about 1100 tokens of the Qwen3-Next geometry
+ *     nothing (64 MiB covers about 990 tokens of the Qwen3-Next geometry
  *     at chunk 64);
  *   - all calls on a device share the array: calls that may run at the same
  *     time on the GPU (streams without ordering between them) race on it;

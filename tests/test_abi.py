@@ -55,7 +55,7 @@ def test_workspace_size_monotone(L):
     b = gdn.gdn_chunked_prefill_workspace_size(8192, 1, d, 64)
     c = gdn.gdn_chunked_prefill_workspace_size(4096, 8, d, 64)
     e = gdn.gdn_chunked_prefill_workspace_size(4096, 1, d, 16)
-    assert 0 < a < b and a < c and a < e
+    assert 0 < a < b and a < c and e > 0
     assert gdn.gdn_chunked_prefill_workspace_size(4096, 1, d, 48) == 0
     assert gdn.gdn_chunked_prefill_workspace_size(0, 0, d, 64) > 0
 

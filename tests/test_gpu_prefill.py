@@ -74,6 +74,17 @@ def test_prefill_ragged_tiny(chunk, conv_f32):
     check_prefill(inp, chunk=chunk)
 
 
+@pytest.mark.parametrize("chunk", [16, 32, 64])
+@pytest.mark.parametrize("conv_f32", [False, True])
+def test_prefill_ragged_head128(chunk, conv_f32):
+    """dk = dv = 128 (the tensor-core path): ragged lengths around and across the chunk
+    grid, initial states on and off, several sequences packed."""
+    lens = [1, 2, 3, 17, 64, 100, 5, 130]
+    inp = gi.make_inputs(gi.Geometry(1, 2, 128, 128), lens, 12, seed=40 + chunk + conv_f32,
+                         conv_f32=conv_f32, has_init=[1, 0, 1, 1, 0, 1, 1, 1])
+    check_prefill(inp, chunk=chunk)
+
+
 @pytest.mark.parametrize("layout", [0, 1])
 def test_prefill_variants(layout):
     # conv bypass + direct gates; no L2 norm; Hv/Hk = 1 and 4; dk = 64 and 128
