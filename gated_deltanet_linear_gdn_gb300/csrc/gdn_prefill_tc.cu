@@ -101,6 +101,24 @@ __device__ __forceinline__ void split8(const float (&x)[8], uint4& hi, uint4& lo
   lo = pack8(l);
 }
 
+// 8 rows x 8 bf16 (one uint4 per row) -> 8 columns (one uint4 per column)
+__device__ __forceinline__ void transpose8x8(const uint4 (&in)[8], uint4 (&out)[8]) {
+  uint16_t m[8][8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint16_t* p = reinterpret_cast<const uint16_t*>(&in[i]);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) m[i][j] = p[j];
+  }
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    uint16_t col[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) col[i] = m[i][j];
+    out[j] = pack8(col);
+  }
+}
+
 template <int N>
 __device__ __forceinline__ void tmem_load(uint32_t addr, float (&v)[N]);
 template <>
@@ -185,13 +203,6 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
 #pragma unroll
       for (int e = 0; e < 8; ++e) ss = fmaf(f[e], f[e], ss);
       *reinterpret_cast<uint4*>(tile + tc::kmajor_offset(tok, 8 * k8, kD)) = v;
-      if (which) {  // k^T tile of this chunk: element (channel, tl)
-        const uint16_t* hv = reinterpret_cast<const uint16_t*>(&v);
-        unsigned char* kt = sm + S::oKtw + ci * (kD * C * 2);
-#pragma unroll
-        for (int e = 0; e < 8; ++e)
-          *reinterpret_cast<uint16_t*>(kt + tc::kmajor_offset(8 * k8 + e, tl, C)) = hv[e];
-      }
     }
     const float inv = a.qk_l2norm ? 1.0f / sqrtf(ss + 1e-6f) : 1.0f;
     (which ? s_ik : s_iq)[tok] = inv;
@@ -215,6 +226,20 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       tc::mma_bf16(tb + 128, tc::kmajor_desc(aq, kD, ks), tc::kmajor_desc(ak, kD, ks), id, ks > 0);
     tc::mma_commit(smem_addr(&s_bar));
   }
+  {  // k^T tiles per chunk: one 8 token x 8 channel block per thread, transposed
+    const int tg = tid >> 4, cg = tid & 15;
+    uint4 in[8], out[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      in[i] = *reinterpret_cast<const uint4*>(sm + S::oK + tc::kmajor_offset(8 * tg + i, 8 * cg, kD));
+    transpose8x8(in, out);
+    const int ci = (8 * tg) / C, tl0 = (8 * tg) % C;
+    unsigned char* kt = sm + S::oKtw + ci * (kD * C * 2);
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      *reinterpret_cast<uint4*>(kt + tc::kmajor_offset(8 * cg + j, tl0, C)) = out[j];
+  }
+  __syncthreads();
   // q and k^T tiles of each chunk -> workspace (read-only use of the smem tiles)
   for (int ci = 0; ci < CPC; ++ci) {
     const int c = c_first + ci;
@@ -355,27 +380,39 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         *reinterpret_cast<uint16_t*>(sm + S::oTl + o) = lo;
       }
     } else {
-      // V^T (raw bf16) and K'^T = (diag(e^G ik) K)^T (split) as [128 x 128 tokens] operands
+      // V^T (raw bf16) and K'^T = (diag(e^G ik) K)^T (split) as [128 x 128 tokens]
+      // operands: 16-byte row loads of 8 tokens x 8 channels, transposed in registers
       const int u = tid - 128;
       const int vc = 2 * a.Hk * kD + h * kD, kc = (a.Hk + kh) * kD;
-      for (int item = u; item < 128 * 16; item += 128) {
-        const int r = item & 127, tg = item >> 7;  // channel r, tokens 8 tg .. 8 tg + 7
-        uint16_t hv[8];
-        float kx[8];
+      for (int blk = u; blk < 256; blk += 128) {
+        const int tg = blk >> 4, cg = blk & 15;
+        uint4 vin[8], kin[8];
+        float sc[8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int tok = 8 * tg + e, ci = tok / C, tl = tok % C;
+        for (int i = 0; i < 8; ++i) {
+          const int tok = 8 * tg + i, ci = tok / C, tl = tok % C;
           const bool valid = tl < s_L[ci];
           const uint16_t* rowp = y + static_cast<int64_t>(s_t0[ci] + tl) * a.D;
-          hv[e] = valid ? rowp[vc + r] : static_cast<uint16_t>(0);
-          kx[e] = valid ? bf2f(rowp[kc + r]) * (expf(s_G[tok]) * s_ik[tok]) : 0.0f;
+          vin[i] = valid ? __ldg(reinterpret_cast<const uint4*>(rowp + vc) + cg) : make_uint4(0u, 0u, 0u, 0u);
+          kin[i] = valid ? __ldg(reinterpret_cast<const uint4*>(rowp + kc) + cg) : make_uint4(0u, 0u, 0u, 0u);
+          sc[i] = valid ? expf(s_G[tok]) * s_ik[tok] : 0.0f;
         }
-        const uint32_t o = tc::kmajor_offset(r, 8 * tg, 128);
-        *reinterpret_cast<uint4*>(sm + S::oVt + o) = pack8(hv);
-        uint4 hi, lo;
-        split8(kx, hi, lo);
-        *reinterpret_cast<uint4*>(sm + S::oQ + o) = hi;  // sKh (aliases sQ)
-        *reinterpret_cast<uint4*>(sm + S::oK + o) = lo;  // sKl (aliases sK)
+        uint4 vt[8], kt[8];
+        transpose8x8(vin, vt);
+        transpose8x8(kin, kt);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const uint32_t o = tc::kmajor_offset(8 * cg + j, 8 * tg, 128);
+          *reinterpret_cast<uint4*>(sm + S::oVt + o) = vt[j];
+          float kx[8];
+          unpack8(kt[j], kx);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) kx[i] *= sc[i];
+          uint4 hi, lo;
+          split8(kx, hi, lo);
+          *reinterpret_cast<uint4*>(sm + S::oQ + o) = hi;  // sKh (aliases sQ)
+          *reinterpret_cast<uint4*>(sm + S::oK + o) = lo;  // sKl (aliases sK)
+        }
       }
     }
     bad = tc_sync(bad);
@@ -545,12 +582,47 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   // tensor-memory columns: D^T raw [0, C), O1^T [64, 64 + C), O2^T [128, 128 + C),
   // state update [256, 384)
   constexpr int NH = C / 2;
+  constexpr int KS = C / 16;
+  // operand descriptors are fixed per CTA; a K step adds 256 bytes (16 units) to the start
+  const uint64_t dSh = tc::kmajor_desc(smem_addr(sm + S::oSh), 128, 0);
+  const uint64_t dSl = tc::kmajor_desc(smem_addr(sm + S::oSl), 128, 0);
+  const uint64_t dWh = tc::kmajor_desc(smem_addr(sm + S::oWh), 128, 0);
+  const uint64_t dWl = tc::kmajor_desc(smem_addr(sm + S::oWl), 128, 0);
+  const uint64_t dQ = tc::kmajor_desc(smem_addr(sm + S::oQ), 128, 0);
+  const uint64_t dDh = tc::kmajor_desc(smem_addr(sm + S::oDh), C, 0);
+  const uint64_t dDl = tc::kmajor_desc(smem_addr(sm + S::oDl), C, 0);
+  const uint64_t dEh = tc::kmajor_desc(smem_addr(sm + S::oEh), C, 0);
+  const uint64_t dEl = tc::kmajor_desc(smem_addr(sm + S::oEl), C, 0);
+  const uint64_t dPh = tc::kmajor_desc(smem_addr(sm + S::oPh), C, 0);
+  const uint64_t dPl = tc::kmajor_desc(smem_addr(sm + S::oPl), C, 0);
+  const uint64_t dKt = tc::kmajor_desc(smem_addr(sm + S::oKt), C, 0);
+  const uint32_t idC = tc::idesc_bf16_f32(128, C), id128 = tc::idesc_bf16_f32(128, 128);
+
+  // MMA group 1 of chunk `it` (thread 0): D^T raw = S W^T, O1^T = S Q^T
+  auto issue_mma1 = [&](int it) -> bool {
+    if (!mbar_wait_bounded(fullA, it & 1)) return false;
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) tc::mma_bf16(tb, dSh + 16 * ks, dWh + 16 * ks, idC, ks > 0);
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) tc::mma_bf16(tb, dSh + 16 * ks, dWl + 16 * ks, idC, 1);
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) tc::mma_bf16(tb, dSl + 16 * ks, dWh + 16 * ks, idC, 1);
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) tc::mma_bf16(tb + 64, dSh + 16 * ks, dQ + 16 * ks, idC, ks > 0);
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) tc::mma_bf16(tb + 64, dSl + 16 * ks, dQ + 16 * ks, idC, 1);
+    tc::mma_commit(mma1);
+    return true;
+  };
+  // a thread 0 failure leaves an MMA group unissued; the other threads' bounded waits
+  // then expire, and every thread learns of it at the next CTA barrier
+  if (tid == 0 && nch > 0 && !bad && !issue_mma1(0)) bad = true;
 
   for (int it = 0; it < nch && !bad; ++it) {
     const int t0 = bos + it * C;
     const int L = min(C, eos - t0);
     const uint32_t par = it & 1;
-    // U^T values this thread needs (row r, tokens half*NH ..)
+    // U^T values this thread needs (row r, tokens half*NH ..), loaded while MMA group 1 runs
     const float* ut = wb.Ut + (static_cast<size_t>(c0 + it) * a.Hv + h) * (kD * C) + r * C + half * NH;
     float Ur[NH];
 #pragma unroll
@@ -558,29 +630,6 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       const float4 v = *reinterpret_cast<const float4*>(ut + e);
       Ur[e] = v.x; Ur[e + 1] = v.y; Ur[e + 2] = v.z; Ur[e + 3] = v.w;
     }
-    // ---- MMA group 1: D^T raw = S W^T (3 products), O1^T = S Q^T (2 products)
-    if (tid == 0) {
-      if (mbar_wait_bounded(fullA, par)) {
-        const uint32_t idC = tc::idesc_bf16_f32(128, C);
-        const uint32_t sh = smem_addr(sm + S::oSh), sl = smem_addr(sm + S::oSl);
-        const uint32_t wh = smem_addr(sm + S::oWh), wl = smem_addr(sm + S::oWl);
-        const uint32_t qq = smem_addr(sm + S::oQ);
-        for (int ks = 0; ks < 8; ++ks)
-          tc::mma_bf16(tb, tc::kmajor_desc(sh, 128, ks), tc::kmajor_desc(wh, 128, ks), idC, ks > 0);
-        for (int ks = 0; ks < 8; ++ks)
-          tc::mma_bf16(tb, tc::kmajor_desc(sh, 128, ks), tc::kmajor_desc(wl, 128, ks), idC, 1);
-        for (int ks = 0; ks < 8; ++ks)
-          tc::mma_bf16(tb, tc::kmajor_desc(sl, 128, ks), tc::kmajor_desc(wh, 128, ks), idC, 1);
-        for (int ks = 0; ks < 8; ++ks)
-          tc::mma_bf16(tb + 64, tc::kmajor_desc(sh, 128, ks), tc::kmajor_desc(qq, 128, ks), idC, ks > 0);
-        for (int ks = 0; ks < 8; ++ks)
-          tc::mma_bf16(tb + 64, tc::kmajor_desc(sl, 128, ks), tc::kmajor_desc(qq, 128, ks), idC, 1);
-        tc::mma_commit(mma1);
-      } else {
-        bad = true;
-      }
-    }
-    if (__syncthreads_or(bad ? 1 : 0)) { bad = true; break; }
     if (!mbar_wait_bounded(mma1, par)) bad = true;
     bad = __any_sync(0xffffffffu, bad);  // warp-uniform before the aligned loads
     tc::fence_after_sync();
@@ -627,35 +676,28 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     // ---- MMA group 2: O2^T = D^T P^T (3 products), update = D'^T K (2 products)
     if (tid == 0) {
       if (mbar_wait_bounded(fullB, par)) {
-        const uint32_t idC = tc::idesc_bf16_f32(128, C);
-        const uint32_t id128 = tc::idesc_bf16_f32(128, 128);
-        const uint32_t dh = smem_addr(sm + S::oDh), dl = smem_addr(sm + S::oDl);
-        const uint32_t eh = smem_addr(sm + S::oEh), el = smem_addr(sm + S::oEl);
-        const uint32_t ph = smem_addr(sm + S::oPh), pl = smem_addr(sm + S::oPl);
-        const uint32_t kt = smem_addr(sm + S::oKt);
-        constexpr int KS = C / 16;
-        for (int ks = 0; ks < KS; ++ks)
-          tc::mma_bf16(tb + 128, tc::kmajor_desc(dh, C, ks), tc::kmajor_desc(ph, C, ks), idC, ks > 0);
-        for (int ks = 0; ks < KS; ++ks)
-          tc::mma_bf16(tb + 128, tc::kmajor_desc(dh, C, ks), tc::kmajor_desc(pl, C, ks), idC, 1);
-        for (int ks = 0; ks < KS; ++ks)
-          tc::mma_bf16(tb + 128, tc::kmajor_desc(dl, C, ks), tc::kmajor_desc(ph, C, ks), idC, 1);
-        for (int ks = 0; ks < KS; ++ks)
-          tc::mma_bf16(tb + 256, tc::kmajor_desc(eh, C, ks), tc::kmajor_desc(kt, C, ks), id128, ks > 0);
-        for (int ks = 0; ks < KS; ++ks)
-          tc::mma_bf16(tb + 256, tc::kmajor_desc(el, C, ks), tc::kmajor_desc(kt, C, ks), id128, 1);
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) tc::mma_bf16(tb + 128, dDh + 16 * ks, dPh + 16 * ks, idC, ks > 0);
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) tc::mma_bf16(tb + 128, dDh + 16 * ks, dPl + 16 * ks, idC, 1);
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) tc::mma_bf16(tb + 128, dDl + 16 * ks, dPh + 16 * ks, idC, 1);
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) tc::mma_bf16(tb + 256, dEh + 16 * ks, dKt + 16 * ks, id128, ks > 0);
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) tc::mma_bf16(tb + 256, dEl + 16 * ks, dKt + 16 * ks, id128, 1);
         tc::mma_commit(mma2);
       } else {
         bad = true;
       }
     }
-    if (__syncthreads_or(bad ? 1 : 0)) { bad = true; break; }
     if (!mbar_wait_bounded(mma2, par)) bad = true;
     bad = __any_sync(0xffffffffu, bad);  // warp-uniform before the aligned loads
     tc::fence_after_sync();
     if (tid == 0 && !bad && it + 1 < nch) issue_B(it + 1);  // P, k^T buffers are free again
+    float Ov[NH];
     if (!bad) {
-      // outputs O = f_t O1 + O2 for the live tokens
+      // O = f_t O1 + O2 into registers (stored below, while the next chunk's MMAs run)
       float o1[NH], o2[NH];
       if constexpr (NH >= 16) {
 #pragma unroll
@@ -675,29 +717,33 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       }
       tc::tmem_wait_ld();
 #pragma unroll
-      for (int e = 0; e < NH; ++e) {
-        const int tt = half * NH + e;
-        if (tt < L) {
-          const float o = fmaf(vec[tt], o1[e], o2[e]);
-          const int64_t oi = (static_cast<int64_t>(t0 + tt) * a.Hv + h) * kD + r;
-          if (a.out_f32) static_cast<float*>(a.out)[oi] = o;
-          else static_cast<uint16_t*>(a.out)[oi] = f2bf(o);
-        }
-      }
-      // S <- g_last S + update
+      for (int e = 0; e < NH; ++e) Ov[e] = fmaf(vec[half * NH + e], o1[e], o2[e]);
+      // S <- g_last S + update, 16 columns at a time
       const float gl = vec[128];
 #pragma unroll
       for (int b0 = 0; b0 < 64; b0 += 16) {
-        float uv[16];
-        tmem_load<16>(tc::taddr(tb, 32 * q, 256 + half * 64 + b0), uv);
+        float tv[16];
+        tmem_load<16>(tc::taddr(tb, 32 * q, 256 + half * 64 + b0), tv);
         tc::tmem_wait_ld();
 #pragma unroll
-        for (int e = 0; e < 16; ++e) Sr[b0 + e] = fmaf(gl, Sr[b0 + e], uv[e]);
+        for (int e = 0; e < 16; ++e) Sr[b0 + e] = fmaf(gl, Sr[b0 + e], tv[e]);
       }
       store_S_tiles();
     }
     bad = tc_sync(bad);
+    if (bad) break;
+    if (tid == 0 && it + 1 < nch && !issue_mma1(it + 1)) bad = true;
+#pragma unroll
+    for (int e = 0; e < NH; ++e) {
+      const int tt = half * NH + e;
+      if (tt < L) {
+        const int64_t oi = (static_cast<int64_t>(t0 + tt) * a.Hv + h) * kD + r;
+        if (a.out_f32) static_cast<float*>(a.out)[oi] = Ov[e];
+        else static_cast<uint16_t*>(a.out)[oi] = f2bf(Ov[e]);
+      }
+    }
   }
+  bad = tc_sync(bad);
   if (!bad) {
 #pragma unroll
     for (int e = 0; e < 64; e += 4)
