@@ -618,10 +618,25 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   // then expire, and every thread learns of it at the next CTA barrier
   if (tid == 0 && nch > 0 && !bad && !issue_mma1(0)) bad = true;
 
+  auto prefetch_chunk = [&](int it) {  // the workspace tiles of chunk c0 + it -> L2
+    const int c = c0 + it;
+    const int kh = h / (a.Hv / a.Hk);
+    const size_t ch = static_cast<size_t>(c) * a.Hv + h;
+    bulk_prefetch_l2(wb.Ut + ch * (kD * C), static_cast<uint32_t>(kD * C * 4));
+    bulk_prefetch_l2(wb.Wt + ch * 2 * wtile, static_cast<uint32_t>(2 * wtile));
+    bulk_prefetch_l2(wb.Pt + ch * 2 * ptile, static_cast<uint32_t>(2 * ptile));
+    bulk_prefetch_l2(wb.vec + ch * kVecFloats, kVecFloats * 4);
+    const size_t ck = static_cast<size_t>(c) * a.Hk + kh;
+    bulk_prefetch_l2(wb.Qt + ck * wb.q_tile, static_cast<uint32_t>(wb.q_tile));
+    bulk_prefetch_l2(wb.Kt + ck * wb.q_tile, static_cast<uint32_t>(wb.q_tile));
+  };
+  if (tid == 32 && nch > 1) prefetch_chunk(1);
+
   for (int it = 0; it < nch && !bad; ++it) {
     const int t0 = bos + it * C;
     const int L = min(C, eos - t0);
     const uint32_t par = it & 1;
+    if (tid == 32 && it + 2 < nch) prefetch_chunk(it + 2);  // two chunks ahead
     // U^T values this thread needs (row r, tokens half*NH ..), loaded while MMA group 1 runs
     const float* ut = wb.Ut + (static_cast<size_t>(c0 + it) * a.Hv + h) * (kD * C) + r * C + half * NH;
     float Ur[NH];
