@@ -236,6 +236,16 @@ def run_ours(args, rank, world):
             nb = decode_bytes(B, geo)
             sweep[str(B)] = {"us": round(ms * 1e3, 2), "GBps": round(nb / ms / 1e6, 1)}
             del t
+        # CUDA-graph buckets (one replay = one graph launch of the fused step)
+        for B in (1, 16):
+            t = decode_setup(B, NUM_SLOTS, seed=B)
+            g = gdn.DecodeGraph(t["mixed"], t["a"], t["b"], t["A_log"], t["dt_bias"], t["conv_w"],
+                                t["conv_b"], t["conv"], t["ssm"], t["slot"], t["out"], dims)
+            ms = float(np.median(timed(lambda: g.launch(stream), 20, 3)))
+            sweep[f"graph_c{B}"] = {"us": round(ms * 1e3, 2),
+                                    "GBps": round(decode_bytes(B, geo) / ms / 1e6, 1)}
+            g.close()
+            del t
         for conv_f32 in (False, True):
             t = decode_setup(1024, 2048, seed=5, conv_f32=conv_f32)
             ms = float(np.median(timed(lambda: decode_call(t), 10, 2)))

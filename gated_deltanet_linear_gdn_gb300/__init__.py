@@ -83,6 +83,14 @@ def lib():
         L.gdn_chunked_prefill_noalloc.argtypes = [P, P, P, I32, P, P, P, P, I32, P, I32, I32, P,
                                                   P, P, P, I32, I32, I32, gdn_dims, F, I32, I32,
                                                   P, I32, P, P]
+        L.gdn_decode_graph_create.restype = I32
+        L.gdn_decode_graph_create.argtypes = [P, P, P, I32, P, P, P, P, I32, P, I32, I32, P, P,
+                                              I32, I32, gdn_dims, F, I32, P, I32, P,
+                                              ctypes.POINTER(ctypes.c_void_p)]
+        L.gdn_graph_launch.restype = I32
+        L.gdn_graph_launch.argtypes = [P, P]
+        L.gdn_graph_destroy.restype = None
+        L.gdn_graph_destroy.argtypes = [P]
         L.gdn_validate_slots.restype = I32
         L.gdn_validate_slots.argtypes = [P, I32, I32]
         L.gdn_status_string.restype = ctypes.c_char_p
@@ -202,6 +210,42 @@ def gdn_chunked_prefill_noalloc(mixed_qkv, a, b, A_log, dt_bias, conv_weight, co
         int(conv_layout), _ptr(ssm_state), _ptr(cu_seqlens), _ptr(slot),
         _ptr(has_initial_state), N, T, ssm_state.shape[0], dims.c(), float(scale),
         int(bool(qk_l2norm)), int(chunk), _ptr(out), _dt(out), _ptr(err), _stream(stream)))
+
+
+class DecodeGraph:
+    """A captured decode step over fixed buffers (gdn_decode_graph_create). The tensors passed
+    at creation are kept referenced here: write each step's inputs into them, then launch()."""
+
+    def __init__(self, mixed_qkv, a, b, A_log, dt_bias, conv_weight, conv_bias, conv_state,
+                 ssm_state, slot, out, dims: Dims, *, silu=True, conv_layout=GDN_CONV_DIM_FIRST,
+                 scale=None, qk_l2norm=True, err=None):
+        self._keep = (mixed_qkv, a, b, A_log, dt_bias, conv_weight, conv_bias, conv_state,
+                      ssm_state, slot, out, err)
+        B = mixed_qkv.shape[0]
+        scale = dims.dk ** -0.5 if scale is None else scale
+        conv_dt = _dt(conv_state) if conv_state is not None else GDN_BF16
+        h = ctypes.c_void_p()
+        _check(lib().gdn_decode_graph_create(
+            _ptr(mixed_qkv), _ptr(a), _ptr(b), _gate_mode(a), _ptr(A_log), _ptr(dt_bias),
+            _ptr(conv_weight), _ptr(conv_bias), int(bool(silu)), _ptr(conv_state), conv_dt,
+            int(conv_layout), _ptr(ssm_state), _ptr(slot), B, ssm_state.shape[0], dims.c(),
+            float(scale), int(bool(qk_l2norm)), _ptr(out), _dt(out), _ptr(err),
+            ctypes.byref(h)))
+        self._h = h
+
+    def launch(self, stream=None):
+        _check(lib().gdn_graph_launch(self._h, _stream(stream)))
+
+    def close(self):
+        if getattr(self, "_h", None):
+            lib().gdn_graph_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 def gdn_validate_slots(host_slot, num_slots) -> int:

@@ -239,6 +239,37 @@ gdn_status gdn_chunked_prefill_noalloc(const void* mixed_qkv, const void* a, con
                                        int32_t* err, void* stream);
 
 /*
+ * CUDA-graph decode buckets ([P2] Rocket, "A reduction barrier makes Qwen GDN
+ * graph replay bit exact": immutable graphs per decode bucket c1, c2, ...,
+ * inactive rows cleared on bucket transitions, slot 0 untouched).
+ *
+ * gdn_decode_graph_create captures ONE gdn_decode_step call -- same arguments,
+ * same validation and the same result codes -- into an instantiated CUDA graph
+ * and returns it in *graph_out. Nothing runs at creation. The graph keeps the
+ * pointers it was created with: the caller keeps those buffers alive and
+ * unmoved, and writes each step's inputs (x, gate inputs, slot table) into
+ * them before gdn_graph_launch. Rows a step does not use get slot 0, which makes
+ * their outputs zero and leaves every state block alone. Creation is a set-up
+ * call (it creates a stream and instantiates a graph); launching is not.
+ * gdn_graph_launch enqueues the graph on `stream` (a cudaStream_t); a replay is
+ * bitwise identical to the direct call. gdn_graph_destroy frees the handle
+ * (NULL is ignored).
+ */
+typedef struct gdn_graph gdn_graph;
+
+gdn_status gdn_decode_graph_create(const void* mixed_qkv, const void* a, const void* b,
+                                   gdn_gate_mode gate_mode, const float* A_log,
+                                   const float* dt_bias, const void* conv_weight,
+                                   const void* conv_bias, int32_t silu, void* conv_state,
+                                   gdn_dtype conv_dtype, gdn_conv_layout conv_layout,
+                                   float* ssm_state, const int32_t* slot, int32_t batch,
+                                   int32_t num_slots, gdn_dims dims, float scale,
+                                   int32_t qk_l2norm, void* out, gdn_dtype out_dtype,
+                                   int32_t* err, gdn_graph** graph_out);
+gdn_status gdn_graph_launch(gdn_graph* graph, void* stream);
+void gdn_graph_destroy(gdn_graph* graph);
+
+/*
  * gdn_validate_slots -- host-side check of a HOST slot table ([P1] Notes,
  * "State ABI": the goldens raise on an active index that is out of range or
  * repeated). Returns 0 if every active slot (> 0) is < num_slots and no
