@@ -39,13 +39,13 @@ NUM_SLOTS = 512
 FALLBACK_HBM_GBS = 6800.0
 
 
-def decode_bytes(B, geo, conv_f32=False, bias=True, out_bytes=2):
-    """Algorithmic bytes of one decode step: per row the fp32 state read + write, x, the
-    conv window read + write, the output and the gate inputs and slot; per call the conv
-    weight and bias and the per-head gate parameters."""
+def decode_bytes(B, geo, conv_f32=False, bias=True, out_bytes=2, state_bytes=4):
+    """Algorithmic bytes of one decode step: per row the state read + write (fp32, or bf16
+    with state_bytes=2), x, the conv window read + write, the output and the gate inputs
+    and slot; per call the conv weight and bias and the per-head gate parameters."""
     s = 4 if conv_f32 else 2
     D = geo.D
-    per_row = (2 * geo.Hv * geo.dv * geo.dk * 4 + 2 * D + 2 * D * (geo.W - 1) * s
+    per_row = (2 * geo.Hv * geo.dv * geo.dk * state_bytes + 2 * D + 2 * D * (geo.W - 1) * s
                + out_bytes * geo.Hv * geo.dv + 2 * 2 * geo.Hv + 4)
     per_call = 2 * D * geo.W + (2 * D if bias else 0) + 8 * geo.Hv
     return B * per_row + per_call
@@ -190,7 +190,7 @@ def run_ours(args, rank, world):
     def b16(x):
         return torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).view(torch.bfloat16)
 
-    def decode_setup(B, num_slots, seed, conv_f32=False, bias=True, silu=True):
+    def decode_setup(B, num_slots, seed, conv_f32=False, bias=True, silu=True, state_bf16=False):
         inp = gi.make_inputs(geo, [1] * B, num_slots, seed, state_pool=False, conv_f32=conv_f32,
                              bias=bias, silu=silu)
         t = dict(
@@ -198,7 +198,8 @@ def run_ours(args, rank, world):
             A_log=torch.from_numpy(inp.A_log).to(dev), dt_bias=torch.from_numpy(inp.dt_bias).to(dev),
             conv_w=b16(inp.conv_w).to(dev), conv_b=None if inp.conv_b is None else b16(inp.conv_b).to(dev),
             conv=(torch.from_numpy(inp.conv_state) if conv_f32 else b16(inp.conv_state)).to(dev),
-            ssm=gi.device_state_pool(num_slots, geo, 0.05, seed + 7, dev),
+            ssm=gi.device_state_pool(num_slots, geo, 0.05, seed + 7, dev,
+                                     dtype=torch.bfloat16 if state_bf16 else torch.float32),
             slot=torch.from_numpy(inp.slot).to(dev),
             out=torch.empty(B, geo.Hv, geo.dv, dtype=torch.bfloat16, device=dev),
             silu=silu, inp=inp)
@@ -252,6 +253,14 @@ def run_ours(args, rank, world):
             nb = decode_bytes(1024, geo, conv_f32=conv_f32)
             key = "1024_of_2048_" + ("f32cache" if conv_f32 else "bf16cache")
             sweep[key] = {"us": round(ms * 1e3, 2), "GBps": round(nb / ms / 1e6, 1)}
+            del t
+        # bf16 recurrent state: half the state bytes per row
+        for B, ns in ((HEADLINE_B, NUM_SLOTS), (1024, 2048)):
+            t = decode_setup(B, ns, seed=6, state_bf16=True)
+            ms = float(np.median(timed(lambda: decode_call(t), 20, 3)))
+            nb = decode_bytes(B, geo, state_bytes=2)
+            sweep[f"bf16state_{B}_of_{ns}"] = {"us": round(ms * 1e3, 2),
+                                               "GBps": round(nb / ms / 1e6, 1)}
             del t
         torch.cuda.empty_cache()
 

@@ -37,7 +37,7 @@ class GDNError(RuntimeError):
 class gdn_dims(ctypes.Structure):
     _fields_ = [("num_k_heads", ctypes.c_int32), ("num_v_heads", ctypes.c_int32),
                 ("head_k_dim", ctypes.c_int32), ("head_v_dim", ctypes.c_int32),
-                ("conv_width", ctypes.c_int32)]
+                ("conv_width", ctypes.c_int32), ("state_bf16", ctypes.c_int32)]
 
 
 @dataclass(frozen=True)
@@ -52,8 +52,15 @@ class Dims:
     def D(self) -> int:
         return 2 * self.Hk * self.dk + self.Hv * self.dv
 
-    def c(self) -> gdn_dims:
-        return gdn_dims(self.Hk, self.Hv, self.dk, self.dv, self.W)
+    def c(self, state_bf16: bool = False) -> gdn_dims:
+        return gdn_dims(self.Hk, self.Hv, self.dk, self.dv, self.W, int(bool(state_bf16)))
+
+
+def _sdims(dims: "Dims", ssm_state) -> gdn_dims:
+    """dims for a call: the state storage type follows the pool tensor's dtype."""
+    if ssm_state.dtype not in (torch.float32, torch.bfloat16):
+        raise ValueError("the recurrent state pool must be float32 or bfloat16")
+    return dims.c(ssm_state.dtype == torch.bfloat16)
 
 
 _lib = None
@@ -163,8 +170,9 @@ def gdn_decode_step(mixed_qkv, a, b, A_log, dt_bias, conv_weight, conv_bias, con
     _check(lib().gdn_decode_step(
         _ptr(mixed_qkv), _ptr(a), _ptr(b), _gate_mode(a), _ptr(A_log), _ptr(dt_bias),
         _ptr(conv_weight), _ptr(conv_bias), int(bool(silu)), _ptr(conv_state), conv_dt,
-        int(conv_layout), _ptr(ssm_state), _ptr(slot), B, ssm_state.shape[0], dims.c(),
-        float(scale), int(bool(qk_l2norm)), _ptr(out), _dt(out), _ptr(err), _stream(stream)))
+        int(conv_layout), _ptr(ssm_state), _ptr(slot), B, ssm_state.shape[0],
+        _sdims(dims, ssm_state), float(scale), int(bool(qk_l2norm)), _ptr(out), _dt(out),
+        _ptr(err), _stream(stream)))
 
 
 def gdn_chunked_prefill_workspace_size(total_tokens, num_seqs, dims: Dims, chunk=64) -> int:
@@ -185,8 +193,8 @@ def gdn_chunked_prefill(mixed_qkv, a, b, A_log, dt_bias, conv_weight, conv_bias,
         _ptr(mixed_qkv), _ptr(a), _ptr(b), _gate_mode(a), _ptr(A_log), _ptr(dt_bias),
         _ptr(conv_weight), _ptr(conv_bias), int(bool(silu)), _ptr(conv_state), conv_dt,
         int(conv_layout), _ptr(ssm_state), _ptr(cu_seqlens), _ptr(slot),
-        _ptr(has_initial_state), N, T, ssm_state.shape[0], dims.c(), float(scale),
-        int(bool(qk_l2norm)), int(chunk), _ptr(out), _dt(out), _ptr(workspace),
+        _ptr(has_initial_state), N, T, ssm_state.shape[0], _sdims(dims, ssm_state),
+        float(scale), int(bool(qk_l2norm)), int(chunk), _ptr(out), _dt(out), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _ptr(err), _stream(stream)))
 
 
@@ -208,8 +216,9 @@ def gdn_chunked_prefill_noalloc(mixed_qkv, a, b, A_log, dt_bias, conv_weight, co
         _ptr(mixed_qkv), _ptr(a), _ptr(b), _gate_mode(a), _ptr(A_log), _ptr(dt_bias),
         _ptr(conv_weight), _ptr(conv_bias), int(bool(silu)), _ptr(conv_state), conv_dt,
         int(conv_layout), _ptr(ssm_state), _ptr(cu_seqlens), _ptr(slot),
-        _ptr(has_initial_state), N, T, ssm_state.shape[0], dims.c(), float(scale),
-        int(bool(qk_l2norm)), int(chunk), _ptr(out), _dt(out), _ptr(err), _stream(stream)))
+        _ptr(has_initial_state), N, T, ssm_state.shape[0], _sdims(dims, ssm_state),
+        float(scale), int(bool(qk_l2norm)), int(chunk), _ptr(out), _dt(out), _ptr(err),
+        _stream(stream)))
 
 
 class DecodeGraph:
@@ -228,9 +237,9 @@ class DecodeGraph:
         _check(lib().gdn_decode_graph_create(
             _ptr(mixed_qkv), _ptr(a), _ptr(b), _gate_mode(a), _ptr(A_log), _ptr(dt_bias),
             _ptr(conv_weight), _ptr(conv_bias), int(bool(silu)), _ptr(conv_state), conv_dt,
-            int(conv_layout), _ptr(ssm_state), _ptr(slot), B, ssm_state.shape[0], dims.c(),
-            float(scale), int(bool(qk_l2norm)), _ptr(out), _dt(out), _ptr(err),
-            ctypes.byref(h)))
+            int(conv_layout), _ptr(ssm_state), _ptr(slot), B, ssm_state.shape[0],
+            _sdims(dims, ssm_state), float(scale), int(bool(qk_l2norm)), _ptr(out), _dt(out),
+            _ptr(err), ctypes.byref(h)))
         self._h = h
 
     def launch(self, stream=None):

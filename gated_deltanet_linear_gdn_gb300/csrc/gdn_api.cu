@@ -25,6 +25,7 @@ gdn_status check_layer(const void* mixed, const void* a, const void* b, gdn_gate
   if (d.num_k_heads <= 0 || d.num_v_heads <= 0 || d.head_k_dim <= 0 || d.head_v_dim <= 0)
     return GDN_ERR_INVALID_ARG;
   if (d.num_v_heads % d.num_k_heads != 0) return GDN_ERR_INVALID_ARG;
+  if (d.state_bf16 != 0 && d.state_bf16 != 1) return GDN_ERR_INVALID_ARG;
   if (num_slots < 1) return GDN_ERR_INVALID_ARG;
   if (gate_mode != GDN_GATE_FUSED && gate_mode != GDN_GATE_DIRECT) return GDN_ERR_INVALID_ARG;
   if (!valid_dtype(out_dtype)) return GDN_ERR_INVALID_ARG;
@@ -58,6 +59,7 @@ gdn_status check_layer(const void* mixed, const void* a, const void* b, gdn_gate
   la.conv_f32 = conv_dtype == GDN_F32;
   la.conv_layout = conv_layout;
   la.ssm = ssm;
+  la.ssm_bf16 = d.state_bf16;
   la.slot = slot;
   la.num_slots = num_slots;
   la.Hk = d.num_k_heads;

@@ -25,6 +25,11 @@ __device__ __forceinline__ uint16_t f2bf(float f) {
   return *reinterpret_cast<uint16_t*>(&b);
 }
 __device__ __forceinline__ float round_bf(float f) { return bf2f(f2bf(f)); }
+// Two floats -> two bf16 (round to nearest even) in one word, lo in the low half.
+__device__ __forceinline__ uint32_t pack_bf2(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
 
 // Unpack 8 bf16 values held in a uint4.
 __device__ __forceinline__ void unpack8(const uint4& u, float* f) {
@@ -66,51 +71,79 @@ __device__ __forceinline__ float silu_f(float x) { return __fdiv_rn(x, __fadd_rn
 // DIM_FIRST: [slots, D, 3] -> 24 contiguous entries; TAP_FIRST: [slots, 3, D].
 // win[ch][j], j = 0 oldest. Requires c0 % 8 == 0 and a 16-byte aligned pool.
 // ---------------------------------------------------------------------------
+// The packed window of 8 channels (24 values in the pool dtype) as 16-byte words,
+// so that several groups' loads can be in flight before any is unpacked.
 template <bool kF32Cache>
-__device__ __forceinline__ void load_conv8(const void* pool, int layout, int64_t slot, int D, int c0,
-                                           float (&win)[8][kConvW - 1]) {
+struct RawWin8 {
+  uint4 v[kF32Cache ? 6 : 3];
+};
+
+template <bool kF32Cache>
+__device__ __forceinline__ void load_conv8_raw(const void* pool, int layout, int64_t slot, int D,
+                                               int c0, RawWin8<kF32Cache>& r) {
+  constexpr int kEs = kF32Cache ? 4 : 2;
+  const char* base = static_cast<const char*>(pool);
   if (layout == GDN_CONV_DIM_FIRST) {
-    if (kF32Cache) {
-      const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(pool) +
-                                                        (slot * D + c0) * (kConvW - 1));
-      float v[24];
+    const uint4* p = reinterpret_cast<const uint4*>(base + (slot * D + c0) * (kConvW - 1) * kEs);
 #pragma unroll
-      for (int i = 0; i < 6; ++i) {
-        float4 t = p[i];
-        v[4 * i] = t.x; v[4 * i + 1] = t.y; v[4 * i + 2] = t.z; v[4 * i + 3] = t.w;
-      }
-#pragma unroll
-      for (int ch = 0; ch < 8; ++ch)
-#pragma unroll
-        for (int j = 0; j < 3; ++j) win[ch][j] = v[3 * ch + j];
-    } else {
-      const uint4* p = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(pool) +
-                                                      (slot * D + c0) * (kConvW - 1));
-      float v[24];
-#pragma unroll
-      for (int i = 0; i < 3; ++i) unpack8(p[i], v + 8 * i);
-#pragma unroll
-      for (int ch = 0; ch < 8; ++ch)
-#pragma unroll
-        for (int j = 0; j < 3; ++j) win[ch][j] = v[3 * ch + j];
-    }
+    for (int i = 0; i < (kF32Cache ? 6 : 3); ++i) r.v[i] = p[i];
   } else {
 #pragma unroll
     for (int j = 0; j < 3; ++j) {
-      const int64_t off = (slot * (kConvW - 1) + j) * D + c0;
+      const uint4* p = reinterpret_cast<const uint4*>(base + ((slot * (kConvW - 1) + j) * D + c0) * kEs);
       if (kF32Cache) {
-        const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(pool) + off);
-        float4 a = p[0], b = p[1];
-        win[0][j] = a.x; win[1][j] = a.y; win[2][j] = a.z; win[3][j] = a.w;
-        win[4][j] = b.x; win[5][j] = b.y; win[6][j] = b.z; win[7][j] = b.w;
+        r.v[2 * j] = p[0];
+        r.v[2 * j + 1] = p[1];
       } else {
-        float v[8];
-        unpack8(*reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(pool) + off), v);
-#pragma unroll
-        for (int ch = 0; ch < 8; ++ch) win[ch][j] = v[ch];
+        r.v[j] = p[0];
       }
     }
   }
+}
+
+template <bool kF32Cache>
+__device__ __forceinline__ void unpack_conv8(const RawWin8<kF32Cache>& r, int layout,
+                                             float (&win)[8][kConvW - 1]) {
+  if (layout == GDN_CONV_DIM_FIRST) {  // 24 values in (channel, tap) order
+    float v[24];
+#pragma unroll
+    for (int i = 0; i < (kF32Cache ? 6 : 3); ++i) {
+      if (kF32Cache) {
+        v[4 * i] = __uint_as_float(r.v[i].x); v[4 * i + 1] = __uint_as_float(r.v[i].y);
+        v[4 * i + 2] = __uint_as_float(r.v[i].z); v[4 * i + 3] = __uint_as_float(r.v[i].w);
+      } else {
+        unpack8(r.v[i], v + 8 * i);
+      }
+    }
+#pragma unroll
+    for (int ch = 0; ch < 8; ++ch)
+#pragma unroll
+      for (int j = 0; j < 3; ++j) win[ch][j] = v[3 * ch + j];
+  } else {  // one 8-channel vector per tap
+#pragma unroll
+    for (int j = 0; j < 3; ++j) {
+      float v[8];
+      if (kF32Cache) {
+        const uint4 a = r.v[2 * j], b = r.v[2 * j + 1];
+        v[0] = __uint_as_float(a.x); v[1] = __uint_as_float(a.y);
+        v[2] = __uint_as_float(a.z); v[3] = __uint_as_float(a.w);
+        v[4] = __uint_as_float(b.x); v[5] = __uint_as_float(b.y);
+        v[6] = __uint_as_float(b.z); v[7] = __uint_as_float(b.w);
+      } else {
+        unpack8(r.v[j], v);
+      }
+#pragma unroll
+      for (int ch = 0; ch < 8; ++ch) win[ch][j] = v[ch];
+    }
+  }
+}
+
+template <bool kF32Cache>
+__device__ __forceinline__ void load_conv8(const void* pool, int layout, int64_t slot, int D, int c0,
+                                           float (&win)[8][kConvW - 1]) {
+  RawWin8<kF32Cache> r;
+  load_conv8_raw<kF32Cache>(pool, layout, slot, D, c0, r);
+  unpack_conv8<kF32Cache>(r, layout, win);
 }
 
 // Store a window whose values are exactly representable in the pool dtype.
@@ -155,24 +188,31 @@ __device__ __forceinline__ void store_conv8(void* pool, int layout, int64_t slot
   }
 }
 
-// Conv of 8 channels [c0, c0+8) for one new input vector x8; rolls win in
-// place and returns the bf16-rounded outputs as floats.
-template <bool kF32Cache>
-__device__ __forceinline__ void conv8_step(float (&win)[8][kConvW - 1], const float (&x8)[8],
-                                           const uint16_t* __restrict__ weight,
-                                           const uint16_t* __restrict__ bias, int c0, bool silu,
-                                           float (&y8)[8]) {
-  float w[32];
+// Conv weights [8 channels][4 taps] and bias of one 8-channel group, packed bf16.
+struct ConvParams8 {
+  uint4 w[4];
+  uint4 b;
+};
+__device__ __forceinline__ ConvParams8 conv8_params(const uint16_t* __restrict__ weight,
+                                                    const uint16_t* __restrict__ bias, int c0) {
+  ConvParams8 p;
   const uint4* wp = reinterpret_cast<const uint4*>(weight + static_cast<int64_t>(c0) * kConvW);
 #pragma unroll
-  for (int i = 0; i < 4; ++i) unpack8(__ldg(wp + i), w + 8 * i);
-  float bv[8];
-  if (bias) {
-    unpack8(__ldg(reinterpret_cast<const uint4*>(bias + c0)), bv);
-  } else {
+  for (int i = 0; i < 4; ++i) p.w[i] = __ldg(wp + i);
+  p.b = bias ? __ldg(reinterpret_cast<const uint4*>(bias + c0)) : make_uint4(0u, 0u, 0u, 0u);
+  return p;
+}
+
+// Conv of 8 channels for one new input vector x8 with loaded parameters; rolls
+// win in place and returns the bf16-rounded outputs as floats. (A missing bias
+// loads as +0, the accumulator's start value either way.)
+template <bool kF32Cache>
+__device__ __forceinline__ void conv8_apply(float (&win)[8][kConvW - 1], const float (&x8)[8],
+                                            const ConvParams8& prm, bool silu, float (&y8)[8]) {
+  float w[32], bv[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) bv[i] = 0.0f;
-  }
+  for (int i = 0; i < 4; ++i) unpack8(prm.w[i], w + 8 * i);
+  unpack8(prm.b, bv);
 #pragma unroll
   for (int ch = 0; ch < 8; ++ch) {
     float full[kConvW] = {win[ch][0], win[ch][1], win[ch][2], x8[ch]};
@@ -186,24 +226,58 @@ __device__ __forceinline__ void conv8_step(float (&win)[8][kConvW - 1], const fl
   }
 }
 
+// Conv of 8 channels [c0, c0+8) for one new input vector x8; rolls win in
+// place and returns the bf16-rounded outputs as floats.
+template <bool kF32Cache>
+__device__ __forceinline__ void conv8_step(float (&win)[8][kConvW - 1], const float (&x8)[8],
+                                           const uint16_t* __restrict__ weight,
+                                           const uint16_t* __restrict__ bias, int c0, bool silu,
+                                           float (&y8)[8]) {
+  conv8_apply<kF32Cache>(win, x8, conv8_params(weight, bias, c0), silu, y8);
+}
+
 // ---------------------------------------------------------------------------
 // Gating (RL-Kernel PR #469, Notes "How the golden relates to the kernel",
 // item 1): fp32, softplus threshold at 20.
 // ---------------------------------------------------------------------------
+// The raw gate inputs of one (token, head), loaded ahead of their arithmetic so the
+// loads can overlap other work; gate_from_raw turns them into alpha = exp(g), beta.
+struct GateRaw {
+  float a, b, A_log, dt_bias;
+};
+__device__ __forceinline__ GateRaw gate_load(const void* a, const void* b, int gate_mode,
+                                             const float* A_log, const float* dt_bias,
+                                             int64_t idx, int h) {
+  GateRaw r;
+  if (gate_mode == GDN_GATE_DIRECT) {
+    r.a = static_cast<const float*>(a)[idx];
+    r.b = static_cast<const float*>(b)[idx];
+    r.A_log = r.dt_bias = 0.0f;
+  } else {
+    r.a = bf2f(static_cast<const uint16_t*>(a)[idx]);
+    r.b = bf2f(static_cast<const uint16_t*>(b)[idx]);
+    r.A_log = A_log[h];
+    r.dt_bias = dt_bias[h];
+  }
+  return r;
+}
+__device__ __forceinline__ void gate_from_raw(const GateRaw& r, int gate_mode, float& alpha,
+                                              float& beta) {
+  if (gate_mode == GDN_GATE_DIRECT) {
+    beta = r.b;
+    alpha = expf(r.a);
+  } else {
+    const float x = __fadd_rn(r.a, r.dt_bias);
+    const float sp = x > 20.0f ? x : log1pf(expf(x));
+    const float g = __fmul_rn(-expf(r.A_log), sp);
+    alpha = expf(g);
+    beta = __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-r.b)));
+  }
+}
 __device__ __forceinline__ void gate_values(const void* a, const void* b, int gate_mode,
                                             const float* A_log, const float* dt_bias, int64_t idx,
                                             int h, float& alpha, float& beta) {
-  if (gate_mode == GDN_GATE_DIRECT) {
-    const float g = static_cast<const float*>(a)[idx];
-    beta = static_cast<const float*>(b)[idx];
-    alpha = expf(g);
-  } else {
-    const float x = __fadd_rn(bf2f(static_cast<const uint16_t*>(a)[idx]), dt_bias[h]);
-    const float sp = x > 20.0f ? x : log1pf(expf(x));
-    const float g = __fmul_rn(-expf(A_log[h]), sp);
-    alpha = expf(g);
-    beta = __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-bf2f(static_cast<const uint16_t*>(b)[idx]))));
-  }
+  gate_from_raw(gate_load(a, b, gate_mode, A_log, dt_bias, idx, h), gate_mode, alpha, beta);
 }
 
 // log-space variant used by the chunked prefill (it needs g itself).

@@ -14,18 +14,29 @@
 // reader). The kernel is persistent -- one CTA per SM walks the units
 // c, c + G, c + 2G, ... -- and warp-specialised:
 //  - producer warp: streams each unit's state through a ring of shared-memory
-//    stages (32 rows each) with bulk copies (cp.async.bulk, the TMA engine),
+//    stages (64 rows each) with bulk copies (cp.async.bulk, the TMA engine),
 //    one "full" mbarrier per stage; it runs up to a ring's worth of stages
 //    (192 KB) ahead, so in-flight bytes cost no registers;
-//  - setup warps (one 8-channel conv group per thread): for the NEXT unit,
-//    compute the conv (rolling its window), the L2-normalised q and k, k.q
-//    and the gates into one of two buffers -- enough of them that this work
-//    stays shorter than streaming a unit's state;
-//  - 8 consumer warps: each takes 4 rows of every stage; a lane holds dk/32
-//    consecutive floats of a row; S k and S q (before the update) share one
-//    xor-shuffle butterfly, the read-out uses o = a (S q) + d (k . q) (equal to
-//    (a S + d k^T) q), and the new rows go from registers to global memory with
-//    128-bit streaming stores. Releasing a stage re-arms it for the producer.
+//  - 2 setup warps: per unit, the conv (rolling its windows), the
+//    L2-normalised q and k, k.q and the gates, written to a setup buffer; every
+//    global load of a unit (gate inputs, input channels, conv windows and
+//    parameters) is issued before anything waits on it. Two schemes, chosen by
+//    measurement: with an fp32 state the warps share each unit (one conv group
+//    per thread, a named barrier, two buffers) -- the shortest setup per unit;
+//    with a bf16 state, whose units stream in half the time, each warp
+//    prepares whole units (unit n to warp n % 2, buffer n % 4) so that two are
+//    in flight;
+//  - 8 consumer warps: each loads its 8 rows of a stage into registers (a lane
+//    holds dk/32 consecutive elements of a row) and hands the stage straight
+//    back to the producer. The 16 dot products (S k and S q before the update,
+//    per row) are summed in one transposed butterfly -- 15 exchanges that halve
+//    the values each lane holds, then one plain step -- instead of 16 separate
+//    5-step butterflies; a lane pair then holds both dots of its row, computes
+//    d = b (v - a S k) and o = a (S q) + d (k . q) (equal to (a S + d k^T) q),
+//    and the d's are broadcast for the row updates (packed f32x2 arithmetic),
+//    which go from registers to global memory with streaming stores.
+// The state may be stored as fp32 or bf16 (the arithmetic is fp32 either way; a
+// bf16 store rounds to nearest even), which halves the bytes a step moves.
 // Every row's arithmetic is the same whatever unit order or CTA runs it, so
 // results are bitwise independent of the batch composition. Every wait is
 // bounded (GDN_DEVERR_TIMEOUT on expiry; the waiting role stops).
@@ -38,8 +49,6 @@ namespace gdn {
 namespace {
 
 constexpr int kConsumerWarps = 8;
-constexpr int kStageRows = 32;
-constexpr int kRowsPerWarp = kStageRows / kConsumerWarps;  // 4
 constexpr int kRingBytes = 192 * 1024;
 
 template <int N> struct VecF;
@@ -62,23 +71,230 @@ template <> __device__ __forceinline__ float4 vec_from<4>(const float (&f)[4]) {
   return make_float4(f[0], f[1], f[2], f[3]);
 }
 
-template <int DK, int R>
+// One lane's VPL consecutive state elements of a row: fp32 in registers, stored as
+// fp32 or (bf16 state) bf16 rounded to nearest even.
+template <int VPL, bool kBf16State>
+struct StateIO;
+template <int VPL>
+struct StateIO<VPL, false> {
+  __device__ static void load(const void* row, int lane, float (&v)[VPL]) {
+    vec_to<VPL>(reinterpret_cast<const typename VecF<VPL>::T*>(row)[lane], v);
+  }
+  __device__ static void store(void* row, int lane, const float (&v)[VPL]) {
+    __stcs(reinterpret_cast<typename VecF<VPL>::T*>(row) + lane, vec_from<VPL>(v));
+  }
+};
+template <>
+struct StateIO<4, true> {
+  __device__ static void load(const void* row, int lane, float (&v)[4]) {
+    const uint2 u = reinterpret_cast<const uint2*>(row)[lane];
+    v[0] = __uint_as_float(u.x << 16); v[1] = __uint_as_float(u.x & 0xFFFF0000u);
+    v[2] = __uint_as_float(u.y << 16); v[3] = __uint_as_float(u.y & 0xFFFF0000u);
+  }
+  __device__ static void store(void* row, int lane, const float (&v)[4]) {
+    uint2 u;
+    u.x = pack_bf2(v[0], v[1]);
+    u.y = pack_bf2(v[2], v[3]);
+    __stcs(reinterpret_cast<uint2*>(row) + lane, u);
+  }
+};
+template <>
+struct StateIO<2, true> {
+  __device__ static void load(const void* row, int lane, float (&v)[2]) {
+    const uint32_t u = reinterpret_cast<const uint32_t*>(row)[lane];
+    v[0] = __uint_as_float(u << 16); v[1] = __uint_as_float(u & 0xFFFF0000u);
+  }
+  __device__ static void store(void* row, int lane, const float (&v)[2]) {
+    __stcs(reinterpret_cast<unsigned int*>(row) + lane, pack_bf2(v[0], v[1]));
+  }
+};
+template <>
+struct StateIO<1, true> {
+  __device__ static void load(const void* row, int lane, float (&v)[1]) {
+    v[0] = bf2f(reinterpret_cast<const uint16_t*>(row)[lane]);
+  }
+  __device__ static void store(void* row, int lane, const float (&v)[1]) {
+    reinterpret_cast<uint16_t*>(row)[lane] = f2bf(v[0]);
+  }
+};
+
+// A lane's share of a row dot product and of the row update, in packed f32x2
+// arithmetic where the lane holds an even number of elements.
+template <int VPL>
+__device__ __forceinline__ float lane_dot(const float (&s)[VPL], const float (&x)[VPL]) {
+  if constexpr (VPL == 1) {
+    return s[0] * x[0];
+  } else {
+    float2 acc = __fmul2_rn(make_float2(s[0], s[1]), make_float2(x[0], x[1]));
+#pragma unroll
+    for (int e = 2; e < VPL; e += 2)
+      acc = __ffma2_rn(make_float2(s[e], s[e + 1]), make_float2(x[e], x[e + 1]), acc);
+    return acc.x + acc.y;
+  }
+}
+// s <- al s + d k (each element: fma(d, k, al * s)).
+template <int VPL>
+__device__ __forceinline__ void lane_update(float (&s)[VPL], const float (&k)[VPL], float al,
+                                            float d) {
+  if constexpr (VPL == 1) {
+    s[0] = fmaf(d, k[0], al * s[0]);
+  } else {
+#pragma unroll
+    for (int e = 0; e < VPL; e += 2) {
+      const float2 r = __ffma2_rn(make_float2(d, d), make_float2(k[e], k[e + 1]),
+                                  __fmul2_rn(make_float2(al, al), make_float2(s[e], s[e + 1])));
+      s[e] = r.x;
+      s[e + 1] = r.y;
+    }
+  }
+}
+
+// Sums V per-lane values across the warp, V in {8, 16}: V-1 exchanges halve the
+// values a lane holds (at each level a lane keeps the half selected by its lane
+// bit and adds the partner's copy of it), then plain butterflies finish. On return
+// red[0] of lane L is the full sum of value L / (32 / V).
+template <int V>
+__device__ __forceinline__ void transposed_warp_sum(float (&red)[V], int lane) {
+  constexpr int LPV = 32 / V;
+#pragma unroll
+  for (int lvl = 0; (1 << lvl) < V; ++lvl) {
+    const int m = 16 >> lvl;
+    const int h = V >> (lvl + 1);
+    const bool up = (lane & m) != 0;
+#pragma unroll
+    for (int j = 0; j < h; ++j) {
+      const float keep = up ? red[h + j] : red[j];
+      const float give = up ? red[j] : red[h + j];
+      red[j] = keep + __shfl_xor_sync(0xffffffffu, give, m);
+    }
+  }
+#pragma unroll
+  for (int m = LPV / 2; m >= 1; m >>= 1) red[0] += __shfl_xor_sync(0xffffffffu, red[0], m);
+}
+
+template <int DK, int R, bool kBf16State>
 struct DecodeCfg {
   static constexpr int DV = DK;
+  static constexpr int kElemBytes = kBf16State ? 2 : 4;
+  static constexpr int kRowBytes = DK * kElemBytes;
   static constexpr int kUnitRows = R * DV;
+  // 64-row stages (8 rows per consumer warp), or the whole unit when it is smaller
+  static constexpr int kStageRows = kUnitRows < 64 ? kUnitRows : 64;
+  static constexpr int kRowsPerWarp = kStageRows / kConsumerWarps;
   static constexpr int kStagesPerUnit = kUnitRows / kStageRows;
-  static constexpr int kStageBytes = kStageRows * DK * 4;
+  static constexpr int kStageBytes = kStageRows * kRowBytes;
+  static_assert(kUnitRows % kStageRows == 0 && DV % kRowsPerWarp == 0, "stage tiling");
+  static_assert(kRowsPerWarp == 4 || kRowsPerWarp == 8, "the reduction handles 8 or 16 values");
+  // Setup scheme (both measured): with an fp32 state the setup warps share each
+  // unit (shortest time per unit; two buffers); with a bf16 state, whose units
+  // stream in half the time, each warp prepares whole units so that two are in
+  // flight (four buffers).
+  static constexpr bool kCoopSetup = !kBf16State;
   static constexpr int kNumStages = kRingBytes / kStageBytes;
   static constexpr int kGroups = (2 * DK + kUnitRows) / 8;  // 8-channel conv groups per unit
-  static constexpr int kSetupWarps = (kGroups + 31) / 32 < 4 ? (kGroups + 31) / 32 : 4;
+  static constexpr int kSetupWarps = 2;
+  static constexpr int kSetupBufs = kCoopSetup ? 2 : 2 * kSetupWarps;
   static constexpr int kThreads = 32 * (1 + kSetupWarps + kConsumerWarps);
   static constexpr int kSetupFloats = 2 * DK + kUnitRows + 2 * R + 1;  // q^, k^, v, a, b, k.q
   static constexpr int kSetupStride = (kSetupFloats + 31) / 32 * 32;
-  // dynamic shared memory: ring, two setup buffers, then the mbarriers
-  static constexpr int kBarOffset = kRingBytes + 2 * kSetupStride * 4;
-  static constexpr int kNumBars = 2 * kNumStages + 4;
+  // dynamic shared memory: ring, the setup buffers, then the mbarriers
+  static constexpr int kBarOffset = kRingBytes + kSetupBufs * kSetupStride * 4;
+  static constexpr int kNumBars = 2 * kNumStages + 2 * kSetupBufs;
   static constexpr int kSmemBytes = kBarOffset + kNumBars * 8;
+  static_assert(kSmemBytes <= 227 * 1024, "decode shared memory exceeds the per-CTA limit");
 };
+
+// Conv group g (8 channels) of unit (row b, k-head kh): its first channel in the
+// packed q|k|v vector and its slot in the setup buffer (q^, k^, v).
+template <int DK, int R>
+__device__ __forceinline__ void group_channels(int g, int kh, int Hk, float* buf, int& c0,
+                                               float*& dst) {
+  constexpr int QG = DK / 8;
+  if (g < QG) { c0 = kh * DK + 8 * g; dst = buf + 8 * g; }
+  else if (g < 2 * QG) { c0 = (Hk + kh) * DK + 8 * (g - QG); dst = buf + DK + 8 * (g - QG); }
+  else { c0 = 2 * Hk * DK + kh * R * DK + 8 * (g - 2 * QG); dst = buf + 2 * DK + 8 * (g - 2 * QG); }
+}
+
+// Every global load of one conv group: the input channels, the conv window and
+// the conv parameters (issued together, before anything waits on them).
+template <bool kF32Cache>
+struct GroupLoads {
+  uint4 x;
+  RawWin8<kF32Cache> win;
+  ConvParams8 prm;
+};
+template <bool kF32Cache>
+__device__ __forceinline__ void group_load(const LayerArgs& a, const uint16_t* xrow, int32_t s,
+                                           int c0, GroupLoads<kF32Cache>& L) {
+  L.x = __ldg(reinterpret_cast<const uint4*>(xrow + c0));
+  if (a.conv_w) {
+    load_conv8_raw<kF32Cache>(a.conv_state, a.conv_layout, s, a.D, c0, L.win);
+    L.prm = conv8_params(static_cast<const uint16_t*>(a.conv_w),
+                         static_cast<const uint16_t*>(a.conv_b), c0);
+  }
+}
+// The group's conv (rolling and storing its window) into dst[0..8).
+template <bool kF32Cache>
+__device__ __forceinline__ void group_conv(const LayerArgs& a, int32_t s, int c0,
+                                           const GroupLoads<kF32Cache>& L, float* dst) {
+  float x8[8];
+  unpack8(L.x, x8);
+  if (a.conv_w) {
+    float win[8][kConvW - 1], y8[8];
+    unpack_conv8<kF32Cache>(L.win, a.conv_layout, win);
+    conv8_apply<kF32Cache>(win, x8, L.prm, a.silu != 0, y8);
+    store_conv8<kF32Cache>(a.conv_state, a.conv_layout, s, a.D, c0, win);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) dst[i] = y8[i];
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) dst[i] = x8[i];
+  }
+}
+
+// One warp, after the conv outputs are in the buffer: L2-normalise q (then scale)
+// and k in place, k.q and the gates of the unit's R heads (raw inputs in lanes < R).
+template <int DK, int R>
+__device__ __forceinline__ void finish_setup(const LayerArgs& a, float* buf, const GateRaw& gr,
+                                             int lane) {
+  constexpr int VPL = DK / 32;
+  float* qb = buf;
+  float* kb = buf + DK;
+  float* gb = buf + 2 * DK + R * DK;  // a[R], b[R], k.q
+  float qv[VPL], kv[VPL], sq = 0.0f, sk = 0.0f;
+#pragma unroll
+  for (int e = 0; e < VPL; ++e) {
+    qv[e] = qb[lane * VPL + e];
+    kv[e] = kb[lane * VPL + e];
+    sq = fmaf(qv[e], qv[e], sq);
+    sk = fmaf(kv[e], kv[e], sk);
+  }
+  sq = warp_sum(sq);
+  sk = warp_sum(sk);
+  const float iq = a.qk_l2norm ? 1.0f / sqrtf(sq + 1e-6f) : 1.0f;
+  const float ik = a.qk_l2norm ? 1.0f / sqrtf(sk + 1e-6f) : 1.0f;
+  float kq = 0.0f;
+#pragma unroll
+  for (int e = 0; e < VPL; ++e) {
+    qv[e] = (qv[e] * iq) * a.scale;
+    kv[e] = kv[e] * ik;
+    kq = fmaf(kv[e], qv[e], kq);
+  }
+  kq = warp_sum(kq);
+  __syncwarp();
+#pragma unroll
+  for (int e = 0; e < VPL; ++e) {
+    qb[lane * VPL + e] = qv[e];
+    kb[lane * VPL + e] = kv[e];
+  }
+  if (lane < R) {
+    float al, be;
+    gate_from_raw(gr, a.gate_mode, al, be);
+    gb[lane] = al;
+    gb[R + lane] = be;
+  }
+  if (lane == 0) gb[2 * R] = kq;
+}
 
 __device__ __forceinline__ bool unit_active(int32_t s, int num_slots) {
   return s > 0 && s < num_slots;
@@ -88,23 +304,46 @@ __device__ __forceinline__ void setup_barrier(int nthreads) {
   asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
 }
 
-template <int DK, int R, bool kF32Cache>
-__global__ void __launch_bounds__(DecodeCfg<DK, R>::kThreads, 1)
+// The slots of this CTA's units (unit i is blockIdx.x + i * gridDim.x) for one
+// warp: read 32 units at a time (lane j holds unit i0 + j's slot) with the next
+// 32 already in flight, and handed out by shuffle -- so walking the units costs no
+// dependent global load per unit. Every lane of the warp must call get().
+struct UnitSlots {
+  int base = -64;
+  int32_t cur = 0, nxt = 0;
+  __device__ __forceinline__ int32_t load(const LayerArgs& a, int i0, int num_units, int lane) {
+    const int u = blockIdx.x + (i0 + lane) * static_cast<int>(gridDim.x);
+    return u < num_units ? a.slot[u / a.Hk] : 0;
+  }
+  __device__ __forceinline__ int32_t get(const LayerArgs& a, int i, int num_units, int lane) {
+    const int b0 = i & ~31;
+    if (b0 != base) {
+      cur = (b0 == base + 32) ? nxt : load(a, b0, num_units, lane);
+      base = b0;
+      nxt = load(a, b0 + 32, num_units, lane);
+    }
+    return __shfl_sync(0xffffffffu, cur, i & 31);
+  }
+};
+
+template <int DK, int R, bool kF32Cache, bool kBf16State>
+__global__ void __launch_bounds__(DecodeCfg<DK, R, kBf16State>::kThreads, 1)
     decode_kernel(LayerArgs a, int num_units) {
-  using Cfg = DecodeCfg<DK, R>;
+  using Cfg = DecodeCfg<DK, R, kBf16State>;
+  using IO = StateIO<DK / 32, kBf16State>;
   constexpr int DV = Cfg::DV;
   constexpr int VPL = DK / 32;
   constexpr int NS = Cfg::kNumStages;
   constexpr int SW = Cfg::kSetupWarps;
-  using V = typename VecF<VPL>::T;
+  constexpr int NB = Cfg::kSetupBufs;
 
   extern __shared__ __align__(1024) unsigned char smem[];
-  float* ring = reinterpret_cast<float*>(smem);
+  unsigned char* ring = smem;
   float* setup = reinterpret_cast<float*>(smem + kRingBytes);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Cfg::kBarOffset);
-  // bars: full[NS], empty[NS], setup_full[2], setup_empty[2]
+  // bars: full[NS], empty[NS], setup_full[NB], setup_empty[NB]
   const uint32_t full0 = smem_addr(bars), empty0 = smem_addr(bars + NS);
-  const uint32_t sfull0 = smem_addr(bars + 2 * NS), sempty0 = smem_addr(bars + 2 * NS + 2);
+  const uint32_t sfull0 = smem_addr(bars + 2 * NS), sempty0 = smem_addr(bars + 2 * NS + NB);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (tid == 0) {
@@ -112,8 +351,8 @@ __global__ void __launch_bounds__(DecodeCfg<DK, R>::kThreads, 1)
       mbar_init(full0 + 8 * i, 1);
       mbar_init(empty0 + 8 * i, kConsumerWarps);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(sfull0 + 8 * i, 32 * SW);
+    for (int i = 0; i < NB; ++i) {
+      mbar_init(sfull0 + 8 * i, Cfg::kCoopSetup ? 32 * SW : 32);
       mbar_init(sempty0 + 8 * i, kConsumerWarps);
     }
     fence_mbar_init();
@@ -125,132 +364,165 @@ __global__ void __launch_bounds__(DecodeCfg<DK, R>::kThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      uint32_t g = 0;  // stages issued so far
-      for (int u = blockIdx.x; u < num_units; u += G) {
-        const int b = u / a.Hk, kh = u % a.Hk;
-        const int32_t s = a.slot[b];
-        if (!unit_active(s, a.num_slots)) continue;
-        const float* src = a.ssm + (static_cast<int64_t>(s) * a.Hv + kh * R) * (DV * DK);
-        bool ok = true;
+    // The warp walks the units (for the slot batches); lane 0 issues the copies.
+    UnitSlots slots;
+    uint32_t g = 0;  // stages issued so far (lane 0)
+    bool ok = true;
+    for (int i = 0, u = blockIdx.x; u < num_units && ok; ++i, u += G) {
+      const int kh = u % a.Hk;
+      const int32_t s = slots.get(a, i, num_units, lane);
+      if (!unit_active(s, a.num_slots)) continue;
+      if (lane == 0) {
+        const unsigned char* src = reinterpret_cast<const unsigned char*>(a.ssm) +
+                                   (static_cast<int64_t>(s) * a.Hv + kh * R) * (DV * Cfg::kRowBytes);
         for (int k = 0; k < Cfg::kStagesPerUnit; ++k, ++g) {
           const uint32_t r = g % NS, c = g / NS;
           if (!mbar_wait_bounded(empty0 + 8 * r, (c & 1) ^ 1)) { ok = false; break; }
           mbar_arrive_expect_tx(full0 + 8 * r, Cfg::kStageBytes);
-          bulk_g2s(smem_addr(ring + static_cast<size_t>(r) * kStageRows * DK),
-                   src + static_cast<int64_t>(k) * kStageRows * DK, Cfg::kStageBytes, full0 + 8 * r);
-        }
-        if (!ok) {
-          if (a.err) atomicOr(a.err, GDN_DEVERR_TIMEOUT);
-          break;
+          bulk_g2s(smem_addr(ring + static_cast<size_t>(r) * Cfg::kStageBytes),
+                   src + static_cast<int64_t>(k) * Cfg::kStageBytes, Cfg::kStageBytes, full0 + 8 * r);
         }
       }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
     }
+    if (!ok && lane == 0 && a.err) atomicOr(a.err, GDN_DEVERR_TIMEOUT);
     return;
   }
 
   if (warp >= 1 && warp <= SW) {
     // ------------------------------------------------------------ setup
-    // SW warps, one 8-channel conv group per thread; they meet at a named
-    // barrier, then warp 1 normalises q and k and computes k.q and the gates.
-    // Every setup thread passes every barrier even after a timeout, so none
-    // can be left waiting on a named barrier.
-    constexpr int QG = DK / 8;
     constexpr int NG = Cfg::kGroups;
-    const int st = tid - 32;  // 0 .. 32*SW-1
-    bool failed = false;
-    uint32_t n = 0;  // active units prepared so far
-    for (int u = blockIdx.x; u < num_units; u += G) {
-      const int b = u / a.Hk, kh = u % a.Hk;
-      const int32_t s = a.slot[b];
-      if (!unit_active(s, a.num_slots)) {
-        if (s >= a.num_slots && st == 0 && kh == 0 && a.err) atomicOr(a.err, GDN_DEVERR_SLOT_RANGE);
-        continue;
-      }
-      const uint32_t p = n & 1, use = n >> 1;
-      if (!failed && !mbar_wait_bounded(sempty0 + 8 * p, (use & 1) ^ 1)) {
-        if (a.err) atomicOr(a.err, GDN_DEVERR_TIMEOUT);
-        failed = true;
-      }
-      float* buf = setup + p * Cfg::kSetupStride;
-      float* qb = buf;
-      float* kb = buf + DK;
-      float* vb = buf + 2 * DK;
-      float* gb = buf + 2 * DK + Cfg::kUnitRows;  // a[R], b[R], k.q
-      if (!failed) {
-        const uint16_t* xrow = static_cast<const uint16_t*>(a.mixed) + static_cast<int64_t>(b) * a.D;
-        for (int g = st; g < NG; g += 32 * SW) {
-          int c0;
-          float* dst;
-          if (g < QG) { c0 = kh * DK + 8 * g; dst = qb + 8 * g; }
-          else if (g < 2 * QG) { c0 = (a.Hk + kh) * DK + 8 * (g - QG); dst = kb + 8 * (g - QG); }
-          else { c0 = 2 * a.Hk * DK + kh * R * DV + 8 * (g - 2 * QG); dst = vb + 8 * (g - 2 * QG); }
-          float x8[8];
-          unpack8(__ldg(reinterpret_cast<const uint4*>(xrow + c0)), x8);
-          if (a.conv_w) {
-            float win[8][kConvW - 1], y8[8];
-            load_conv8<kF32Cache>(a.conv_state, a.conv_layout, s, a.D, c0, win);
-            conv8_step<kF32Cache>(win, x8, static_cast<const uint16_t*>(a.conv_w),
-                                  static_cast<const uint16_t*>(a.conv_b), c0, a.silu != 0, y8);
-            store_conv8<kF32Cache>(a.conv_state, a.conv_layout, s, a.D, c0, win);
+    uint32_t n = 0;  // ordinal of the next active unit
+    if constexpr (Cfg::kCoopSetup) {
+      // The SW warps share each unit, one conv group per thread; they meet at a
+      // named barrier, then the first setup warp normalises q and k and writes
+      // k.q and the gates. This scheme waits for its buffer before loading and
+      // loads the gate inputs last: with an fp32 state (HBM-saturated) that
+      // measured faster than issuing the unit's loads early. Every setup thread
+      // passes every barrier even after a timeout, so none is left waiting on
+      // the named barrier.
+      const int st = tid - 32;  // 0 .. 32*SW-1
+      bool failed = false;
+      for (int u = blockIdx.x; u < num_units; u += G) {
+        const int b = u / a.Hk, kh = u % a.Hk;
+        const int32_t s = a.slot[b];
+        if (!unit_active(s, a.num_slots)) {
+          if (s >= a.num_slots && st == 0 && kh == 0 && a.err) atomicOr(a.err, GDN_DEVERR_SLOT_RANGE);
+          continue;
+        }
+        const uint32_t p = n % NB, use = n / NB;
+        if (!failed && !mbar_wait_bounded(sempty0 + 8 * p, (use & 1) ^ 1)) {
+          if (a.err) atomicOr(a.err, GDN_DEVERR_TIMEOUT);
+          failed = true;
+        }
+        float* buf = setup + p * Cfg::kSetupStride;
+        if (!failed) {
+          const uint16_t* xrow = static_cast<const uint16_t*>(a.mixed) + static_cast<int64_t>(b) * a.D;
+          for (int g = st; g < NG; g += 32 * SW) {
+            int c0;
+            float* dst;
+            group_channels<DK, R>(g, kh, a.Hk, buf, c0, dst);
+            float x8[8];
+            unpack8(__ldg(reinterpret_cast<const uint4*>(xrow + c0)), x8);
+            if (a.conv_w) {
+              float win[8][kConvW - 1], y8[8];
+              load_conv8<kF32Cache>(a.conv_state, a.conv_layout, s, a.D, c0, win);
+              conv8_step<kF32Cache>(win, x8, static_cast<const uint16_t*>(a.conv_w),
+                                    static_cast<const uint16_t*>(a.conv_b), c0, a.silu != 0, y8);
+              store_conv8<kF32Cache>(a.conv_state, a.conv_layout, s, a.D, c0, win);
 #pragma unroll
-            for (int i = 0; i < 8; ++i) dst[i] = y8[i];
-          } else {
+              for (int i = 0; i < 8; ++i) dst[i] = y8[i];
+            } else {
 #pragma unroll
-            for (int i = 0; i < 8; ++i) dst[i] = x8[i];
+              for (int i = 0; i < 8; ++i) dst[i] = x8[i];
+            }
           }
         }
+        setup_barrier(32 * SW);
+        if (warp == 1 && !__any_sync(0xffffffffu, failed)) {
+          GateRaw gr{};
+          if (lane < R) {
+            const int h = kh * R + lane;
+            gr = gate_load(a.a, a.b, a.gate_mode, a.A_log, a.dt_bias,
+                           static_cast<int64_t>(b) * a.Hv + h, h);
+          }
+          finish_setup<DK, R>(a, buf, gr, lane);
+        }
+        mbar_arrive(sfull0 + 8 * p);  // every setup thread: its writes are released
+        ++n;
       }
-      if (SW > 1) setup_barrier(32 * SW);
-      else __syncwarp();
-      if (warp == 1 && !failed) {
-        float qv[VPL], kv[VPL], sq = 0.0f, sk = 0.0f;
-#pragma unroll
-        for (int e = 0; e < VPL; ++e) {
-          qv[e] = qb[lane * VPL + e];
-          kv[e] = kb[lane * VPL + e];
-          sq = fmaf(qv[e], qv[e], sq);
-          sk = fmaf(kv[e], kv[e], sk);
+    } else {
+      // Each warp prepares whole units: active unit n goes to warp n % SW and
+      // buffer n % NB. The loads of up to two conv groups per lane are in flight
+      // before the warp waits for its buffer.
+      constexpr int NGL = (NG + 31) / 32;  // conv groups per lane
+      const int w = warp - 1;
+      UnitSlots slots;
+      for (int i = 0, u = blockIdx.x; u < num_units; ++i, u += G) {
+        const int b = u / a.Hk, kh = u % a.Hk;
+        const int32_t s = slots.get(a, i, num_units, lane);
+        if (!unit_active(s, a.num_slots)) {
+          if (s >= a.num_slots && w == 0 && lane == 0 && kh == 0 && a.err)
+            atomicOr(a.err, GDN_DEVERR_SLOT_RANGE);
+          continue;
         }
-        sq = warp_sum(sq);
-        sk = warp_sum(sk);
-        const float iq = a.qk_l2norm ? 1.0f / sqrtf(sq + 1e-6f) : 1.0f;
-        const float ik = a.qk_l2norm ? 1.0f / sqrtf(sk + 1e-6f) : 1.0f;
-        float kq = 0.0f;
-#pragma unroll
-        for (int e = 0; e < VPL; ++e) {
-          qv[e] = (qv[e] * iq) * a.scale;
-          kv[e] = kv[e] * ik;
-          kq = fmaf(kv[e], qv[e], kq);
-        }
-        kq = warp_sum(kq);
-#pragma unroll
-        for (int e = 0; e < VPL; ++e) {
-          qb[lane * VPL + e] = qv[e];
-          kb[lane * VPL + e] = kv[e];
-        }
+        const uint32_t my = n++;
+        if (static_cast<int>(my % SW) != w) continue;
+        const uint32_t p = my % NB, use = my / NB;
+        float* buf = setup + p * Cfg::kSetupStride;
+        GateRaw gr{};
         if (lane < R) {
           const int h = kh * R + lane;
-          float al, be;
-          gate_values(a.a, a.b, a.gate_mode, a.A_log, a.dt_bias,
-                      static_cast<int64_t>(b) * a.Hv + h, h, al, be);
-          gb[lane] = al;
-          gb[R + lane] = be;
+          gr = gate_load(a.a, a.b, a.gate_mode, a.A_log, a.dt_bias,
+                         static_cast<int64_t>(b) * a.Hv + h, h);
         }
-        if (lane == 0) gb[2 * R] = kq;
+        const uint16_t* xrow = static_cast<const uint16_t*>(a.mixed) + static_cast<int64_t>(b) * a.D;
+        bool waited = false, failed = false;
+#pragma unroll
+        for (int j0 = 0; j0 < NGL; j0 += 2) {
+          GroupLoads<kF32Cache> L[2];
+          int c0[2];
+          float* dst[2];
+          bool on[2];
+#pragma unroll
+          for (int jj = 0; jj < 2; ++jj) {
+            const int g = lane + 32 * (j0 + jj);
+            on[jj] = (j0 + jj < NGL) && g < NG;
+            c0[jj] = 0;
+            dst[jj] = buf;
+            if (on[jj]) {
+              group_channels<DK, R>(g, kh, a.Hk, buf, c0[jj], dst[jj]);
+              group_load<kF32Cache>(a, xrow, s, c0[jj], L[jj]);
+            }
+          }
+          if (!waited) {  // the buffer must be free before it is written
+            waited = true;
+            if (!mbar_wait_bounded(sempty0 + 8 * p, (use & 1) ^ 1)) { failed = true; break; }
+          }
+#pragma unroll
+          for (int jj = 0; jj < 2; ++jj)
+            if (on[jj]) group_conv<kF32Cache>(a, s, c0[jj], L[jj], dst[jj]);
+        }
+        if (__any_sync(0xffffffffu, failed)) {  // the consumers time out on this buffer too
+          if (lane == 0 && a.err) atomicOr(a.err, GDN_DEVERR_TIMEOUT);
+          return;
+        }
+        __syncwarp();
+        finish_setup<DK, R>(a, buf, gr, lane);
+        mbar_arrive(sfull0 + 8 * p);  // every lane: its writes are released
       }
-      mbar_arrive(sfull0 + 8 * p);  // every setup thread: its writes are released
-      ++n;
     }
     return;
   }
 
   // -------------------------------------------------------------- consumers
   const int cw = warp - 1 - SW;
+  constexpr int RPW = Cfg::kRowsPerWarp;
   uint32_t g = 0, n = 0;
-  for (int u = blockIdx.x; u < num_units; u += G) {
+  UnitSlots slots;
+  for (int i = 0, u = blockIdx.x; u < num_units; ++i, u += G) {
     const int b = u / a.Hk, kh = u % a.Hk;
-    const int32_t s = a.slot[b];
+    const int32_t s = slots.get(a, i, num_units, lane);
     const int64_t out_base = (static_cast<int64_t>(b) * a.Hv + kh * R) * DV;
     if (!unit_active(s, a.num_slots)) {  // inactive / invalid row: zero outputs, no state touched
       for (int i = cw * 32 + lane; i < per_unit_rows; i += kConsumerWarps * 32) {
@@ -259,8 +531,9 @@ __global__ void __launch_bounds__(DecodeCfg<DK, R>::kThreads, 1)
       }
       continue;
     }
-    const uint32_t p = n & 1;
-    if (!mbar_wait_bounded(sfull0 + 8 * p, (n >> 1) & 1)) {
+    const uint32_t p = n % NB;
+    // warp-uniform waits: a timed-out warp leaves as a whole (it shuffles below)
+    if (!__all_sync(0xffffffffu, mbar_wait_bounded(sfull0 + 8 * p, (n / NB) & 1))) {
       if (lane == 0 && a.err) atomicOr(a.err, GDN_DEVERR_TIMEOUT);
       return;
     }
@@ -274,46 +547,50 @@ __global__ void __launch_bounds__(DecodeCfg<DK, R>::kThreads, 1)
     const float* vb = buf + 2 * DK;
     const float* gb = buf + 2 * DK + per_unit_rows;
     const float kq = gb[2 * R];
-    float* dst_base = a.ssm + (static_cast<int64_t>(s) * a.Hv + kh * R) * (DV * DK);
+    unsigned char* dst_base = reinterpret_cast<unsigned char*>(a.ssm) +
+                              (static_cast<int64_t>(s) * a.Hv + kh * R) * (DV * Cfg::kRowBytes);
     for (int k = 0; k < Cfg::kStagesPerUnit; ++k, ++g) {
       const uint32_t r = g % NS, c = g / NS;
-      if (!mbar_wait_bounded(full0 + 8 * r, c & 1)) {
+      if (!__all_sync(0xffffffffu, mbar_wait_bounded(full0 + 8 * r, c & 1))) {
         if (lane == 0 && a.err) atomicOr(a.err, GDN_DEVERR_TIMEOUT);
         return;
       }
-      const int row0 = k * kStageRows + cw * kRowsPerWarp;
+      const int row0 = k * Cfg::kStageRows + cw * RPW;
       const int hl = row0 / DV;
       const float al = gb[hl], be = gb[R + hl];
-      const float* src = ring + static_cast<size_t>(r) * kStageRows * DK + cw * kRowsPerWarp * DK;
-      float o[kRowsPerWarp];
+      const unsigned char* src = ring + static_cast<size_t>(r) * Cfg::kStageBytes +
+                                 cw * RPW * Cfg::kRowBytes;
+      // this warp's rows -> registers; the stage goes back to the producer at once
+      float sv[RPW][VPL];
 #pragma unroll
-      for (int i = 0; i < kRowsPerWarp; ++i) {
-        float sv[VPL];
-        vec_to<VPL>(reinterpret_cast<const V*>(src + i * DK)[lane], sv);
-        float pk = 0.0f, pq = 0.0f;
-#pragma unroll
-        for (int e = 0; e < VPL; ++e) { pk = fmaf(sv[e], kv[e], pk); pq = fmaf(sv[e], qv[e], pq); }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-          pk += __shfl_xor_sync(0xffffffffu, pk, off);
-          pq += __shfl_xor_sync(0xffffffffu, pq, off);
-        }
-        const float delta = be * (vb[row0 + i] - al * pk);
-        float nw[VPL];
-#pragma unroll
-        for (int e = 0; e < VPL; ++e) nw[e] = fmaf(delta, kv[e], al * sv[e]);
-        __stcs(reinterpret_cast<V*>(dst_base + static_cast<int64_t>(row0 + i) * DK) + lane,
-               vec_from<VPL>(nw));
-        o[i] = fmaf(delta, kq, al * pq);
-      }
+      for (int i = 0; i < RPW; ++i) IO::load(src + i * Cfg::kRowBytes, lane, sv[i]);
       __syncwarp();
-      if (lane == 0) mbar_arrive(empty0 + 8 * r);  // this warp is done with the stage
-      if (lane < kRowsPerWarp) {
-        float ov = o[0];
+      if (lane == 0) mbar_arrive(empty0 + 8 * r);
+      // (S k)_i and (S q)_i of the warp's rows, as values 2i and 2i+1
+      float red[2 * RPW];
 #pragma unroll
-        for (int i = 1; i < kRowsPerWarp; ++i) ov = (lane == i) ? o[i] : ov;
-        if (a.out_f32) static_cast<float*>(a.out)[out_base + row0 + lane] = ov;
-        else static_cast<uint16_t*>(a.out)[out_base + row0 + lane] = f2bf(ov);
+      for (int i = 0; i < RPW; ++i) {
+        red[2 * i] = lane_dot<VPL>(sv[i], kv);
+        red[2 * i + 1] = lane_dot<VPL>(sv[i], qv);
+      }
+      transposed_warp_sum<2 * RPW>(red, lane);
+      // lanes of value pair i (row i) swap halves: both then hold (S k)_i and (S q)_i
+      constexpr int LPV = 32 / (2 * RPW);
+      const float other = __shfl_xor_sync(0xffffffffu, red[0], LPV);
+      const bool is_q = ((lane / LPV) & 1) != 0;
+      const float pk = is_q ? other : red[0], pq = is_q ? red[0] : other;
+      const int ri = lane / (2 * LPV);
+      const float delta = be * (vb[row0 + ri] - al * pk);
+      if (lane % (2 * LPV) == 0) {  // o_i = a (S q)_i + d_i (k . q)
+        const float ov = fmaf(delta, kq, al * pq);
+        if (a.out_f32) static_cast<float*>(a.out)[out_base + row0 + ri] = ov;
+        else static_cast<uint16_t*>(a.out)[out_base + row0 + ri] = f2bf(ov);
+      }
+#pragma unroll
+      for (int i = 0; i < RPW; ++i) {
+        const float d = __shfl_sync(0xffffffffu, delta, i * 2 * LPV);
+        lane_update<VPL>(sv[i], kv, al, d);
+        IO::store(dst_base + static_cast<int64_t>(row0 + i) * Cfg::kRowBytes, lane, sv[i]);
       }
     }
     __syncwarp();
@@ -335,10 +612,10 @@ int sm_count() {
   return count[dev];
 }
 
-template <int DK, int R, bool kF32Cache>
+template <int DK, int R, bool kF32Cache, bool kBf16State>
 cudaError_t launch_one(const LayerArgs& a, int B, cudaStream_t s) {
-  using Cfg = DecodeCfg<DK, R>;
-  auto kern = decode_kernel<DK, R, kF32Cache>;
+  using Cfg = DecodeCfg<DK, R, kBf16State>;
+  auto kern = decode_kernel<DK, R, kF32Cache, kBf16State>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        Cfg::kSmemBytes);
   if (e != cudaSuccess) return e;
@@ -350,8 +627,12 @@ cudaError_t launch_one(const LayerArgs& a, int B, cudaStream_t s) {
 
 template <int DK, int R>
 cudaError_t launch_dk_r(const LayerArgs& a, int B, cudaStream_t s) {
-  if (a.conv_f32) return launch_one<DK, R, true>(a, B, s);
-  return launch_one<DK, R, false>(a, B, s);
+  if (a.ssm_bf16) {
+    if (a.conv_f32) return launch_one<DK, R, true, true>(a, B, s);
+    return launch_one<DK, R, false, true>(a, B, s);
+  }
+  if (a.conv_f32) return launch_one<DK, R, true, false>(a, B, s);
+  return launch_one<DK, R, false, false>(a, B, s);
 }
 
 template <int DK>

@@ -39,7 +39,8 @@ struct LayerArgs {
   void* conv_state;
   int conv_f32;
   int conv_layout;
-  float* ssm;  // [num_slots, Hv, dv, dk]
+  float* ssm;  // [num_slots, Hv, dv, dk], fp32 or (ssm_bf16) bf16 data
+  int ssm_bf16;
   const int32_t* slot;
   int num_slots;
   int Hk, Hv, dk, dv, D;

@@ -281,9 +281,11 @@ __global__ void __launch_bounds__(kPreThreads)
   const int kh = h / (a.Hv / a.Hk);
   const int32_t slot = a.slot[i];
   const bool init = (p.has_init == nullptr) || (p.has_init[i] != 0);
-  float* Sg = a.ssm + (static_cast<int64_t>(slot) * a.Hv + h) * DV * DK + static_cast<int64_t>(r0) * DK;
+  const int64_t soff = (static_cast<int64_t>(slot) * a.Hv + h) * DV * DK + static_cast<int64_t>(r0) * DK;
+  float* Sg = a.ssm + soff;                                  // fp32 state
+  uint16_t* Sb = reinterpret_cast<uint16_t*>(a.ssm) + soff;  // bf16 state
   for (int idx = tid; idx < DVS * DK; idx += kPreThreads)
-    Ss[(idx / DK) * KP + idx % DK] = init ? Sg[idx] : 0.0f;
+    Ss[(idx / DK) * KP + idx % DK] = init ? (a.ssm_bf16 ? bf2f(Sb[idx]) : Sg[idx]) : 0.0f;
 
   const int qc = kh * DK, kc = (a.Hk + kh) * DK;
   for (int c = chunk_off[i]; c < chunk_off[i + 1]; ++c) {
@@ -398,7 +400,11 @@ __global__ void __launch_bounds__(kPreThreads)
     }
   }
   __syncthreads();
-  for (int idx = tid; idx < DVS * DK; idx += kPreThreads) Sg[idx] = Ss[(idx / DK) * KP + idx % DK];
+  for (int idx = tid; idx < DVS * DK; idx += kPreThreads) {
+    const float v = Ss[(idx / DK) * KP + idx % DK];
+    if (a.ssm_bf16) Sb[idx] = f2bf(v);  // rounded to bf16 only here, at the write-back
+    else Sg[idx] = v;
+  }
 }
 
 template <int DK>

@@ -556,12 +556,24 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     if (nch > 0) { issue_A(0); issue_B(0); }
   }
   // state (half a row per thread) -> registers and the split operand tiles
-  float* Sg = a.ssm + (static_cast<int64_t>(slot) * a.Hv + h) * (kD * kD) + r * kD + half * 64;
+  const int64_t soff = (static_cast<int64_t>(slot) * a.Hv + h) * (kD * kD) + r * kD + half * 64;
+  float* Sg = a.ssm + soff;                                          // fp32 state
+  uint16_t* Sb = reinterpret_cast<uint16_t*>(a.ssm) + soff;          // bf16 state
   float Sr[64];
+  if (a.ssm_bf16) {
 #pragma unroll
-  for (int e = 0; e < 64; e += 4) {
-    float4 v = init ? *reinterpret_cast<const float4*>(Sg + e) : make_float4(0.f, 0.f, 0.f, 0.f);
-    Sr[e] = v.x; Sr[e + 1] = v.y; Sr[e + 2] = v.z; Sr[e + 3] = v.w;
+    for (int e = 0; e < 64; e += 8) {
+      float f[8];
+      unpack8(init ? *reinterpret_cast<const uint4*>(Sb + e) : make_uint4(0u, 0u, 0u, 0u), f);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) Sr[e + i] = f[i];
+    }
+  } else {
+#pragma unroll
+    for (int e = 0; e < 64; e += 4) {
+      float4 v = init ? *reinterpret_cast<const float4*>(Sg + e) : make_float4(0.f, 0.f, 0.f, 0.f);
+      Sr[e] = v.x; Sr[e + 1] = v.y; Sr[e + 2] = v.z; Sr[e + 3] = v.w;
+    }
   }
   auto store_S_tiles = [&]() {
 #pragma unroll
@@ -760,9 +772,19 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   }
   bad = tc_sync(bad);
   if (!bad) {
+    if (a.ssm_bf16) {  // rounded to bf16 only here, at the write-back
 #pragma unroll
-    for (int e = 0; e < 64; e += 4)
-      *reinterpret_cast<float4*>(Sg + e) = make_float4(Sr[e], Sr[e + 1], Sr[e + 2], Sr[e + 3]);
+      for (int e = 0; e < 64; e += 8) {
+        uint16_t hb[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) hb[i] = f2bf(Sr[e + i]);
+        *reinterpret_cast<uint4*>(Sb + e) = pack8(hb);
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < 64; e += 4)
+        *reinterpret_cast<float4*>(Sg + e) = make_float4(Sr[e], Sr[e + 1], Sr[e + 2], Sr[e + 3]);
+    }
   } else if (tid == 0 && a.err) {
     atomicOr(a.err, GDN_DEVERR_TIMEOUT);
   }

@@ -48,15 +48,31 @@ __device__ __forceinline__ uint64_t global_ns() {
   return t;
 }
 
+// try_wait with a suspend-time hint: the thread sleeps in hardware until the
+// phase completes or about `hint_ns` pass, instead of spinning on the barrier.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity,
+                                                    uint32_t hint_ns) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return done != 0;
+}
+
 // Waits for phase `parity` of an mbarrier, giving up after `limit_ns` of wall
 // time. Returns false on timeout (the caller records an error and skips the
-// work that needed the data).
+// work that needed the data). Between checks of the clock the thread sleeps on
+// the barrier rather than spinning, leaving issue slots to the working warps.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
                                                   uint64_t limit_ns = 1000000000ull) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_ns();
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait_sleep(bar, parity, 100000u)) return true;
     if (global_ns() - t0 > limit_ns) return false;
   }
 }

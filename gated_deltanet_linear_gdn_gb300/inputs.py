@@ -65,6 +65,7 @@ class LayerInputs:
     scale: float
     qk_l2norm: bool = True
     meta: dict = field(default_factory=dict)
+    state_bf16: bool = False     # ssm_state holds bf16 bit patterns (uint16) when True
 
     @property
     def num_slots(self) -> int:
@@ -91,7 +92,7 @@ def make_inputs(geo: Geometry, lengths, num_slots: int, seed: int, *, conv=True,
                 silu=True, conv_f32=False, conv_layout=0, gate_direct=False,
                 conv_w_std=0.02, conv_state_std=1.0, state_std=0.05, A_log_range=(0.0, 2.0),
                 dt_bias_zero=True, has_init=True, slots=None, state_pool=True,
-                normalise_k_input=False) -> LayerInputs:
+                normalise_k_input=False, state_bf16=False) -> LayerInputs:
     """Generic generator: sequences of the given lengths (decode = all ones).
 
     mixed q|k|v ~ N(0,1) bf16; a, b ~ N(0,1) bf16 (fused gates) with
@@ -99,6 +100,7 @@ def make_inputs(geo: Geometry, lengths, num_slots: int, seed: int, *, conv=True,
     conv state ~ N(0, conv_state_std); recurrent state ~ N(0, state_std) fp32.
     normalise_k_input scales each k head vector of the input to unit length.
     gate_direct draws g = -|N(0,1)| and beta ~ U(0,1) as f32 instead of a, b.
+    state_bf16 stores the drawn state pool as bf16 bit patterns.
     """
     rng = np.random.default_rng(seed)
     lengths = [int(x) for x in lengths]
@@ -141,9 +143,12 @@ def make_inputs(geo: Geometry, lengths, num_slots: int, seed: int, *, conv=True,
     if has_init is not True:
         hi_arr = (np.zeros(N, np.uint8) if has_init is False
                   else np.asarray(has_init, dtype=np.uint8))
+    if state_bf16:
+        ssm = f32_to_bf16_bits(ssm)
     return LayerInputs(geo, mixed, a, b, gate_direct, A_log, dt_bias, conv_w, conv_b, silu,
                        conv_state, conv_f32, conv_layout, ssm, slot, cu, hi_arr,
-                       float(geo.dk ** -0.5), True, {"seed": seed, "lengths": lengths})
+                       float(geo.dk ** -0.5), True, {"seed": seed, "lengths": lengths},
+                       bool(state_bf16))
 
 
 # --------------------------------------------------------------------------- named workloads
@@ -211,13 +216,16 @@ def correlated_keys(T=64, seed=0, geo: Geometry = QWEN3_NEXT, eps=0.01) -> Layer
                        float(geo.dk ** -0.5), True, {"seed": seed, "lengths": [T]})
 
 
-def device_state_pool(num_slots: int, geo: Geometry, std: float, seed: int, device="cuda"):
-    """fp32 state pool [num_slots, Hv, dv, dk] ~ N(0, std) drawn on the device (seeded torch
-    generator): for benchmark pools too large to draw on the host quickly."""
+def device_state_pool(num_slots: int, geo: Geometry, std: float, seed: int, device="cuda",
+                      dtype=None):
+    """State pool [num_slots, Hv, dv, dk] ~ N(0, std) drawn on the device (seeded torch
+    generator), fp32 unless dtype says otherwise: for benchmark pools too large to draw
+    on the host quickly."""
     import torch
 
     g = torch.Generator(device=device)
     g.manual_seed(int(seed))
-    pool = torch.empty((num_slots, geo.Hv, geo.dv, geo.dk), dtype=torch.float32, device=device)
+    pool = torch.empty((num_slots, geo.Hv, geo.dv, geo.dk), dtype=dtype or torch.float32,
+                       device=device)
     pool.normal_(0.0, float(std), generator=g)
     return pool

@@ -79,6 +79,12 @@ typedef struct {
   int32_t head_k_dim;  /* dk */
   int32_t head_v_dim;  /* dv */
   int32_t conv_width;  /* W */
+  /* Recurrent-state storage: 0 = fp32 (default), 1 = bf16. The arithmetic stays fp32;
+   * only the write into the pool rounds to bf16 (round to nearest even), as the state
+   * ABI of RL-Kernel PR #469 "C6: GDN decode-step goldens and recurrent/conv state
+   * contract" (Summary) has it. With 1, `ssm_state` points at bf16 data of the same
+   * shape. */
+  int32_t state_bf16;
 } gdn_dims;
 
 /* Bits of the device error word (int32, caller-zeroed; the kernels only OR
@@ -137,7 +143,7 @@ gdn_status gdn_conv_update(const void* x, void* conv_state, gdn_dtype state_dtyp
  *   conv_weight [D, W] bf16, or NULL to bypass the conv (conv_state unused)
  *   conv_bias   [D] bf16 or NULL
  *   conv_state  conv pool as in gdn_conv_update, in place
- *   ssm_state   [num_slots, Hv, dv, dk] f32, in place
+ *   ssm_state   [num_slots, Hv, dv, dk] f32 (bf16 when dims.state_bf16), in place
  *   slot        [B] int32
  *   scale       multiplier applied to q (dk^-0.5 in Qwen3-Next)
  *   out         [B, Hv, dv] of out_dtype (bf16 or f32); inactive rows zeroed

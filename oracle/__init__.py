@@ -59,7 +59,7 @@ def lib():
         _lib.gdn_ref_conv_update.argtypes = [P, P, I, I, P, P, I, P, I, I, I, I, P, P, P]
         _lib.gdn_ref_layer.restype = I
         _lib.gdn_ref_layer.argtypes = [P, P, P, I, P, P, P, P, I, P, I, I, P, P, P, P, I, I, I,
-                                       I, I, I, I, I, D, I, P, P, P, I, P]
+                                       I, I, I, I, I, D, I, P, P, P, I, P, I]
         _lib.gdn_ref_recurrent_head_batch_dependent.restype = None
         _lib.gdn_ref_recurrent_head_batch_dependent.argtypes = [P, P, P, P, P, P, I, I, I, I, P]
     return _lib
@@ -176,8 +176,12 @@ def conv_update(x_bits, conv_state, cache_f32, layout, w_bits, bias_bits, silu, 
 
 def layer(mixed_bits, a, b, gate_direct, A_log, dt_bias, conv_w_bits, conv_b_bits, silu,
           conv_state, conv_f32, conv_layout, ssm_state, cu_seqlens, slot, has_init,
-          Hk, Hv, dk, dv, W=4, scale=None, qk_l2norm=True, head_mask=None, nthreads=1):
+          Hk, Hv, dk, dv, W=4, scale=None, qk_l2norm=True, head_mask=None, nthreads=1,
+          state_bf16=False):
     """Packed-sequence GDN layer (decode = every sequence of length 1).
+
+    state_bf16: the recurrent state is stored in bf16 (values in the fp64 pool are then
+    bf16-representable; each call's final state is rounded once, RNE).
 
     conv_state (uint16/float32 pool) and ssm_state (float64 pool
     [num_slots, Hv, dv, dk]) are updated IN PLACE. Returns
@@ -211,7 +215,8 @@ def layer(mixed_bits, a, b, gate_direct, A_log, dt_bias, conv_w_bits, conv_b_bit
                              _p(w), _p(cb), int(silu), _p(conv_state), int(conv_f32),
                              int(conv_layout), _p(ssm_state), _p(cu), _p(slot), _p(hi), N, Ttot,
                              num_slots, Hk, Hv, dk, dv, W, float(scale), int(bool(qk_l2norm)),
-                             _p(out), _p(out_bits), _p(hm), int(nthreads), _p(err))
+                             _p(out), _p(out_bits), _p(hm), int(nthreads), _p(err),
+                             int(bool(state_bf16)))
     if rc != 0:
         raise ValueError("oracle rejected the layer arguments")
     return out, out_bits, int(err[0])
@@ -219,12 +224,12 @@ def layer(mixed_bits, a, b, gate_direct, A_log, dt_bias, conv_w_bits, conv_b_bit
 
 def decode_step(mixed_bits, a, b, gate_direct, A_log, dt_bias, conv_w_bits, conv_b_bits, silu,
                 conv_state, conv_f32, conv_layout, ssm_state, slot, Hk, Hv, dk, dv, W=4,
-                scale=None, qk_l2norm=True, head_mask=None, nthreads=1):
+                scale=None, qk_l2norm=True, head_mask=None, nthreads=1, state_bf16=False):
     """One decode step over B rows (each row a length-1 sequence starting from its slot)."""
     B = np.asarray(slot).size
     cu = np.arange(B + 1, dtype=np.int32)
     out, out_bits, err = layer(mixed_bits, a, b, gate_direct, A_log, dt_bias, conv_w_bits,
                                conv_b_bits, silu, conv_state, conv_f32, conv_layout, ssm_state,
                                cu, slot, None, Hk, Hv, dk, dv, W, scale, qk_l2norm, head_mask,
-                               nthreads)
+                               nthreads, state_bf16)
     return out, out_bits, err

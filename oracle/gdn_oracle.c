@@ -487,6 +487,8 @@ static void run_units(unit_fn fn, void* ctx, int n, int nthreads) {
  *            the same (nullable)
  * head_mask  [Hv] (nullable): heads with mask 0 are skipped (their outputs and
  *            states untouched) -- lets large cases be sampled by head.
+ * state_bf16 1: the pool holds bf16 values (exact in fp64); each call's final state
+ *            is rounded to bf16 when stored, the arithmetic staying fp64.
  */
 typedef struct {
   const uint16_t* y;   /* conv output bits [Ttot, D] */
@@ -501,6 +503,7 @@ typedef struct {
   double* out;
   uint16_t* out_bits;
   const uint8_t* head_mask;
+  int state_bf16;  /* 1: the stored state is rounded to bf16 ([P1] Summary, state ABI) */
 } rule_ctx;
 
 static void rule_unit(void* p, int unit) {
@@ -548,6 +551,9 @@ static void rule_unit(void* p, int unit) {
       if (c->out_bits) c->out_bits[oi] = gdn_ref_round_bf16(o[r]);
     }
   }
+  /* bf16 storage: round once, at the write-back; the arithmetic stayed fp64 */
+  if (c->state_bf16)
+    for (int e = 0; e < dv * dk; ++e) S[e] = round_bf16_val(S[e]);
   memcpy(Sp, S, sizeof(double) * dv * dk);
   free(S); free(q); free(k); free(v); free(o);
 }
@@ -592,7 +598,7 @@ int gdn_ref_layer(const uint16_t* mixed_qkv, const void* a, const void* b, int g
                   const int32_t* slot, const uint8_t* has_init, int N, int Ttot, int num_slots,
                   int Hk, int Hv, int dk, int dv, int W, double scale, int qk_l2norm,
                   double* out, uint16_t* out_bits, const uint8_t* head_mask, int nthreads,
-                  int32_t* err) {
+                  int32_t* err, int state_bf16) {
   int D = 2 * Hk * dk + Hv * dv;
   if (Hk <= 0 || Hv % Hk != 0 || W < 2 || W > 16) return 1;
   for (int i = 0; i < N; ++i)
@@ -606,7 +612,8 @@ int gdn_ref_layer(const uint16_t* mixed_qkv, const void* a, const void* b, int g
     memcpy(y, mixed_qkv, sizeof(uint16_t) * (size_t)Ttot * D);
   }
   rule_ctx rc = {y, a, b, gate_direct, A_log, dt_bias, ssm_state, cu_seqlens, slot, has_init,
-                 num_slots, Hk, Hv, dk, dv, D, qk_l2norm, scale, out, out_bits, head_mask};
+                 num_slots, Hk, Hv, dk, dv, D, qk_l2norm, scale, out, out_bits, head_mask,
+                 state_bf16};
   run_units(rule_unit, &rc, N * Hv, nthreads);
   free(y);
   return 0;

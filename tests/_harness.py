@@ -49,7 +49,7 @@ class Device:
             self.conv_state = f(inp.conv_state)
         else:
             self.conv_state = fb(inp.conv_state)
-        self.ssm = f(inp.ssm_state)
+        self.ssm = fb(inp.ssm_state) if inp.state_bf16 else f(inp.ssm_state)
         self.slot = f(inp.slot)
         self.cu = f(inp.cu_seqlens)
         self.has_init = f(inp.has_init)
@@ -110,14 +110,17 @@ class OracleRun:
         slot_c = np.array([mp[int(s)] if 0 < s < ns else (int(s) if s <= 0 else nsc)
                            for s in inp.slot], dtype=np.int32)
         self.slot_c = slot_c
-        self.ssm = np.ascontiguousarray(inp.ssm_state[self.sel].astype(np.float64))
+        pool = inp.ssm_state[self.sel]
+        if inp.state_bf16:
+            pool = gi.bf16_bits_to_f32(pool)
+        self.ssm = np.ascontiguousarray(pool.astype(np.float64))
         self.conv = (None if inp.conv_state is None
                      else np.ascontiguousarray(inp.conv_state[self.sel]))
         self.out, self.out_bits, self.err = oracle.layer(
             inp.mixed, inp.a, inp.b, inp.gate_direct, inp.A_log, inp.dt_bias, inp.conv_w,
             inp.conv_b, inp.silu, self.conv, inp.conv_f32, inp.conv_layout, self.ssm,
             inp.cu_seqlens, slot_c, inp.has_init, geo.Hk, geo.Hv, geo.dk, geo.dv, geo.W,
-            inp.scale, inp.qk_l2norm, head_mask, nthreads)
+            inp.scale, inp.qk_l2norm, head_mask, nthreads, inp.state_bf16)
 
 
 def rel_err(x, ref) -> float:
@@ -147,6 +150,23 @@ def bf16_store_within(bits, ref, tol) -> bool:
     half_ulp = np.ldexp(1.0, np.frexp(np.abs(ref))[1] - 9)  # 2^(e-1-8): half ULP for |ref| in [2^(e-1), 2^e)
     bound = tol * np.abs(ref).max() + half_ulp + 1e-45
     return bool(np.all(np.abs(got - ref) <= bound))
+
+
+def ssm_host(d: "Device") -> np.ndarray:
+    """The device state pool as fp64 values (fp32 or bf16 storage)."""
+    if d.ssm.dtype == torch.bfloat16:
+        return gi.bf16_bits_to_f32(torch_to_bits(d.ssm)).astype(np.float64)
+    return d.ssm.cpu().numpy().astype(np.float64)
+
+
+def bf16_state_within(got, ref_rounded, tol) -> bool:
+    """A bf16-stored state against the oracle's bf16-rounded state: elementwise within
+    tol * max|ref| plus one bf16 ULP (the two fp roundings may land on either side of a
+    rounding boundary)."""
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref_rounded, np.float64)
+    ulp = np.ldexp(1.0, np.frexp(np.abs(ref))[1] - 8)
+    return bool(np.all(np.abs(got - ref) <= tol * np.abs(ref).max() + ulp + 1e-45))
 
 
 def tensor_hash(t: torch.Tensor) -> int:

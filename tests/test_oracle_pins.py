@@ -567,3 +567,40 @@ def test_batch_invariance_check_catches_batch_dependence(oracle):
 
     assert invariant(lambda B: oracle.recurrent_head)
     assert not invariant(lambda B: (lambda *a: oracle.recurrent_head_batch_dependent(*a, B)))
+
+
+# --------------------------------------------------------------------------- bf16 state
+
+def test_bf16_state_is_the_fp64_state_rounded_once(oracle):
+    """RL-Kernel PR #469, Summary (state ABI): the state takes its storage dtype only when it is
+    written. A bf16-state call equals the full-precision call with the final state rounded
+    once (RNE), and identical outputs (read out before the write)."""
+    geo = gi.TINY
+    case = gi.make_inputs(geo, [5, 3], 6, seed=12)
+    pool16 = gi.bf16_bits_to_f32(gi.f32_to_bf16_bits(case.ssm_state)).astype(np.float64)
+    conv_a, conv_b = case.conv_state.copy(), case.conv_state.copy()
+    ssm_a, ssm_b = pool16.copy(), pool16.copy()
+    args = (case.mixed, case.a, case.b, False, case.A_log, case.dt_bias, case.conv_w,
+            case.conv_b, 1)
+    out_a, _, _ = oracle.layer(*args, conv_a, 0, 0, ssm_a, case.cu_seqlens, case.slot, None,
+                               geo.Hk, geo.Hv, geo.dk, geo.dv)
+    out_b, _, _ = oracle.layer(*args, conv_b, 0, 0, ssm_b, case.cu_seqlens, case.slot, None,
+                               geo.Hk, geo.Hv, geo.dk, geo.dv, state_bf16=True)
+    assert np.array_equal(out_a, out_b)
+    rounded = bfv(oracle.round_bf16_array(ssm_a.ravel())).reshape(ssm_a.shape)
+    assert np.array_equal(ssm_b, rounded)
+    touched = sorted(set(int(s) for s in case.slot))
+    assert not np.array_equal(ssm_b[touched], pool16[touched])
+
+
+def test_bf16_state_identity_step_is_exact(oracle):
+    """g = 0 and beta = 0 leave S unchanged: a bf16 state round-trips bitwise."""
+    geo = gi.Geometry(1, 1, 8, 8)
+    rng = np.random.default_rng(4)
+    pool = bfv(bf(rng.standard_normal((3, 1, 8, 8)))).copy()
+    before = pool.copy()
+    mixed = bf(rng.standard_normal((1, geo.D)))
+    g = np.zeros((1, 1), np.float32); beta = np.zeros((1, 1), np.float32)
+    oracle.decode_step(mixed, g, beta, True, None, None, None, None, 0, None, 0, 0, pool,
+                       np.array([2], np.int32), 1, 1, 8, 8, state_bf16=True)
+    assert np.array_equal(pool, before)
