@@ -88,15 +88,15 @@ def load_bf16_peak():
 
 def kernel_source_digest():
     h = hashlib.sha256()
-    for f in ("gdn_decode.cu", "gdn_common.cuh"):
+    for f in ("gdn_decode.cu", "gdn_common.cuh", "gdn_ptx.cuh"):
         with open(os.path.join(ROOT, "gated_deltanet_linear_gdn_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
 
-def ncu_traffic():
-    """Per-launch DRAM bytes of the decode kernel from the committed ncu summary, if it was
-    taken on the current kernel source (else None)."""
+def ncu_traffic(state="f32"):
+    """Per-launch DRAM bytes of the headline decode kernel (fp32 or bf16 state) from the
+    committed ncu summary, if it was taken on the current kernel source (else None)."""
     p = os.path.join(ROOT, "profiles", "decode_traffic.json")
     if not os.path.exists(p):
         return None
@@ -104,7 +104,7 @@ def ncu_traffic():
         j = json.load(f)
     if j.get("source_digest") != kernel_source_digest():
         return None
-    return j
+    return j.get("launches", {}).get(state)
 
 
 def aggregate_ranks(mean_ms: float, bytes_per_rank: int, world: int, device=None):
@@ -306,7 +306,7 @@ def run_ours(args, rank, world):
         torch.cuda.empty_cache()
 
     # ---- e2e through the public API with pinned host buffers ----
-    t = decode_setup(args.batch, args.num_slots, seed=args.batch)
+    t = decode_setup(args.batch, args.num_slots, seed=args.batch, state_bf16=args.state_bf16)
     h_mixed = t["mixed"].cpu().pin_memory()
     h_a, h_b = t["a"].cpu().pin_memory(), t["b"].cpu().pin_memory()
     h_slot = t["slot"].cpu().pin_memory()
@@ -325,7 +325,7 @@ def run_ours(args, rank, world):
     d2h = h_out.numel() * h_out.element_size()
 
     # ---- headline: exactly K timed decode steps ----
-    nbytes = decode_bytes(args.batch, geo)
+    nbytes = decode_bytes(args.batch, geo, state_bytes=2 if args.state_bf16 else 4)
     if world > 1:
         import torch.distributed as dist
         dist.barrier()
@@ -342,7 +342,7 @@ def run_ours(args, rank, world):
         return None
     peak, peak_kind = load_peaks()
     achieved = nbytes / (mean_ms * 1e-3) / 1e9
-    traffic = ncu_traffic()
+    traffic = ncu_traffic("bf16" if args.state_bf16 else "f32")
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(mean_ms, 5),
@@ -350,7 +350,8 @@ def run_ours(args, rank, world):
         "data": "synthetic",
         "config": {"workload": "GDN decode step, Qwen3-Next geometry Hk=16 Hv=32 dk=dv=128 "
                                f"D=8192 W=4, B={args.batch} rows over {args.num_slots} shuffled "
-                               "slots, bf16 conv cache, fp32 state, bf16 I/O",
+                               f"slots, bf16 conv cache, {'bf16' if args.state_bf16 else 'fp32'} "
+                               "state, bf16 I/O",
                    "batch": args.batch, "num_slots": args.num_slots,
                    "bytes_per_step": nbytes, "l2": "flushed between timed steps (512 MiB write)"},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
@@ -466,6 +467,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--batch", type=int, default=HEADLINE_B, help="headline decode rows")
     ap.add_argument("--num-slots", type=int, default=NUM_SLOTS, help="headline slot pool size")
+    ap.add_argument("--state-bf16", action="store_true",
+                    help="headline decode on a bf16 recurrent-state pool (default fp32)")
     ap.add_argument("--prefill-tokens", type=int, default=4096,
                     help="length of the single-sequence prefill case")
     ap.add_argument("--no-varlen", action="store_true", help="skip the ~32k-token varlen case")
