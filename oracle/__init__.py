@@ -60,6 +60,8 @@ def lib():
         _lib.gdn_ref_layer.restype = I
         _lib.gdn_ref_layer.argtypes = [P, P, P, I, P, P, P, P, I, P, I, I, P, P, P, P, I, I, I,
                                        I, I, I, I, I, D, I, P, P, P, I, P, I]
+        _lib.gdn_ref_gated_rmsnorm.restype = None
+        _lib.gdn_ref_gated_rmsnorm.argtypes = [P, P, P, D, D, I, ctypes.c_int64, I, P]
         _lib.gdn_ref_recurrent_head_batch_dependent.restype = None
         _lib.gdn_ref_recurrent_head_batch_dependent.argtypes = [P, P, P, P, P, P, I, I, I, I, P]
     return _lib
@@ -144,6 +146,24 @@ def unit_lower_inverse(A):
     T = np.zeros((n, n), dtype=np.float64)
     lib().gdn_ref_unit_lower_inverse(_p(A), n, _p(T))
     return T
+
+
+def gated_rmsnorm(o, z_bits, w, offset=0.0, eps=1e-6, act="silu"):
+    """Output gate of the GDN block (gdn_oracle.c, gdn_ref_gated_rmsnorm): for each vector
+    o[..., :] over the value-head dim, y = o / sqrt(mean(o^2) + eps) * (w + offset) * act(z),
+    act = SiLU or sigmoid. o: fp64 [..., dv]; z_bits: bf16 bits of the same shape; w: fp32 [dv].
+    Returns fp64 y."""
+    o = np.ascontiguousarray(o, dtype=np.float64)
+    dv = o.shape[-1]
+    z_bits = np.ascontiguousarray(z_bits, dtype=np.uint16).reshape(o.shape)
+    w = np.ascontiguousarray(w, dtype=np.float32)
+    assert w.shape == (dv,)
+    y = np.empty_like(o)
+    L = lib()
+    L.gdn_ref_gated_rmsnorm(_p(o), _p(z_bits), _p(w), ctypes.c_double(offset), ctypes.c_double(eps),
+                            ctypes.c_int({"silu": 0, "sigmoid": 1}[act]),
+                            ctypes.c_int64(o.size // dv), ctypes.c_int(dv), _p(y))
+    return y
 
 
 def validate_slots(slot, num_slots) -> int:

@@ -28,6 +28,10 @@
  *   [P4] vLLM PR #53864 "Numerical root cause and fix": the chunked prefill
  *        inverts the lower-triangular per-chunk KK^T block; three
  *        Newton-Schulz rounds with bf16 intermediates fail on correlated keys.
+ *   [P1] page, Summary by CodeRabbit and Walkthrough (RL-Kernel PRs #466-#468,
+ *        "Gated RMSNorm CUDA kernel for the GDN block"): the GDN output goes
+ *        through a gated RMSNorm, with SiLU or sigmoid gating and a weight
+ *        offset (zero for the plain form, one for the zero-centred one).
  *
  * Precision: everything is fp64 except where [P1] fixes it -- the conv
  * accumulator (fp32, each add rounded to fp32) and the tap products (rounded
@@ -617,6 +621,32 @@ int gdn_ref_layer(const uint16_t* mixed_qkv, const void* a, const void* b, int g
   run_units(rule_unit, &rc, N * Hv, nthreads);
   free(y);
   return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Output gate: gated RMSNorm of o over each value head ([P1] page, Summary   */
+/* by CodeRabbit: gated RMSNorm with SiLU or sigmoid gating; Walkthrough:     */
+/* the weight offset)                                                         */
+/* ------------------------------------------------------------------------ */
+
+/* For each of `rows` vectors o[r][0..dv) (one token, one value head):
+ *   y[i] = o[i] / sqrt(mean_j o[j]^2 + eps) * (w[i] + offset) * act(z[i]),
+ * act = SiLU (z * sigmoid(z), act_kind 0) or sigmoid (act_kind 1). The norm is
+ * taken before the gate (the GDN block normalises the core output, then gates
+ * it with z). z arrives as bf16 bits, w as fp32; all arithmetic is fp64. */
+void gdn_ref_gated_rmsnorm(const double* o, const uint16_t* z, const float* w, double offset,
+                           double eps, int act_kind, int64_t rows, int dv, double* y) {
+  for (int64_t r = 0; r < rows; ++r) {
+    const double* orow = o + (size_t)r * dv;
+    double ss = 0.0;
+    for (int i = 0; i < dv; ++i) ss += orow[i] * orow[i];
+    const double inv = 1.0 / sqrt(ss / dv + eps);
+    for (int i = 0; i < dv; ++i) {
+      const double zi = bf16_to_f64(z[(size_t)r * dv + i]);
+      const double gate = act_kind == 0 ? zi * gdn_ref_sigmoid(zi) : gdn_ref_sigmoid(zi);
+      y[(size_t)r * dv + i] = orow[i] * inv * ((double)w[i] + offset) * gate;
+    }
+  }
 }
 
 /* ------------------------------------------------------------------------ */

@@ -604,3 +604,58 @@ def test_bf16_state_identity_step_is_exact(oracle):
     oracle.decode_step(mixed, g, beta, True, None, None, None, None, 0, None, 0, 0, pool,
                        np.array([2], np.int32), 1, 1, 8, 8, state_bf16=True)
     assert np.array_equal(pool, before)
+
+
+# --------------------------------------------------------------------------- output gate
+
+def _gate_case(seed, shape=(3, 4, 128)):
+    rng = np.random.default_rng(seed)
+    o = rng.standard_normal(shape)
+    z = gi.f32_to_bf16_bits(rng.standard_normal(shape, dtype=np.float32) * np.float32(2.0))
+    w = rng.standard_normal(shape[-1]).astype(np.float32)
+    return o, z, w
+
+
+@pytest.mark.parametrize("act", ["silu", "sigmoid"])
+@pytest.mark.parametrize("offset", [0.0, 1.0])
+def test_gated_rmsnorm_matches_torch_rms_norm_times_gate(oracle, act, offset):
+    """RL-Kernel PRs #466-#468 (gated RMSNorm, SiLU or sigmoid gating, weight offset): the
+    oracle equals torch's own fp64 rms_norm with weight w + offset, times act(z)."""
+    import torch
+    o, z, w = _gate_case(1)
+    y = oracle.gated_rmsnorm(o, z, w, offset=offset, eps=1e-6, act=act)
+    zt = torch.from_numpy(gi.bf16_bits_to_f32(z).astype(np.float64))
+    wt = torch.from_numpy(w.astype(np.float64)) + offset
+    g = torch.nn.functional.silu(zt) if act == "silu" else torch.sigmoid(zt)
+    ref = torch.nn.functional.rms_norm(torch.from_numpy(o), [o.shape[-1]], wt, 1e-6) * g
+    assert np.abs(y - ref.numpy()).max() <= 1e-13 * np.abs(ref.numpy()).max()
+
+
+def test_gated_rmsnorm_closed_forms(oracle):
+    """Invariants of y = o / rms(o) * (w + offset) * act(z), eps = 0."""
+    o, z, w = _gate_case(2)
+    y = oracle.gated_rmsnorm(o, z, w, eps=0.0)
+    # scale invariance and odd symmetry in o
+    assert np.abs(oracle.gated_rmsnorm(3.7 * o, z, w, eps=0.0) - y).max() <= 1e-13 * np.abs(y).max()
+    assert np.array_equal(oracle.gated_rmsnorm(-o, z, w, eps=0.0), -y)
+    # the normalised vector has unit rms: mean((y / ((w + off) act(z)))^2) = 1
+    zf = gi.bf16_bits_to_f32(z).astype(np.float64)
+    silu = zf / (1.0 + np.exp(-zf))
+    n = y / (w.astype(np.float64) * silu)
+    assert np.allclose(np.mean(n * n, axis=-1), 1.0, rtol=1e-12)
+    # a constant head vector c*1 normalises to sign(c)*1
+    c = np.full((1, 128), -0.3)
+    yc = oracle.gated_rmsnorm(c, z[0, :1], w, eps=0.0)
+    assert np.allclose(yc, -(w.astype(np.float64) * silu[0, :1]), rtol=1e-14, atol=0)
+    # z = 0: SiLU gate is exactly 0; the sigmoid gate is exactly 1/2
+    z0 = np.zeros_like(z)
+    assert np.all(oracle.gated_rmsnorm(o, z0, w, act="silu") == 0.0)
+    ys = oracle.gated_rmsnorm(o, z0, w, eps=0.0, act="sigmoid")
+    rms = np.sqrt(np.mean(o * o, axis=-1, keepdims=True))
+    assert np.allclose(ys, 0.5 * o / rms * w.astype(np.float64), rtol=1e-13, atol=0)
+    # the weight offset: w = 0 with offset 1 equals w = 1 with offset 0
+    ones = np.ones(128, np.float32)
+    assert np.array_equal(oracle.gated_rmsnorm(o, z, np.zeros(128, np.float32), offset=1.0),
+                          oracle.gated_rmsnorm(o, z, ones, offset=0.0))
+    # eps enters under the root: a zero head stays zero, a tiny head is not blown up
+    assert np.all(oracle.gated_rmsnorm(np.zeros((1, 128)), z[0, :1], w, eps=1e-6) == 0.0)
