@@ -39,15 +39,19 @@ NUM_SLOTS = 512
 FALLBACK_HBM_GBS = 6800.0
 
 
-def decode_bytes(B, geo, conv_f32=False, bias=True, out_bytes=2, state_bytes=4):
+def decode_bytes(B, geo, conv_f32=False, bias=True, out_bytes=2, state_bytes=4, gated=False):
     """Algorithmic bytes of one decode step: per row the state read + write (fp32, or bf16
     with state_bytes=2), x, the conv window read + write, the output and the gate inputs
-    and slot; per call the conv weight and bias and the per-head gate parameters."""
+    and slot; per call the conv weight and bias and the per-head gate parameters. With the
+    output gate, per row the bf16 z and per call the fp32 norm weight."""
     s = 4 if conv_f32 else 2
     D = geo.D
     per_row = (2 * geo.Hv * geo.dv * geo.dk * state_bytes + 2 * D + 2 * D * (geo.W - 1) * s
                + out_bytes * geo.Hv * geo.dv + 2 * 2 * geo.Hv + 4)
     per_call = 2 * D * geo.W + (2 * D if bias else 0) + 8 * geo.Hv
+    if gated:
+        per_row += 2 * geo.Hv * geo.dv
+        per_call += 4 * geo.dv
     return B * per_row + per_call
 
 
@@ -205,10 +209,10 @@ def run_ours(args, rank, world):
             silu=silu, inp=inp)
         return t
 
-    def decode_call(t):
+    def decode_call(t, gate=None):
         gdn.gdn_decode_step(t["mixed"], t["a"], t["b"], t["A_log"], t["dt_bias"], t["conv_w"],
                             t["conv_b"], t["conv"], t["ssm"], t["slot"], t["out"], dims,
-                            silu=t["silu"], stream=stream)
+                            silu=t["silu"], gate=gate, stream=stream)
 
     def timed(fn, steps, warmup, do_flush=True):
         for _ in range(warmup):
@@ -262,6 +266,16 @@ def run_ours(args, rank, world):
             sweep[f"bf16state_{B}_of_{ns}"] = {"us": round(ms * 1e3, 2),
                                                "GBps": round(nb / ms / 1e6, 1)}
             del t
+        # the output gate (gated RMSNorm with z) fused into the step
+        t = decode_setup(HEADLINE_B, NUM_SLOTS, seed=HEADLINE_B)
+        gz = torch.randn(HEADLINE_B, geo.Hv, geo.dv, device=dev).to(torch.bfloat16)
+        gw = torch.ones(geo.dv, device=dev)
+        og = gdn.OutputGate(gz, gw)
+        ms = float(np.median(timed(lambda: decode_call(t, og), 20, 3)))
+        nb = decode_bytes(HEADLINE_B, geo, gated=True)
+        sweep[f"gated_{HEADLINE_B}_of_{NUM_SLOTS}"] = {"us": round(ms * 1e3, 2),
+                                                      "GBps": round(nb / ms / 1e6, 1)}
+        del t, gz, gw, og
         torch.cuda.empty_cache()
 
     # ---- chunked prefill ----

@@ -26,6 +26,7 @@ GDN_BF16, GDN_F32 = 0, 1
 GDN_CONV_DIM_FIRST, GDN_CONV_TAP_FIRST = 0, 1
 GDN_GATE_FUSED, GDN_GATE_DIRECT = 0, 1
 GDN_DEVERR_SLOT_RANGE, GDN_DEVERR_SEQLENS = 1, 2
+GDN_ACT_SILU, GDN_ACT_SIGMOID = 0, 1
 
 
 class GDNError(RuntimeError):
@@ -56,6 +57,32 @@ class Dims:
         return gdn_dims(self.Hk, self.Hv, self.dk, self.dv, self.W, int(bool(state_bf16)))
 
 
+class gdn_output_gate(ctypes.Structure):
+    _fields_ = [("z", ctypes.c_void_p), ("weight", ctypes.c_void_p),
+                ("weight_offset", ctypes.c_float), ("eps", ctypes.c_float),
+                ("act", ctypes.c_int32)]
+
+
+class OutputGate:
+    """The GDN block's output gate (include/gdn.h, gdn_output_gate): out = o / rms(o) *
+    (weight + weight_offset) * act(z) per value head. z: bf16 [tokens, Hv, dv] on the device;
+    weight: f32 [dv] on the device; act "silu" or "sigmoid"."""
+
+    def __init__(self, z, weight, *, weight_offset=0.0, eps=1e-6, act="silu"):
+        if z.dtype != torch.bfloat16 or weight.dtype != torch.float32:
+            raise ValueError("z must be bfloat16 and weight float32")
+        self.z, self.weight = z, weight
+        self._c = gdn_output_gate(_ptr(z), _ptr(weight), float(weight_offset), float(eps),
+                                  {"silu": GDN_ACT_SILU, "sigmoid": GDN_ACT_SIGMOID}[act])
+
+    def ref(self):
+        return ctypes.byref(self._c)
+
+
+def _gate(gate):
+    return None if gate is None else gate.ref()
+
+
 def _sdims(dims: "Dims", ssm_state) -> gdn_dims:
     """dims for a call: the state storage type follows the pool tensor's dtype."""
     if ssm_state.dtype not in (torch.float32, torch.bfloat16):
@@ -79,20 +106,20 @@ def lib():
         L.gdn_conv_update.argtypes = [P, P, I32, I32, P, P, I32, P, I32, I32, I32, I32, P, P, P]
         L.gdn_decode_step.restype = I32
         L.gdn_decode_step.argtypes = [P, P, P, I32, P, P, P, P, I32, P, I32, I32, P, P, I32, I32,
-                                      gdn_dims, F, I32, P, I32, P, P]
+                                      gdn_dims, F, I32, P, P, I32, P, P]
         L.gdn_chunked_prefill_workspace_size.restype = ctypes.c_size_t
         L.gdn_chunked_prefill_workspace_size.argtypes = [I32, I32, gdn_dims, I32]
         L.gdn_chunked_prefill.restype = I32
         L.gdn_chunked_prefill.argtypes = [P, P, P, I32, P, P, P, P, I32, P, I32, I32, P, P, P, P,
-                                          I32, I32, I32, gdn_dims, F, I32, I32, P, I32, P,
+                                          I32, I32, I32, gdn_dims, F, I32, I32, P, P, I32, P,
                                           ctypes.c_size_t, P, P]
         L.gdn_chunked_prefill_noalloc.restype = I32
         L.gdn_chunked_prefill_noalloc.argtypes = [P, P, P, I32, P, P, P, P, I32, P, I32, I32, P,
                                                   P, P, P, I32, I32, I32, gdn_dims, F, I32, I32,
-                                                  P, I32, P, P]
+                                                  P, P, I32, P, P]
         L.gdn_decode_graph_create.restype = I32
         L.gdn_decode_graph_create.argtypes = [P, P, P, I32, P, P, P, P, I32, P, I32, I32, P, P,
-                                              I32, I32, gdn_dims, F, I32, P, I32, P,
+                                              I32, I32, gdn_dims, F, I32, P, P, I32, P,
                                               ctypes.POINTER(ctypes.c_void_p)]
         L.gdn_graph_launch.restype = I32
         L.gdn_graph_launch.argtypes = [P, P]
@@ -159,11 +186,12 @@ def _gate_mode(a):
 
 def gdn_decode_step(mixed_qkv, a, b, A_log, dt_bias, conv_weight, conv_bias, conv_state,
                     ssm_state, slot, out, dims: Dims, *, silu=True,
-                    conv_layout=GDN_CONV_DIM_FIRST, scale=None, qk_l2norm=True, err=None,
-                    stream=None):
+                    conv_layout=GDN_CONV_DIM_FIRST, scale=None, qk_l2norm=True, gate=None,
+                    err=None, stream=None):
     """One fused decode step (conv state and ssm_state updated in place).
 
-    a, b: bf16 [B, Hv] (fused gates with A_log, dt_bias) or f32 g, beta (direct)."""
+    a, b: bf16 [B, Hv] (fused gates with A_log, dt_bias) or f32 g, beta (direct).
+    gate: an OutputGate, or None for the plain core output."""
     B = mixed_qkv.shape[0]
     scale = dims.dk ** -0.5 if scale is None else scale
     conv_dt = _dt(conv_state) if conv_state is not None else GDN_BF16
@@ -171,8 +199,8 @@ def gdn_decode_step(mixed_qkv, a, b, A_log, dt_bias, conv_weight, conv_bias, con
         _ptr(mixed_qkv), _ptr(a), _ptr(b), _gate_mode(a), _ptr(A_log), _ptr(dt_bias),
         _ptr(conv_weight), _ptr(conv_bias), int(bool(silu)), _ptr(conv_state), conv_dt,
         int(conv_layout), _ptr(ssm_state), _ptr(slot), B, ssm_state.shape[0],
-        _sdims(dims, ssm_state), float(scale), int(bool(qk_l2norm)), _ptr(out), _dt(out),
-        _ptr(err), _stream(stream)))
+        _sdims(dims, ssm_state), float(scale), int(bool(qk_l2norm)), _gate(gate), _ptr(out),
+        _dt(out), _ptr(err), _stream(stream)))
 
 
 def gdn_chunked_prefill_workspace_size(total_tokens, num_seqs, dims: Dims, chunk=64) -> int:
@@ -183,7 +211,7 @@ def gdn_chunked_prefill_workspace_size(total_tokens, num_seqs, dims: Dims, chunk
 def gdn_chunked_prefill(mixed_qkv, a, b, A_log, dt_bias, conv_weight, conv_bias, conv_state,
                         ssm_state, cu_seqlens, slot, has_initial_state, out, workspace,
                         dims: Dims, *, chunk=64, silu=True, conv_layout=GDN_CONV_DIM_FIRST,
-                        scale=None, qk_l2norm=True, err=None, stream=None):
+                        scale=None, qk_l2norm=True, gate=None, err=None, stream=None):
     """Chunked prefill over packed sequences (states updated in place by slot)."""
     T = mixed_qkv.shape[0]
     N = slot.shape[0]
@@ -194,7 +222,8 @@ def gdn_chunked_prefill(mixed_qkv, a, b, A_log, dt_bias, conv_weight, conv_bias,
         _ptr(conv_weight), _ptr(conv_bias), int(bool(silu)), _ptr(conv_state), conv_dt,
         int(conv_layout), _ptr(ssm_state), _ptr(cu_seqlens), _ptr(slot),
         _ptr(has_initial_state), N, T, ssm_state.shape[0], _sdims(dims, ssm_state),
-        float(scale), int(bool(qk_l2norm)), int(chunk), _ptr(out), _dt(out), _ptr(workspace),
+        float(scale), int(bool(qk_l2norm)), int(chunk), _gate(gate), _ptr(out), _dt(out),
+        _ptr(workspace),
         workspace.numel() * workspace.element_size(), _ptr(err), _stream(stream)))
 
 
@@ -202,7 +231,7 @@ def gdn_chunked_prefill_noalloc(mixed_qkv, a, b, A_log, dt_bias, conv_weight, co
                                 conv_state, ssm_state, cu_seqlens, slot, has_initial_state, out,
                                 dims: Dims, *, chunk=64, silu=True,
                                 conv_layout=GDN_CONV_DIM_FIRST, scale=None, qk_l2norm=True,
-                                err=None, stream=None):
+                                gate=None, err=None, stream=None):
     """gdn_chunked_prefill without a caller workspace, for callers that cannot allocate device
     memory: the library's fixed GDN_NOALLOC_SCRATCH_BYTES array serves as the workspace.
     Raises GDNError(GDN_ERR_SCRATCH_LIMIT) when the call needs more than that. Calls that may
@@ -217,8 +246,8 @@ def gdn_chunked_prefill_noalloc(mixed_qkv, a, b, A_log, dt_bias, conv_weight, co
         _ptr(conv_weight), _ptr(conv_bias), int(bool(silu)), _ptr(conv_state), conv_dt,
         int(conv_layout), _ptr(ssm_state), _ptr(cu_seqlens), _ptr(slot),
         _ptr(has_initial_state), N, T, ssm_state.shape[0], _sdims(dims, ssm_state),
-        float(scale), int(bool(qk_l2norm)), int(chunk), _ptr(out), _dt(out), _ptr(err),
-        _stream(stream)))
+        float(scale), int(bool(qk_l2norm)), int(chunk), _gate(gate), _ptr(out), _dt(out),
+        _ptr(err), _stream(stream)))
 
 
 class DecodeGraph:
@@ -227,9 +256,9 @@ class DecodeGraph:
 
     def __init__(self, mixed_qkv, a, b, A_log, dt_bias, conv_weight, conv_bias, conv_state,
                  ssm_state, slot, out, dims: Dims, *, silu=True, conv_layout=GDN_CONV_DIM_FIRST,
-                 scale=None, qk_l2norm=True, err=None):
+                 scale=None, qk_l2norm=True, gate=None, err=None):
         self._keep = (mixed_qkv, a, b, A_log, dt_bias, conv_weight, conv_bias, conv_state,
-                      ssm_state, slot, out, err)
+                      ssm_state, slot, out, err, gate)
         B = mixed_qkv.shape[0]
         scale = dims.dk ** -0.5 if scale is None else scale
         conv_dt = _dt(conv_state) if conv_state is not None else GDN_BF16
@@ -238,8 +267,8 @@ class DecodeGraph:
             _ptr(mixed_qkv), _ptr(a), _ptr(b), _gate_mode(a), _ptr(A_log), _ptr(dt_bias),
             _ptr(conv_weight), _ptr(conv_bias), int(bool(silu)), _ptr(conv_state), conv_dt,
             int(conv_layout), _ptr(ssm_state), _ptr(slot), B, ssm_state.shape[0],
-            _sdims(dims, ssm_state), float(scale), int(bool(qk_l2norm)), _ptr(out), _dt(out),
-            _ptr(err), ctypes.byref(h)))
+            _sdims(dims, ssm_state), float(scale), int(bool(qk_l2norm)), _gate(gate), _ptr(out),
+            _dt(out), _ptr(err), ctypes.byref(h)))
         self._h = h
 
     def launch(self, stream=None):

@@ -75,6 +75,29 @@ gdn_status check_layer(const void* mixed, const void* a, const void* b, gdn_gate
   return GDN_OK;
 }
 
+// The optional output gate: NULL leaves `la` ungated.
+gdn_status check_gate(const gdn_output_gate* g, gdn::LayerArgs& la) {
+  la.gated = 0;
+  la.gate_z = nullptr;
+  la.gate_w = nullptr;
+  la.gate_offset = 0.0f;
+  la.gate_eps = 0.0f;
+  la.gate_act = 0;
+  if (!g) return GDN_OK;
+  if (!g->z || !g->weight || !aligned(g->z, 16) || !aligned(g->weight, 16))
+    return GDN_ERR_INVALID_ARG;
+  if (g->act != GDN_ACT_SILU && g->act != GDN_ACT_SIGMOID) return GDN_ERR_INVALID_ARG;
+  if (!(g->eps >= 0.0f) || !(g->eps < 3.0e38f) || !(g->weight_offset == g->weight_offset))
+    return GDN_ERR_INVALID_ARG;  // eps finite and non-negative, offset not NaN
+  la.gated = 1;
+  la.gate_z = g->z;
+  la.gate_w = g->weight;
+  la.gate_offset = g->weight_offset;
+  la.gate_eps = g->eps;
+  la.gate_act = g->act;
+  return GDN_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -104,7 +127,8 @@ gdn_status gdn_decode_step(const void* mixed_qkv, const void* a, const void* b,
                            void* conv_state, gdn_dtype conv_dtype, gdn_conv_layout conv_layout,
                            float* ssm_state, const int32_t* slot, int32_t batch,
                            int32_t num_slots, gdn_dims dims, float scale, int32_t qk_l2norm,
-                           void* out, gdn_dtype out_dtype, int32_t* err, void* stream) {
+                           const gdn_output_gate* gate, void* out, gdn_dtype out_dtype,
+                           int32_t* err, void* stream) {
   if (batch < 0) return GDN_ERR_INVALID_ARG;
   if (batch == 0) return GDN_OK;
   if (batch > 65535) return GDN_ERR_UNSUPPORTED;
@@ -113,6 +137,9 @@ gdn_status gdn_decode_step(const void* mixed_qkv, const void* a, const void* b,
                               silu, conv_state, conv_dtype, conv_layout, ssm_state, slot, num_slots,
                               dims, scale, qk_l2norm, out, out_dtype, err, la);
   if (st != GDN_OK) return st;
+  st = check_gate(gate, la);
+  if (st != GDN_OK) return st;
+  if (la.gated && !aligned(out, 16)) return GDN_ERR_INVALID_ARG;  // 16-byte gated stores
   return from_cuda(gdn::launch_decode(la, batch, static_cast<cudaStream_t>(stream)));
 }
 
@@ -134,9 +161,10 @@ gdn_status gdn_chunked_prefill(const void* mixed_qkv, const void* a, const void*
                                float* ssm_state, const int32_t* cu_seqlens, const int32_t* slot,
                                const uint8_t* has_initial_state, int32_t num_seqs,
                                int32_t total_tokens, int32_t num_slots, gdn_dims dims,
-                               float scale, int32_t qk_l2norm, int32_t chunk, void* out,
-                               gdn_dtype out_dtype, void* workspace, size_t workspace_bytes,
-                               int32_t* err, void* stream) {
+                               float scale, int32_t qk_l2norm, int32_t chunk,
+                               const gdn_output_gate* gate, void* out, gdn_dtype out_dtype,
+                               void* workspace, size_t workspace_bytes, int32_t* err,
+                               void* stream) {
   if (num_seqs < 0 || total_tokens < 0) return GDN_ERR_INVALID_ARG;
   if (chunk != 16 && chunk != 32 && chunk != 64) return GDN_ERR_UNSUPPORTED;
   if (num_seqs == 0) return total_tokens == 0 ? GDN_OK : GDN_ERR_INVALID_ARG;
@@ -155,6 +183,9 @@ gdn_status gdn_chunked_prefill(const void* mixed_qkv, const void* a, const void*
                               silu, conv_state, conv_dtype, conv_layout, ssm_state, slot, num_slots,
                               dims, scale, qk_l2norm, out, out_dtype, err, la);
   if (st != GDN_OK) return st;
+  st = check_gate(gate, la);
+  if (st != GDN_OK) return st;
+  if (la.gated && !aligned(out, 16)) return GDN_ERR_INVALID_ARG;  // vector row access
   const size_t need = gdn_chunked_prefill_workspace_size(total_tokens, num_seqs, dims, chunk);
   if (!workspace || workspace_bytes < need || !aligned(workspace, 16)) return GDN_ERR_INVALID_ARG;
   gdn::PrefillExtra p{cu_seqlens, has_initial_state, num_seqs, total_tokens, chunk, workspace,

@@ -194,12 +194,16 @@ struct DecodeCfg {
   static constexpr int kGroups = (2 * DK + kUnitRows) / 8;  // 8-channel conv groups per unit
   static constexpr int kSetupWarps = 2;
   static constexpr int kSetupBufs = kCoopSetup ? 2 : 2 * kSetupWarps;
-  static constexpr int kThreads = 32 * (1 + kSetupWarps + kConsumerWarps);
+  // + 1 epilogue warp (the output gate; it returns at once in an ungated call)
+  static constexpr int kEpiWarp = 1 + kSetupWarps + kConsumerWarps;
+  static constexpr int kThreads = 32 * (kEpiWarp + 1);
   static constexpr int kSetupFloats = 2 * DK + kUnitRows + 2 * R + 1;  // q^, k^, v, a, b, k.q
   static constexpr int kSetupStride = (kSetupFloats + 31) / 32 * 32;
-  // dynamic shared memory: ring, the setup buffers, then the mbarriers
-  static constexpr int kBarOffset = kRingBytes + kSetupBufs * kSetupStride * 4;
-  static constexpr int kNumBars = 2 * kNumStages + 2 * kSetupBufs;
+  // dynamic shared memory: ring, the setup buffers, two unit-sized o buffers
+  // (gated calls), then the mbarriers
+  static constexpr int kOBufOffset = kRingBytes + kSetupBufs * kSetupStride * 4;
+  static constexpr int kBarOffset = kOBufOffset + 2 * kUnitRows * 4;
+  static constexpr int kNumBars = 2 * kNumStages + 2 * kSetupBufs + 4;
   static constexpr int kSmemBytes = kBarOffset + kNumBars * 8;
   static_assert(kSmemBytes <= 227 * 1024, "decode shared memory exceeds the per-CTA limit");
 };
@@ -341,9 +345,12 @@ __global__ void __launch_bounds__(DecodeCfg<DK, R, kBf16State>::kThreads, 1)
   unsigned char* ring = smem;
   float* setup = reinterpret_cast<float*>(smem + kRingBytes);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Cfg::kBarOffset);
-  // bars: full[NS], empty[NS], setup_full[NB], setup_empty[NB]
+  float* obuf = reinterpret_cast<float*>(smem + Cfg::kOBufOffset);
+  // bars: full[NS], empty[NS], setup_full[NB], setup_empty[NB], o_full[2], o_empty[2]
   const uint32_t full0 = smem_addr(bars), empty0 = smem_addr(bars + NS);
   const uint32_t sfull0 = smem_addr(bars + 2 * NS), sempty0 = smem_addr(bars + 2 * NS + NB);
+  const uint32_t ofull0 = smem_addr(bars + 2 * NS + 2 * NB);
+  const uint32_t oempty0 = smem_addr(bars + 2 * NS + 2 * NB + 2);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (tid == 0) {
@@ -354,6 +361,10 @@ __global__ void __launch_bounds__(DecodeCfg<DK, R, kBf16State>::kThreads, 1)
     for (int i = 0; i < NB; ++i) {
       mbar_init(sfull0 + 8 * i, Cfg::kCoopSetup ? 32 * SW : 32);
       mbar_init(sempty0 + 8 * i, kConsumerWarps);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(ofull0 + 8 * i, kConsumerWarps);
+      mbar_init(oempty0 + 8 * i, 1);
     }
     fence_mbar_init();
   }
@@ -515,6 +526,101 @@ __global__ void __launch_bounds__(DecodeCfg<DK, R, kBf16State>::kThreads, 1)
     return;
   }
 
+  if (warp == Cfg::kEpiWarp) {
+    // ------------------------------------------------------------ epilogue
+    // Output gate (gated calls only): per active unit, wait for the consumers'
+    // fp32 o in o buffer n % 2, then per value head
+    //   out = o / sqrt(mean(o^2) + eps) * (w + offset) * act(z).
+    // A lane takes 8-element chunks c = lane + 32 j of the unit's R*dv outputs;
+    // the dv/8 lanes of one head sum o^2 with xor shuffles.
+    if (!a.gated) return;
+    constexpr int NCH = Cfg::kUnitRows / 8;
+    constexpr int NCL = (NCH + 31) / 32;
+    constexpr int LPH = DV / 8;  // lanes per head within one pass
+    float wv[NCL][8];
+#pragma unroll
+    for (int j = 0; j < NCL; ++j) {
+      const int c = lane + 32 * j;
+      const int i0 = (8 * c) % DV;
+      const float4 w0 = __ldg(reinterpret_cast<const float4*>(a.gate_w + i0));
+      const float4 w1 = __ldg(reinterpret_cast<const float4*>(a.gate_w + i0 + 4));
+      const float wr[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+      for (int e = 0; e < 8; ++e) wv[j][e] = wr[e] + a.gate_offset;
+    }
+    UnitSlots slots;
+    uint32_t n = 0;
+    for (int i = 0, u = blockIdx.x; u < num_units; ++i, u += G) {
+      const int b = u / a.Hk, kh = u % a.Hk;
+      const int32_t s = slots.get(a, i, num_units, lane);
+      if (!unit_active(s, a.num_slots)) continue;
+      const uint32_t po = n & 1, use = n >> 1;
+      const int64_t base = (static_cast<int64_t>(b) * a.Hv + kh * R) * DV;
+      uint4 zr[NCL];
+#pragma unroll
+      for (int j = 0; j < NCL; ++j) {
+        const int c = lane + 32 * j;
+        zr[j] = c < NCH ? __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.gate_z) +
+                                                               base + 8 * c))
+                        : make_uint4(0u, 0u, 0u, 0u);
+      }
+      if (!__all_sync(0xffffffffu, mbar_wait_bounded(ofull0 + 8 * po, use & 1))) {
+        if (lane == 0 && a.err) atomicOr(a.err, GDN_DEVERR_TIMEOUT);
+        return;
+      }
+      const float* ob = obuf + po * Cfg::kUnitRows;
+#pragma unroll
+      for (int j = 0; j < NCL; ++j) {
+        const int c = lane + 32 * j;
+        const bool on = c < NCH;
+        float ov[8];
+        if (on) {
+          const float4 o0 = reinterpret_cast<const float4*>(ob + 8 * c)[0];
+          const float4 o1 = reinterpret_cast<const float4*>(ob + 8 * c)[1];
+          ov[0] = o0.x; ov[1] = o0.y; ov[2] = o0.z; ov[3] = o0.w;
+          ov[4] = o1.x; ov[5] = o1.y; ov[6] = o1.z; ov[7] = o1.w;
+        } else {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) ov[e] = 0.0f;
+        }
+        float ss = 0.0f;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) ss = fmaf(ov[e], ov[e], ss);
+#pragma unroll
+        for (int m = LPH / 2; m >= 1; m >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, m);
+        const float den = ss / static_cast<float>(DV) + a.gate_eps;
+        const float inv = den > 0.0f ? 1.0f / sqrtf(den) : 0.0f;  // all-zero head, eps 0
+        float z8[8], y[8];
+        unpack8(zr[j], z8);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float act = a.gate_act == GDN_ACT_SIGMOID
+                                ? __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-z8[e])))
+                                : silu_f(z8[e]);
+          y[e] = ((ov[e] * inv) * wv[j][e]) * act;
+        }
+        if (on) {
+          if (a.out_f32) {
+            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(a.out) + base + 8 * c);
+            dst[0] = make_float4(y[0], y[1], y[2], y[3]);
+            dst[1] = make_float4(y[4], y[5], y[6], y[7]);
+          } else {
+            uint4 pk;
+            pk.x = pack_bf2(y[0], y[1]);
+            pk.y = pack_bf2(y[2], y[3]);
+            pk.z = pack_bf2(y[4], y[5]);
+            pk.w = pack_bf2(y[6], y[7]);
+            *reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.out) + base + 8 * c) = pk;
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(oempty0 + 8 * po);  // the consumers may refill this buffer
+      ++n;
+    }
+    return;
+  }
+
   // -------------------------------------------------------------- consumers
   const int cw = warp - 1 - SW;
   constexpr int RPW = Cfg::kRowsPerWarp;
@@ -537,6 +643,13 @@ __global__ void __launch_bounds__(DecodeCfg<DK, R, kBf16State>::kThreads, 1)
       if (lane == 0 && a.err) atomicOr(a.err, GDN_DEVERR_TIMEOUT);
       return;
     }
+    const uint32_t po = n & 1;  // o buffer of a gated call
+    if (a.gated &&
+        !__all_sync(0xffffffffu, mbar_wait_bounded(oempty0 + 8 * po, ((n >> 1) & 1) ^ 1))) {
+      if (lane == 0 && a.err) atomicOr(a.err, GDN_DEVERR_TIMEOUT);
+      return;
+    }
+    float* ob = obuf + po * Cfg::kUnitRows;
     const float* buf = setup + p * Cfg::kSetupStride;
     float qv[VPL], kv[VPL];
 #pragma unroll
@@ -583,7 +696,8 @@ __global__ void __launch_bounds__(DecodeCfg<DK, R, kBf16State>::kThreads, 1)
       const float delta = be * (vb[row0 + ri] - al * pk);
       if (lane % (2 * LPV) == 0) {  // o_i = a (S q)_i + d_i (k . q)
         const float ov = fmaf(delta, kq, al * pq);
-        if (a.out_f32) static_cast<float*>(a.out)[out_base + row0 + ri] = ov;
+        if (a.gated) ob[row0 + ri] = ov;  // the epilogue warp gates and stores it
+        else if (a.out_f32) static_cast<float*>(a.out)[out_base + row0 + ri] = ov;
         else static_cast<uint16_t*>(a.out)[out_base + row0 + ri] = f2bf(ov);
       }
 #pragma unroll
@@ -594,7 +708,10 @@ __global__ void __launch_bounds__(DecodeCfg<DK, R, kBf16State>::kThreads, 1)
       }
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(sempty0 + 8 * p);  // this warp no longer reads the setup buffer
+    if (lane == 0) {
+      mbar_arrive(sempty0 + 8 * p);  // this warp no longer reads the setup buffer
+      if (a.gated) mbar_arrive(ofull0 + 8 * po);  // its o values are in the o buffer
+    }
     ++n;
   }
 }

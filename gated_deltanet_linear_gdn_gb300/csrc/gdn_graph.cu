@@ -27,8 +27,8 @@ gdn_status gdn_decode_graph_create(const void* mixed_qkv, const void* a, const v
                                    gdn_dtype conv_dtype, gdn_conv_layout conv_layout,
                                    float* ssm_state, const int32_t* slot, int32_t batch,
                                    int32_t num_slots, gdn_dims dims, float scale,
-                                   int32_t qk_l2norm, void* out, gdn_dtype out_dtype,
-                                   int32_t* err, gdn_graph** graph_out) {
+                                   int32_t qk_l2norm, const gdn_output_gate* gate, void* out,
+                                   gdn_dtype out_dtype, int32_t* err, gdn_graph** graph_out) {
   if (!graph_out) return GDN_ERR_INVALID_ARG;
   *graph_out = nullptr;
   if (batch <= 0) return GDN_ERR_INVALID_ARG;
@@ -42,7 +42,7 @@ gdn_status gdn_decode_graph_create(const void* mixed_qkv, const void* a, const v
   }
   st = gdn_decode_step(mixed_qkv, a, b, gate_mode, A_log, dt_bias, conv_weight, conv_bias, silu,
                        conv_state, conv_dtype, conv_layout, ssm_state, slot, batch, num_slots,
-                       dims, scale, qk_l2norm, out, out_dtype, err, cs);
+                       dims, scale, qk_l2norm, gate, out, out_dtype, err, cs);
   const cudaError_t ce = cudaStreamEndCapture(cs, &g);
   cudaStreamDestroy(cs);
   if (st != GDN_OK) {

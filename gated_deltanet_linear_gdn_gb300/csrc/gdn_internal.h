@@ -49,6 +49,13 @@ struct LayerArgs {
   void* out;
   int out_f32;
   int32_t* err;
+  // output gate (gated RMSNorm of o per value head); gated == 0: out = o
+  int gated;
+  const void* gate_z;  // [tokens, Hv, dv] bf16
+  const float* gate_w; // [dv]
+  float gate_offset;
+  float gate_eps;
+  int gate_act;        // gdn_gate_act
 };
 
 struct PrefillExtra {
@@ -63,6 +70,8 @@ struct PrefillExtra {
 
 cudaError_t launch_conv_update(const ConvUpdateArgs& a, cudaStream_t s);
 cudaError_t launch_decode(const LayerArgs& a, int B, cudaStream_t s);
+// the output gate in place over `rows` rows of dv values of a.out (gdn_gate.cu)
+cudaError_t launch_output_gate(const LayerArgs& a, int64_t rows, cudaStream_t s);
 cudaError_t launch_prefill(const LayerArgs& a, const PrefillExtra& p, cudaStream_t s);
 size_t prefill_workspace_bytes(int total_tokens, int num_seqs, int Hk, int Hv, int dk, int dv,
                                int chunk, int conv);

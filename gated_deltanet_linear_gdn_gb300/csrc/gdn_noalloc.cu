@@ -60,8 +60,8 @@ extern "C" gdn_status gdn_chunked_prefill_noalloc(
     int32_t silu, void* conv_state, gdn_dtype conv_dtype, gdn_conv_layout conv_layout,
     float* ssm_state, const int32_t* cu_seqlens, const int32_t* slot,
     const uint8_t* has_initial_state, int32_t num_seqs, int32_t total_tokens, int32_t num_slots,
-    gdn_dims dims, float scale, int32_t qk_l2norm, int32_t chunk, void* out, gdn_dtype out_dtype,
-    int32_t* err, void* stream) {
+    gdn_dims dims, float scale, int32_t qk_l2norm, int32_t chunk, const gdn_output_gate* gate,
+    void* out, gdn_dtype out_dtype, int32_t* err, void* stream) {
   if (num_seqs < 0 || total_tokens < 0) return GDN_ERR_INVALID_ARG;
   const size_t need = gdn_chunked_prefill_workspace_size(total_tokens, num_seqs, dims, chunk);
   if (need == 0) {
@@ -69,8 +69,8 @@ extern "C" gdn_status gdn_chunked_prefill_noalloc(
     return gdn_chunked_prefill(mixed_qkv, a, b, gate_mode, A_log, dt_bias, conv_weight,
                                conv_bias, silu, conv_state, conv_dtype, conv_layout, ssm_state,
                                cu_seqlens, slot, has_initial_state, num_seqs, total_tokens,
-                               num_slots, dims, scale, qk_l2norm, chunk, out, out_dtype, nullptr,
-                               0, err, stream);
+                               num_slots, dims, scale, qk_l2norm, chunk, gate, out, out_dtype,
+                               nullptr, 0, err, stream);
   }
   if (need > static_cast<size_t>(GDN_NOALLOC_SCRATCH_BYTES)) return GDN_ERR_SCRATCH_LIMIT;
   void* ws = nullptr;
@@ -78,6 +78,6 @@ extern "C" gdn_status gdn_chunked_prefill_noalloc(
   return gdn_chunked_prefill(mixed_qkv, a, b, gate_mode, A_log, dt_bias, conv_weight, conv_bias,
                              silu, conv_state, conv_dtype, conv_layout, ssm_state, cu_seqlens,
                              slot, has_initial_state, num_seqs, total_tokens, num_slots, dims,
-                             scale, qk_l2norm, chunk, out, out_dtype, ws,
+                             scale, qk_l2norm, chunk, gate, out, out_dtype, ws,
                              static_cast<size_t>(GDN_NOALLOC_SCRATCH_BYTES), err, stream);
 }

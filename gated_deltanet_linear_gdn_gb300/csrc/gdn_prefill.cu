@@ -475,12 +475,16 @@ size_t prefill_workspace_bytes(int total_tokens, int num_seqs, int Hk, int Hv, i
 }
 
 cudaError_t launch_prefill(const LayerArgs& a, const PrefillExtra& p, cudaStream_t s) {
+  cudaError_t e;
   switch (a.dk) {
-    case 32: return launch_prefill_dk<32>(a, p, s);
-    case 64: return launch_prefill_dk<64>(a, p, s);
-    case 128: return a.dv == 128 ? launch_prefill_tc(a, p, s) : launch_prefill_dk<128>(a, p, s);
+    case 32: e = launch_prefill_dk<32>(a, p, s); break;
+    case 64: e = launch_prefill_dk<64>(a, p, s); break;
+    case 128: e = a.dv == 128 ? launch_prefill_tc(a, p, s) : launch_prefill_dk<128>(a, p, s); break;
     default: return cudaErrorInvalidValue;
   }
+  if (e != cudaSuccess || !a.gated) return e;
+  // the output gate over every (token, value head) row of out, after the state pass
+  return launch_output_gate(a, static_cast<int64_t>(p.total_tokens) * a.Hv, s);
 }
 
 }  // namespace gdn

@@ -87,6 +87,34 @@ typedef struct {
   int32_t state_bf16;
 } gdn_dims;
 
+/*
+ * Output gate of the GDN block: a gated RMSNorm of the core output o over each
+ * value head, before the output projection (RL-Kernel PRs #466-#468, "Gated
+ * RMSNorm CUDA kernel for the GDN block": Summary by CodeRabbit -- SiLU or
+ * sigmoid gating -- and Walkthrough -- a weight offset). Per token t and value
+ * head h, with o the core output:
+ *   out[t, h, i] = o[i] / sqrt(mean_j o[j]^2 + eps) * (weight[i] + weight_offset)
+ *                  * act(z[t, h, i]),   act = SiLU (z * sigmoid(z)) or sigmoid,
+ * and an all-zero o with eps 0 gating to zero. The norm comes before the gate.
+ * Arithmetic is fp32; the result is stored in out_dtype. The decode step gates
+ * the unrounded fp32 o inside its own kernel; the chunked prefill stores o in
+ * out_dtype first and gates it in place after its state pass (with a bf16
+ * output that is the block's unfused arithmetic). weight_offset is 0 for the
+ * plain form and 1 for the zero-centred one (weight stored as w - 1). `out`
+ * must be 16-byte aligned in a gated call.
+ *   z       [tokens, Hv, dv] bf16, 16-byte aligned (tokens = B for decode)
+ *   weight  [dv] f32, 16-byte aligned
+ *   eps     >= 0 (1e-6 in Qwen3-Next)
+ */
+typedef enum { GDN_ACT_SILU = 0, GDN_ACT_SIGMOID = 1 } gdn_gate_act;
+typedef struct {
+  const void* z;
+  const float* weight;
+  float weight_offset;
+  float eps;
+  int32_t act; /* gdn_gate_act */
+} gdn_output_gate;
+
 /* Bits of the device error word (int32, caller-zeroed; the kernels only OR
  * bits into it with plain stores). */
 #define GDN_DEVERR_SLOT_RANGE 1 /* an active slot >= num_slots */
@@ -146,6 +174,8 @@ gdn_status gdn_conv_update(const void* x, void* conv_state, gdn_dtype state_dtyp
  *   ssm_state   [num_slots, Hv, dv, dk] f32 (bf16 when dims.state_bf16), in place
  *   slot        [B] int32
  *   scale       multiplier applied to q (dk^-0.5 in Qwen3-Next)
+ *   gate        NULL: out = o. Otherwise out = the gated RMSNorm of o (see
+ *               gdn_output_gate), computed in the same kernel from the fp32 o
  *   out         [B, Hv, dv] of out_dtype (bf16 or f32); inactive rows zeroed
  * Supported: dk == dv in {32, 64, 128}, W == 4, Hv % Hk == 0, D % 8 == 0.
  */
@@ -155,7 +185,8 @@ gdn_status gdn_decode_step(const void* mixed_qkv, const void* a, const void* b,
                            void* conv_state, gdn_dtype conv_dtype, gdn_conv_layout conv_layout,
                            float* ssm_state, const int32_t* slot, int32_t batch,
                            int32_t num_slots, gdn_dims dims, float scale, int32_t qk_l2norm,
-                           void* out, gdn_dtype out_dtype, int32_t* err, void* stream);
+                           const gdn_output_gate* gate, void* out, gdn_dtype out_dtype,
+                           int32_t* err, void* stream);
 
 /*
  * gdn_chunked_prefill_workspace_size -- bytes of device workspace that
@@ -185,6 +216,8 @@ size_t gdn_chunked_prefill_workspace_size(int32_t total_tokens, int32_t num_seqs
  *   cu_seqlens  [num_seqs + 1] int32, device: 0 = c0 <= c1 <= ... = total_tokens
  *   slot        [num_seqs] int32;  has_initial_state [num_seqs] uint8 or NULL
  *   out         [total_tokens, Hv, dv] of out_dtype
+ *   gate        NULL, or the output gate applied to every token's o (as in
+ *               gdn_decode_step)
  *   chunk       chunk size C in {16, 32, 64}
  *   workspace   device scratch of >= gdn_chunked_prefill_workspace_size bytes,
  *               16-byte aligned; its contents on entry do not matter
@@ -199,9 +232,10 @@ gdn_status gdn_chunked_prefill(const void* mixed_qkv, const void* a, const void*
                                float* ssm_state, const int32_t* cu_seqlens, const int32_t* slot,
                                const uint8_t* has_initial_state, int32_t num_seqs,
                                int32_t total_tokens, int32_t num_slots, gdn_dims dims,
-                               float scale, int32_t qk_l2norm, int32_t chunk, void* out,
-                               gdn_dtype out_dtype, void* workspace, size_t workspace_bytes,
-                               int32_t* err, void* stream);
+                               float scale, int32_t qk_l2norm, int32_t chunk,
+                               const gdn_output_gate* gate, void* out, gdn_dtype out_dtype,
+                               void* workspace, size_t workspace_bytes, int32_t* err,
+                               void* stream);
 
 /*
  * gdn_chunked_prefill_noalloc -- gdn_chunked_prefill for callers that cannot
@@ -241,16 +275,18 @@ gdn_status gdn_chunked_prefill_noalloc(const void* mixed_qkv, const void* a, con
                                        const int32_t* slot, const uint8_t* has_initial_state,
                                        int32_t num_seqs, int32_t total_tokens, int32_t num_slots,
                                        gdn_dims dims, float scale, int32_t qk_l2norm,
-                                       int32_t chunk, void* out, gdn_dtype out_dtype,
-                                       int32_t* err, void* stream);
+                                       int32_t chunk, const gdn_output_gate* gate, void* out,
+                                       gdn_dtype out_dtype, int32_t* err, void* stream);
 
 /*
  * CUDA-graph decode buckets ([P2] Rocket, "A reduction barrier makes Qwen GDN
  * graph replay bit exact": immutable graphs per decode bucket c1, c2, ...,
  * inactive rows cleared on bucket transitions, slot 0 untouched).
  *
- * gdn_decode_graph_create captures ONE gdn_decode_step call -- same arguments,
- * same validation and the same result codes -- into an instantiated CUDA graph
+ * gdn_decode_graph_create captures ONE gdn_decode_step call -- same arguments
+ * (the gate struct, if any, is read at creation; its z and weight buffers are
+ * kept by pointer like every other buffer), same validation and the same
+ * result codes -- into an instantiated CUDA graph
  * and returns it in *graph_out. Nothing runs at creation. The graph keeps the
  * pointers it was created with: the caller keeps those buffers alive and
  * unmoved, and writes each step's inputs (x, gate inputs, slot table) into
@@ -270,8 +306,8 @@ gdn_status gdn_decode_graph_create(const void* mixed_qkv, const void* a, const v
                                    gdn_dtype conv_dtype, gdn_conv_layout conv_layout,
                                    float* ssm_state, const int32_t* slot, int32_t batch,
                                    int32_t num_slots, gdn_dims dims, float scale,
-                                   int32_t qk_l2norm, void* out, gdn_dtype out_dtype,
-                                   int32_t* err, gdn_graph** graph_out);
+                                   int32_t qk_l2norm, const gdn_output_gate* gate, void* out,
+                                   gdn_dtype out_dtype, int32_t* err, gdn_graph** graph_out);
 gdn_status gdn_graph_launch(gdn_graph* graph, void* stream);
 void gdn_graph_destroy(gdn_graph* graph);
 

@@ -633,14 +633,16 @@ int gdn_ref_layer(const uint16_t* mixed_qkv, const void* a, const void* b, int g
  *   y[i] = o[i] / sqrt(mean_j o[j]^2 + eps) * (w[i] + offset) * act(z[i]),
  * act = SiLU (z * sigmoid(z), act_kind 0) or sigmoid (act_kind 1). The norm is
  * taken before the gate (the GDN block normalises the core output, then gates
- * it with z). z arrives as bf16 bits, w as fp32; all arithmetic is fp64. */
+ * it with z). z arrives as bf16 bits, w as fp32; all arithmetic is fp64. The
+ * pages leave 0/0 open: an all-zero head with eps = 0 gates to zero. */
 void gdn_ref_gated_rmsnorm(const double* o, const uint16_t* z, const float* w, double offset,
                            double eps, int act_kind, int64_t rows, int dv, double* y) {
   for (int64_t r = 0; r < rows; ++r) {
     const double* orow = o + (size_t)r * dv;
     double ss = 0.0;
     for (int i = 0; i < dv; ++i) ss += orow[i] * orow[i];
-    const double inv = 1.0 / sqrt(ss / dv + eps);
+    const double den = ss / dv + eps;
+    const double inv = den > 0.0 ? 1.0 / sqrt(den) : 0.0; /* all-zero head, eps 0: zero out */
     for (int i = 0; i < dv; ++i) {
       const double zi = bf16_to_f64(z[(size_t)r * dv + i]);
       const double gate = act_kind == 0 ? zi * gdn_ref_sigmoid(zi) : gdn_ref_sigmoid(zi);

@@ -63,7 +63,7 @@ class Device:
         return torch_to_bits(self.conv_state)
 
 
-def gpu_decode(d: Device, out_f32=True, silu=None, stream=None):
+def gpu_decode(d: Device, out_f32=True, silu=None, stream=None, gate=None):
     inp = d.inp
     geo = inp.geo
     B = inp.slot.size
@@ -72,11 +72,12 @@ def gpu_decode(d: Device, out_f32=True, silu=None, stream=None):
     gdn.gdn_decode_step(d.mixed, d.a, d.b, d.A_log, d.dt_bias, d.conv_w, d.conv_b, d.conv_state,
                         d.ssm, d.slot, out, dims_of(geo),
                         silu=inp.silu if silu is None else silu, conv_layout=inp.conv_layout,
-                        scale=inp.scale, qk_l2norm=inp.qk_l2norm, err=d.err, stream=stream)
+                        scale=inp.scale, qk_l2norm=inp.qk_l2norm, gate=gate, err=d.err,
+                        stream=stream)
     return out
 
 
-def gpu_prefill(d: Device, chunk=64, out_f32=True, workspace=None, stream=None):
+def gpu_prefill(d: Device, chunk=64, out_f32=True, workspace=None, stream=None, gate=None):
     inp = d.inp
     geo = inp.geo
     T = inp.total_tokens
@@ -90,7 +91,7 @@ def gpu_prefill(d: Device, chunk=64, out_f32=True, workspace=None, stream=None):
                             d.conv_state, d.ssm, d.cu, d.slot, d.has_init, out, workspace,
                             dims_of(geo), chunk=chunk, silu=inp.silu,
                             conv_layout=inp.conv_layout, scale=inp.scale,
-                            qk_l2norm=inp.qk_l2norm, err=d.err, stream=stream)
+                            qk_l2norm=inp.qk_l2norm, gate=gate, err=d.err, stream=stream)
     return out
 
 

@@ -89,13 +89,13 @@ def _decode(L, dims=None, **kw):
     d = dims or gdn.Dims(2, 4, 32, 32)
     args = dict(mixed=FAKE, a=FAKE, b=FAKE, gm=0, A=FAKE, dt=FAKE, cw=None, cb=None, silu=1,
                 cs=None, cdt=0, lay=0, ssm=FAKE, slot=FAKE, B=2, ns=8, scale=0.1, l2=1,
-                out=FAKE, odt=1)
+                gate=None, out=FAKE, odt=1)
     args.update(kw)
     return L.gdn_decode_step(args["mixed"], args["a"], args["b"], args["gm"], args["A"],
                              args["dt"], args["cw"], args["cb"], args["silu"], args["cs"],
                              args["cdt"], args["lay"], args["ssm"], args["slot"], args["B"],
-                             args["ns"], d.c(), args["scale"], args["l2"], args["out"],
-                             args["odt"], None, None)
+                             args["ns"], d.c(), args["scale"], args["l2"], args["gate"],
+                             args["out"], args["odt"], None, None)
 
 
 def test_decode_argument_errors(L):
@@ -113,16 +113,40 @@ def test_decode_argument_errors(L):
     assert _decode(L, odt=9) == gdn.GDN_ERR_INVALID_ARG
 
 
+def _gate_struct(z=FAKE, w=FAKE, off=0.0, eps=1e-6, act=0):
+    g = gdn.gdn_output_gate(z, w, off, eps, act)
+    return ctypes.byref(g), g
+
+
+def test_output_gate_argument_errors(L):
+    """Every call here fails a host check before anything is launched."""
+    for kw, want in [(dict(z=None), gdn.GDN_ERR_INVALID_ARG),
+                     (dict(w=None), gdn.GDN_ERR_INVALID_ARG),
+                     (dict(z=P(0x10008)), gdn.GDN_ERR_INVALID_ARG),   # z not 16-byte aligned
+                     (dict(w=P(0x10004)), gdn.GDN_ERR_INVALID_ARG),   # weight not 16-byte aligned
+                     (dict(act=2), gdn.GDN_ERR_INVALID_ARG),
+                     (dict(eps=-1.0), gdn.GDN_ERR_INVALID_ARG),
+                     (dict(eps=float("nan")), gdn.GDN_ERR_INVALID_ARG),
+                     (dict(eps=float("inf")), gdn.GDN_ERR_INVALID_ARG),
+                     (dict(off=float("nan")), gdn.GDN_ERR_INVALID_ARG)]:
+        ref, _keep = _gate_struct(**kw)
+        assert _decode(L, gate=ref) == want, kw
+    ref, _keep = _gate_struct()
+    assert _decode(L, gate=ref, out=P(0x10004)) == gdn.GDN_ERR_INVALID_ARG  # gated out 16 B
+    assert _decode(L, gate=ref, ssm=None) == gdn.GDN_ERR_INVALID_ARG  # layer checks come first
+
+
 def test_prefill_argument_errors(L):
     d = gdn.Dims(2, 4, 32, 32)
 
     def call(**kw):
-        args = dict(cu=FAKE, slot=FAKE, N=1, T=8, chunk=16, ws=FAKE, nbytes=1 << 30, mixed=FAKE)
+        args = dict(cu=FAKE, slot=FAKE, N=1, T=8, chunk=16, ws=FAKE, nbytes=1 << 30, mixed=FAKE,
+                    gate=None)
         args.update(kw)
         return L.gdn_chunked_prefill(args["mixed"], FAKE, FAKE, 0, FAKE, FAKE, None, None, 1,
                                      None, 0, 0, FAKE, args["cu"], args["slot"], None, args["N"],
-                                     args["T"], 8, d.c(), 0.1, 1, args["chunk"], FAKE, 1,
-                                     args["ws"], args["nbytes"], None, None)
+                                     args["T"], 8, d.c(), 0.1, 1, args["chunk"], args["gate"],
+                                     FAKE, 1, args["ws"], args["nbytes"], None, None)
 
     assert call(N=0, T=0) == gdn.GDN_OK
     assert call(N=0, T=5) == gdn.GDN_ERR_INVALID_ARG

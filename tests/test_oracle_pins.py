@@ -657,5 +657,6 @@ def test_gated_rmsnorm_closed_forms(oracle):
     ones = np.ones(128, np.float32)
     assert np.array_equal(oracle.gated_rmsnorm(o, z, np.zeros(128, np.float32), offset=1.0),
                           oracle.gated_rmsnorm(o, z, ones, offset=0.0))
-    # eps enters under the root: a zero head stays zero, a tiny head is not blown up
+    # eps enters under the root: a zero head stays zero, with or without eps (0/0 reads as 0)
     assert np.all(oracle.gated_rmsnorm(np.zeros((1, 128)), z[0, :1], w, eps=1e-6) == 0.0)
+    assert np.all(oracle.gated_rmsnorm(np.zeros((1, 128)), z[0, :1], w, eps=0.0) == 0.0)
