@@ -319,6 +319,44 @@ def run_ours(args, rank, world):
             del tt, ws
         torch.cuda.empty_cache()
 
+    # ---- mixed step: 64 decode rows + one 4096-token prefill (with conv) ----
+    mixed = {}
+    if not args.no_prefill:
+        nd, Tp = 64, 4096
+        inp = gi.make_inputs(geo, [1] * nd + [Tp], NUM_SLOTS, seed=12, state_pool=False)
+        mt = dict(mixed=b16(inp.mixed).to(dev), a=b16(inp.a).to(dev), b=b16(inp.b).to(dev),
+                  A_log=torch.from_numpy(inp.A_log).to(dev),
+                  dt_bias=torch.from_numpy(inp.dt_bias).to(dev),
+                  conv_w=b16(inp.conv_w).to(dev), conv_b=b16(inp.conv_b).to(dev),
+                  conv=b16(inp.conv_state).to(dev),
+                  ssm=gi.device_state_pool(NUM_SLOTS, geo, 0.05, 13, dev),
+                  slot=torch.from_numpy(inp.slot).to(dev),
+                  cu=torch.tensor([0, Tp], dtype=torch.int32, device=dev),
+                  out=torch.empty(nd + Tp, geo.Hv, geo.dv, dtype=torch.bfloat16, device=dev))
+        ws = torch.empty(gdn.gdn_chunked_prefill_workspace_size(Tp, 1, dims, 64),
+                         dtype=torch.uint8, device=dev)
+
+        def mixed_call():
+            gdn.gdn_mixed_step(mt["mixed"], mt["a"], mt["b"], mt["A_log"], mt["dt_bias"],
+                               mt["conv_w"], mt["conv_b"], mt["conv"], mt["ssm"], mt["slot"], nd,
+                               mt["cu"], None, mt["out"], ws, dims, chunk=64, stream=stream)
+
+        def separate_calls():
+            gdn.gdn_decode_step(mt["mixed"][:nd], mt["a"][:nd], mt["b"][:nd], mt["A_log"],
+                                mt["dt_bias"], mt["conv_w"], mt["conv_b"], mt["conv"], mt["ssm"],
+                                mt["slot"][:nd], mt["out"][:nd], dims, stream=stream)
+            gdn.gdn_chunked_prefill(mt["mixed"][nd:], mt["a"][nd:], mt["b"][nd:], mt["A_log"],
+                                    mt["dt_bias"], mt["conv_w"], mt["conv_b"], mt["conv"],
+                                    mt["ssm"], mt["cu"], mt["slot"][nd:], None, mt["out"][nd:],
+                                    ws, dims, chunk=64, stream=stream)
+        ms_m = float(np.median(timed(mixed_call, 7, 3)))
+        ms_s = float(np.median(timed(separate_calls, 7, 3)))
+        mixed["decode64_prefill4096"] = {"mixed_us": round(ms_m * 1e3, 1),
+                                         "separate_us": round(ms_s * 1e3, 1),
+                                         "speedup": round(ms_s / ms_m, 3)}
+        del mt, ws
+        torch.cuda.empty_cache()
+
     # ---- e2e through the public API with pinned host buffers ----
     t = decode_setup(args.batch, args.num_slots, seed=args.batch, state_bf16=args.state_bf16)
     h_mixed = t["mixed"].cpu().pin_memory()
@@ -380,6 +418,7 @@ def run_ours(args, rank, world):
         "clocks": clk,
         "decode_sweep": sweep,
         "prefill": prefill,
+        "mixed_step": mixed,
         "context": {"pages_gb10_c16_GBps": 175.14,
                     "note": "GB10 (SM121) whole GDN transition incl. W4A4 projections; context only"},
     }

@@ -117,6 +117,10 @@ def lib():
         L.gdn_chunked_prefill_noalloc.argtypes = [P, P, P, I32, P, P, P, P, I32, P, I32, I32, P,
                                                   P, P, P, I32, I32, I32, gdn_dims, F, I32, I32,
                                                   P, P, I32, P, P]
+        L.gdn_mixed_step.restype = I32
+        L.gdn_mixed_step.argtypes = [P, P, P, I32, P, P, P, P, I32, P, I32, I32, P, P, I32, P, P,
+                                     I32, I32, I32, gdn_dims, F, I32, I32, P, P, I32, P,
+                                     ctypes.c_size_t, P, P]
         L.gdn_decode_graph_create.restype = I32
         L.gdn_decode_graph_create.argtypes = [P, P, P, I32, P, P, P, P, I32, P, I32, I32, P, P,
                                               I32, I32, gdn_dims, F, I32, P, P, I32, P,
@@ -248,6 +252,28 @@ def gdn_chunked_prefill_noalloc(mixed_qkv, a, b, A_log, dt_bias, conv_weight, co
         _ptr(has_initial_state), N, T, ssm_state.shape[0], _sdims(dims, ssm_state),
         float(scale), int(bool(qk_l2norm)), int(chunk), _gate(gate), _ptr(out), _dt(out),
         _ptr(err), _stream(stream)))
+
+
+def gdn_mixed_step(mixed_qkv, a, b, A_log, dt_bias, conv_weight, conv_bias, conv_state,
+                   ssm_state, slot, num_decode, cu_seqlens, has_initial_state, out, workspace,
+                   dims: Dims, *, chunk=64, silu=True, conv_layout=GDN_CONV_DIM_FIRST,
+                   scale=None, qk_l2norm=True, gate=None, err=None, stream=None):
+    """A step of num_decode decode rows followed by prefill sequences, packed in one token
+    array (include/gdn.h, gdn_mixed_step). slot: decode rows' slots then one per prefill
+    sequence; cu_seqlens: offsets within the prefill part; workspace: the prefill part's."""
+    nd = int(num_decode)
+    N = slot.shape[0] - nd
+    T = mixed_qkv.shape[0] - nd
+    scale = dims.dk ** -0.5 if scale is None else scale
+    conv_dt = _dt(conv_state) if conv_state is not None else GDN_BF16
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().gdn_mixed_step(
+        _ptr(mixed_qkv), _ptr(a), _ptr(b), _gate_mode(a), _ptr(A_log), _ptr(dt_bias),
+        _ptr(conv_weight), _ptr(conv_bias), int(bool(silu)), _ptr(conv_state), conv_dt,
+        int(conv_layout), _ptr(ssm_state), _ptr(slot), nd, _ptr(cu_seqlens),
+        _ptr(has_initial_state), N, T, ssm_state.shape[0], _sdims(dims, ssm_state),
+        float(scale), int(bool(qk_l2norm)), int(chunk), _gate(gate), _ptr(out), _dt(out),
+        _ptr(workspace), ws_bytes, _ptr(err), _stream(stream)))
 
 
 class DecodeGraph:

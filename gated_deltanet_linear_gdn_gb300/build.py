@@ -17,7 +17,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libgdn.so")
 SOURCES = ["gdn_api.cu", "gdn_conv.cu", "gdn_decode.cu", "gdn_prefill.cu", "gdn_prefill_tc.cu",
-           "gdn_graph.cu", "gdn_noalloc.cu", "gdn_gate.cu"]
+           "gdn_graph.cu", "gdn_noalloc.cu", "gdn_gate.cu", "gdn_mixed.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I" + INCLUDE]
 

@@ -72,6 +72,7 @@ gdn_status check_layer(const void* mixed, const void* a, const void* b, gdn_gate
   la.out = out;
   la.out_f32 = out_dtype == GDN_F32;
   la.err = err;
+  la.max_ctas = 0;
   return GDN_OK;
 }
 
@@ -99,6 +100,68 @@ gdn_status check_gate(const gdn_output_gate* g, gdn::LayerArgs& la) {
 }
 
 }  // namespace
+
+namespace gdn {
+
+gdn_status prepare_decode(const void* mixed_qkv, const void* a, const void* b,
+                          gdn_gate_mode gate_mode, const float* A_log, const float* dt_bias,
+                          const void* conv_weight, const void* conv_bias, int32_t silu,
+                          void* conv_state, gdn_dtype conv_dtype, gdn_conv_layout conv_layout,
+                          float* ssm_state, const int32_t* slot, int32_t batch, int32_t num_slots,
+                          gdn_dims dims, float scale, int32_t qk_l2norm,
+                          const gdn_output_gate* gate, void* out, gdn_dtype out_dtype,
+                          int32_t* err, LayerArgs& la) {
+  if (batch <= 0) return GDN_ERR_INVALID_ARG;
+  if (batch > 65535) return GDN_ERR_UNSUPPORTED;
+  gdn_status st = check_layer(mixed_qkv, a, b, gate_mode, A_log, dt_bias, conv_weight, conv_bias,
+                              silu, conv_state, conv_dtype, conv_layout, ssm_state, slot, num_slots,
+                              dims, scale, qk_l2norm, out, out_dtype, err, la);
+  if (st != GDN_OK) return st;
+  st = check_gate(gate, la);
+  if (st != GDN_OK) return st;
+  if (la.gated && !aligned(out, 16)) return GDN_ERR_INVALID_ARG;  // 16-byte gated stores
+  return GDN_OK;
+}
+
+gdn_status prepare_prefill(const void* mixed_qkv, const void* a, const void* b,
+                           gdn_gate_mode gate_mode, const float* A_log, const float* dt_bias,
+                           const void* conv_weight, const void* conv_bias, int32_t silu,
+                           void* conv_state, gdn_dtype conv_dtype, gdn_conv_layout conv_layout,
+                           float* ssm_state, const int32_t* cu_seqlens, const int32_t* slot,
+                           const uint8_t* has_initial_state, int32_t num_seqs,
+                           int32_t total_tokens, int32_t num_slots, gdn_dims dims, float scale,
+                           int32_t qk_l2norm, int32_t chunk, const gdn_output_gate* gate,
+                           void* out, gdn_dtype out_dtype, void* workspace,
+                           size_t workspace_bytes, int32_t* err, LayerArgs& la,
+                           PrefillExtra& p) {
+  if (num_seqs < 0 || total_tokens < 0) return GDN_ERR_INVALID_ARG;
+  if (chunk != 16 && chunk != 32 && chunk != 64) return GDN_ERR_UNSUPPORTED;
+  if (num_seqs == 0) return GDN_ERR_INVALID_ARG;  // (an empty call is the callers' no-op)
+  if (num_seqs > 65535) return GDN_ERR_UNSUPPORTED;
+  if (!cu_seqlens) return GDN_ERR_INVALID_ARG;
+  if (total_tokens == 0) {
+    // no token is read or written: empty per-token arrays may be null
+    const void* ph = ssm_state;
+    if (!mixed_qkv) mixed_qkv = ph;
+    if (!a) a = ph;
+    if (!b) b = ph;
+    if (!out) out = const_cast<void*>(ph);
+  }
+  gdn_status st = check_layer(mixed_qkv, a, b, gate_mode, A_log, dt_bias, conv_weight, conv_bias,
+                              silu, conv_state, conv_dtype, conv_layout, ssm_state, slot, num_slots,
+                              dims, scale, qk_l2norm, out, out_dtype, err, la);
+  if (st != GDN_OK) return st;
+  st = check_gate(gate, la);
+  if (st != GDN_OK) return st;
+  if (la.gated && total_tokens > 0 && !aligned(out, 16)) return GDN_ERR_INVALID_ARG;
+  const size_t need = gdn_chunked_prefill_workspace_size(total_tokens, num_seqs, dims, chunk);
+  if (!workspace || workspace_bytes < need || !aligned(workspace, 16)) return GDN_ERR_INVALID_ARG;
+  p = PrefillExtra{cu_seqlens, has_initial_state, num_seqs, total_tokens, chunk, workspace,
+                   workspace_bytes, nullptr};
+  return GDN_OK;
+}
+
+}  // namespace gdn
 
 extern "C" {
 
@@ -129,17 +192,13 @@ gdn_status gdn_decode_step(const void* mixed_qkv, const void* a, const void* b,
                            int32_t num_slots, gdn_dims dims, float scale, int32_t qk_l2norm,
                            const gdn_output_gate* gate, void* out, gdn_dtype out_dtype,
                            int32_t* err, void* stream) {
-  if (batch < 0) return GDN_ERR_INVALID_ARG;
   if (batch == 0) return GDN_OK;
-  if (batch > 65535) return GDN_ERR_UNSUPPORTED;
   gdn::LayerArgs la;
-  gdn_status st = check_layer(mixed_qkv, a, b, gate_mode, A_log, dt_bias, conv_weight, conv_bias,
-                              silu, conv_state, conv_dtype, conv_layout, ssm_state, slot, num_slots,
-                              dims, scale, qk_l2norm, out, out_dtype, err, la);
+  const gdn_status st = gdn::prepare_decode(
+      mixed_qkv, a, b, gate_mode, A_log, dt_bias, conv_weight, conv_bias, silu, conv_state,
+      conv_dtype, conv_layout, ssm_state, slot, batch, num_slots, dims, scale, qk_l2norm, gate,
+      out, out_dtype, err, la);
   if (st != GDN_OK) return st;
-  st = check_gate(gate, la);
-  if (st != GDN_OK) return st;
-  if (la.gated && !aligned(out, 16)) return GDN_ERR_INVALID_ARG;  // 16-byte gated stores
   return from_cuda(gdn::launch_decode(la, batch, static_cast<cudaStream_t>(stream)));
 }
 
@@ -165,31 +224,16 @@ gdn_status gdn_chunked_prefill(const void* mixed_qkv, const void* a, const void*
                                const gdn_output_gate* gate, void* out, gdn_dtype out_dtype,
                                void* workspace, size_t workspace_bytes, int32_t* err,
                                void* stream) {
-  if (num_seqs < 0 || total_tokens < 0) return GDN_ERR_INVALID_ARG;
-  if (chunk != 16 && chunk != 32 && chunk != 64) return GDN_ERR_UNSUPPORTED;
-  if (num_seqs == 0) return total_tokens == 0 ? GDN_OK : GDN_ERR_INVALID_ARG;
-  if (num_seqs > 65535) return GDN_ERR_UNSUPPORTED;
-  if (!cu_seqlens) return GDN_ERR_INVALID_ARG;
+  if (num_seqs == 0 && total_tokens == 0 && (chunk == 16 || chunk == 32 || chunk == 64))
+    return GDN_OK;
   gdn::LayerArgs la;
-  if (total_tokens == 0) {
-    // no token is read or written: empty per-token arrays may be null
-    const void* ph = ssm_state;
-    if (!mixed_qkv) mixed_qkv = ph;
-    if (!a) a = ph;
-    if (!b) b = ph;
-    if (!out) out = const_cast<void*>(ph);
-  }
-  gdn_status st = check_layer(mixed_qkv, a, b, gate_mode, A_log, dt_bias, conv_weight, conv_bias,
-                              silu, conv_state, conv_dtype, conv_layout, ssm_state, slot, num_slots,
-                              dims, scale, qk_l2norm, out, out_dtype, err, la);
+  gdn::PrefillExtra p;
+  const gdn_status st = gdn::prepare_prefill(
+      mixed_qkv, a, b, gate_mode, A_log, dt_bias, conv_weight, conv_bias, silu, conv_state,
+      conv_dtype, conv_layout, ssm_state, cu_seqlens, slot, has_initial_state, num_seqs,
+      total_tokens, num_slots, dims, scale, qk_l2norm, chunk, gate, out, out_dtype, workspace,
+      workspace_bytes, err, la, p);
   if (st != GDN_OK) return st;
-  st = check_gate(gate, la);
-  if (st != GDN_OK) return st;
-  if (la.gated && !aligned(out, 16)) return GDN_ERR_INVALID_ARG;  // vector row access
-  const size_t need = gdn_chunked_prefill_workspace_size(total_tokens, num_seqs, dims, chunk);
-  if (!workspace || workspace_bytes < need || !aligned(workspace, 16)) return GDN_ERR_INVALID_ARG;
-  gdn::PrefillExtra p{cu_seqlens, has_initial_state, num_seqs, total_tokens, chunk, workspace,
-                      workspace_bytes};
   return from_cuda(gdn::launch_prefill(la, p, static_cast<cudaStream_t>(stream)));
 }
 

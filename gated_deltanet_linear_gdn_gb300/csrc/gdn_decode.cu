@@ -716,18 +716,6 @@ __global__ void __launch_bounds__(DecodeCfg<DK, R, kBf16State>::kThreads, 1)
   }
 }
 
-int sm_count() {
-  static int count[64] = {0};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
-  if (count[dev] == 0) {
-    int c = 0;
-    if (cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || c <= 0)
-      c = 148;
-    count[dev] = c;
-  }
-  return count[dev];
-}
 
 template <int DK, int R, bool kF32Cache, bool kBf16State>
 cudaError_t launch_one(const LayerArgs& a, int B, cudaStream_t s) {
@@ -737,7 +725,8 @@ cudaError_t launch_one(const LayerArgs& a, int B, cudaStream_t s) {
                                        Cfg::kSmemBytes);
   if (e != cudaSuccess) return e;
   const int units = B * a.Hk;
-  const int grid = units < sm_count() ? units : sm_count();
+  int grid = units < sm_count() ? units : sm_count();
+  if (a.max_ctas > 0 && grid > a.max_ctas) grid = a.max_ctas;
   kern<<<grid, Cfg::kThreads, Cfg::kSmemBytes, s>>>(a, units);
   return cudaGetLastError();
 }
@@ -763,6 +752,19 @@ cudaError_t launch_dk(const LayerArgs& a, int B, cudaStream_t s) {
 }
 
 }  // namespace
+
+int sm_count() {
+  static int count[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (count[dev] == 0) {
+    int c = 0;
+    if (cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || c <= 0)
+      c = 148;
+    count[dev] = c;
+  }
+  return count[dev];
+}
 
 cudaError_t launch_decode(const LayerArgs& a, int B, cudaStream_t s) {
   switch (a.dk) {

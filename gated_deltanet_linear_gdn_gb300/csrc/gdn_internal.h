@@ -56,6 +56,7 @@ struct LayerArgs {
   float gate_offset;
   float gate_eps;
   int gate_act;        // gdn_gate_act
+  int max_ctas;        // decode: cap on the persistent grid (0 = one CTA per SM)
 };
 
 struct PrefillExtra {
@@ -66,9 +67,32 @@ struct PrefillExtra {
   int chunk;
   void* workspace;
   size_t workspace_bytes;
+  cudaEvent_t before_pass;  // recorded on the stream just before the state pass (nullable)
 };
 
 cudaError_t launch_conv_update(const ConvUpdateArgs& a, cudaStream_t s);
+
+// Argument checks of the decode and prefill calls (gdn_api.cu), without launching:
+// on GDN_OK `la` (and `p`) describe the call.
+gdn_status prepare_decode(const void* mixed_qkv, const void* a, const void* b,
+                          gdn_gate_mode gate_mode, const float* A_log, const float* dt_bias,
+                          const void* conv_weight, const void* conv_bias, int32_t silu,
+                          void* conv_state, gdn_dtype conv_dtype, gdn_conv_layout conv_layout,
+                          float* ssm_state, const int32_t* slot, int32_t batch, int32_t num_slots,
+                          gdn_dims dims, float scale, int32_t qk_l2norm,
+                          const gdn_output_gate* gate, void* out, gdn_dtype out_dtype,
+                          int32_t* err, LayerArgs& la);
+gdn_status prepare_prefill(const void* mixed_qkv, const void* a, const void* b,
+                           gdn_gate_mode gate_mode, const float* A_log, const float* dt_bias,
+                           const void* conv_weight, const void* conv_bias, int32_t silu,
+                           void* conv_state, gdn_dtype conv_dtype, gdn_conv_layout conv_layout,
+                           float* ssm_state, const int32_t* cu_seqlens, const int32_t* slot,
+                           const uint8_t* has_initial_state, int32_t num_seqs,
+                           int32_t total_tokens, int32_t num_slots, gdn_dims dims, float scale,
+                           int32_t qk_l2norm, int32_t chunk, const gdn_output_gate* gate,
+                           void* out, gdn_dtype out_dtype, void* workspace,
+                           size_t workspace_bytes, int32_t* err, LayerArgs& la, PrefillExtra& p);
+int sm_count();  // SMs of the current device (gdn_decode.cu)
 cudaError_t launch_decode(const LayerArgs& a, int B, cudaStream_t s);
 // the output gate in place over `rows` rows of dv values of a.out (gdn_gate.cu)
 cudaError_t launch_output_gate(const LayerArgs& a, int64_t rows, cudaStream_t s);

@@ -452,6 +452,7 @@ cudaError_t launch_prefill_dk(const LayerArgs& a, const PrefillExtra& p, cudaStr
   constexpr int DVS = DK / kDvSplitMax < 32 ? 32 : DK / kDvSplitMax;
   const size_t sm2 = pass_smem<DK, DVS>();
   cudaFuncSetAttribute(pass_kernel<DK, DVS>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(sm2));
+  if (p.before_pass && (e = cudaEventRecord(p.before_pass, s)) != cudaSuccess) return e;
   if (p.num_seqs > 0)
     pass_kernel<DK, DVS><<<dim3(p.num_seqs, a.Hv, DK / DVS), kPreThreads, sm2, s>>>(
         a, p, y, seq_ok, chunk_off, Wb, Ub, Pb, Gb);

@@ -823,6 +823,7 @@ cudaError_t launch_tc_c(const LayerArgs& a, const PrefillExtra& p, const TcLayou
   auto k2 = pass_tc_kernel<C>;
   e = cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, PassSmem<C>::kBytes);
   if (e != cudaSuccess) return e;
+  if (p.before_pass && (e = cudaEventRecord(p.before_pass, s)) != cudaSuccess) return e;
   k2<<<dim3(p.num_seqs, a.Hv), kThreadsTc, PassSmem<C>::kBytes, s>>>(a, p, seq_ok, chunk_off, wb);
   return cudaGetLastError();
 }

@@ -279,6 +279,45 @@ gdn_status gdn_chunked_prefill_noalloc(const void* mixed_qkv, const void* a, con
                                        gdn_dtype out_dtype, int32_t* err, void* stream);
 
 /*
+ * gdn_mixed_step -- one step that holds decode rows and prefill sequences
+ * together, packed decode rows first (RL-Kernel PR #469 page, "Not
+ * reproducible from this branch: the mixed decode+prefill measurement": a
+ * provider that sends mixed-step decodes through another kernel makes their
+ * results depend on the step's composition). Here the decode rows run the
+ * fused decode kernel and the prefill sequences the chunked path, exactly as
+ * gdn_decode_step and gdn_chunked_prefill would: every output, recurrent state
+ * and conv state is bitwise the separate calls', whatever the mix.
+ *
+ * Packing: token rows [0, num_decode) are decode rows (one token each), rows
+ * [num_decode, num_decode + prefill_tokens) the prefill sequences, for
+ * mixed_qkv, a, b, out and the gate's z alike. slot holds num_decode +
+ * num_prefill_seqs entries, decode rows first; cu_seqlens [num_prefill_seqs+1]
+ * counts tokens from the start of the prefill part (0 ... prefill_tokens);
+ * has_initial_state covers the prefill sequences. All active slots of the step
+ * must be distinct. workspace is the prefill part's
+ * (gdn_chunked_prefill_workspace_size(prefill_tokens, num_prefill_seqs, ...)).
+ * Either part may be empty. Argument checks and result codes are those of the
+ * two separate calls.
+ *
+ * Scheduling: the decode rows run on a library-owned side stream that waits
+ * for the prefill's state pass to start, on the SMs the pass leaves free; the
+ * caller's stream then waits for the side stream, so the call is ordered on
+ * `stream` like any other. The side stream and its events are created on the
+ * first call per device that holds both parts: make it before any stream
+ * capture. Mixed calls on one device enqueue one at a time.
+ */
+gdn_status gdn_mixed_step(const void* mixed_qkv, const void* a, const void* b,
+                          gdn_gate_mode gate_mode, const float* A_log, const float* dt_bias,
+                          const void* conv_weight, const void* conv_bias, int32_t silu,
+                          void* conv_state, gdn_dtype conv_dtype, gdn_conv_layout conv_layout,
+                          float* ssm_state, const int32_t* slot, int32_t num_decode,
+                          const int32_t* cu_seqlens, const uint8_t* has_initial_state,
+                          int32_t num_prefill_seqs, int32_t prefill_tokens, int32_t num_slots,
+                          gdn_dims dims, float scale, int32_t qk_l2norm, int32_t chunk,
+                          const gdn_output_gate* gate, void* out, gdn_dtype out_dtype,
+                          void* workspace, size_t workspace_bytes, int32_t* err, void* stream);
+
+/*
  * CUDA-graph decode buckets ([P2] Rocket, "A reduction barrier makes Qwen GDN
  * graph replay bit exact": immutable graphs per decode bucket c1, c2, ...,
  * inactive rows cleared on bucket transitions, slot 0 untouched).
