@@ -492,7 +492,9 @@ struct PassSmem {
   static constexpr int oWh = oEl + kD_, oWl = oWh + kW, oQ = oWl + kW;
   static constexpr int oPh = oQ + kW, oPl = oPh + kP, oKt = oPl + kP;
   static constexpr int oVec = oKt + kD_;        // two vec buffers of kVecFloats
-  static constexpr int kBytes = oVec + 2 * kVecFloats * 4;
+  static constexpr int oO = oVec + 2 * kVecFloats * 4;  // bf16 output tile [C x 128]
+  static constexpr int kBytes = oO + C * 128 * 2;
+  static_assert(kBytes <= 227 * 1024, "pass shared memory exceeds the per-CTA limit");
 };
 
 template <int C>
@@ -526,18 +528,24 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   const uint32_t mma1 = smem_addr(&s_bar[2]), mma2 = smem_addr(&s_bar[3]);
   const size_t wtile = wb.w_tile, ptile = wb.p_tile;
 
-  auto issue_A = [&](int it) {  // W hi/lo, q tile, vec of chunk c0 + it
+  // W hi/lo, q tile, vec of chunk c0 + it, all on one fullA phase (armed with the total):
+  // W and vec as soon as group 1's W products are done, q once its Q products are
+  auto issue_A_w = [&](int it) {
     const int c = c0 + it;
-    const int kh = h / (a.Hv / a.Hk);
     const unsigned char* w = wb.Wt + (static_cast<size_t>(c) * a.Hv + h) * 2 * wtile;
-    const unsigned char* qt = wb.Qt + (static_cast<size_t>(c) * a.Hk + kh) * wb.q_tile;
     const float* vec = wb.vec + (static_cast<size_t>(c) * a.Hv + h) * kVecFloats;
     mbar_arrive_expect_tx(fullA, static_cast<uint32_t>(2 * wtile + wb.q_tile + kVecFloats * 4));
     bulk_g2s(smem_addr(sm + S::oWh), w, static_cast<uint32_t>(wtile), fullA);
     bulk_g2s(smem_addr(sm + S::oWl), w + wtile, static_cast<uint32_t>(wtile), fullA);
-    bulk_g2s(smem_addr(sm + S::oQ), qt, static_cast<uint32_t>(wb.q_tile), fullA);
     bulk_g2s(smem_addr(sm + S::oVec + (it & 1) * kVecFloats * 4), vec, kVecFloats * 4, fullA);
   };
+  auto issue_A_q = [&](int it) {
+    const int c = c0 + it;
+    const int kh = h / (a.Hv / a.Hk);
+    const unsigned char* qt = wb.Qt + (static_cast<size_t>(c) * a.Hk + kh) * wb.q_tile;
+    bulk_g2s(smem_addr(sm + S::oQ), qt, static_cast<uint32_t>(wb.q_tile), fullA);
+  };
+  auto issue_A = [&](int it) { issue_A_w(it); issue_A_q(it); };
   auto issue_B = [&](int it) {  // P hi/lo, k^T tile of chunk c0 + it
     const int c = c0 + it;
     const int kh = h / (a.Hv / a.Hk);
@@ -610,7 +618,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   const uint64_t dKt = tc::kmajor_desc(smem_addr(sm + S::oKt), C, 0);
   const uint32_t idC = tc::idesc_bf16_f32(128, C), id128 = tc::idesc_bf16_f32(128, 128);
 
-  // MMA group 1 of chunk `it` (thread 0): D^T raw = S W^T, O1^T = S Q^T
+  // MMA group 1 of chunk `it` (thread 0): D^T raw = S W^T, committed on its own --
+  // the chain needs only D -- then O1^T = S Q^T, which completes under group 2's commit
   auto issue_mma1 = [&](int it) -> bool {
     if (!mbar_wait_bounded(fullA, it & 1)) return false;
 #pragma unroll
@@ -619,11 +628,11 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     for (int ks = 0; ks < 8; ++ks) tc::mma_bf16(tb, dSh + 16 * ks, dWl + 16 * ks, idC, 1);
 #pragma unroll
     for (int ks = 0; ks < 8; ++ks) tc::mma_bf16(tb, dSl + 16 * ks, dWh + 16 * ks, idC, 1);
+    tc::mma_commit(mma1);
 #pragma unroll
     for (int ks = 0; ks < 8; ++ks) tc::mma_bf16(tb + 64, dSh + 16 * ks, dQ + 16 * ks, idC, ks > 0);
 #pragma unroll
     for (int ks = 0; ks < 8; ++ks) tc::mma_bf16(tb + 64, dSl + 16 * ks, dQ + 16 * ks, idC, 1);
-    tc::mma_commit(mma1);
     return true;
   };
   // a thread 0 failure leaves an MMA group unissued; the other threads' bounded waits
@@ -644,23 +653,27 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   };
   if (tid == 32 && nch > 1) prefetch_chunk(1);
 
-  for (int it = 0; it < nch && !bad; ++it) {
-    const int t0 = bos + it * C;
-    const int L = min(C, eos - t0);
-    const uint32_t par = it & 1;
-    if (tid == 32 && it + 2 < nch) prefetch_chunk(it + 2);  // two chunks ahead
-    // U^T values this thread needs (row r, tokens half*NH ..), loaded while MMA group 1 runs
+  // U^T values this thread needs (row r, tokens half*NH ..) of chunk `it`, loaded while
+  // MMA group 1 runs
+  float Ur[NH];
+  auto load_U = [&](int it) {
     const float* ut = wb.Ut + (static_cast<size_t>(c0 + it) * a.Hv + h) * (kD * C) + r * C + half * NH;
-    float Ur[NH];
 #pragma unroll
     for (int e = 0; e < NH; e += 4) {
       const float4 v = *reinterpret_cast<const float4*>(ut + e);
       Ur[e] = v.x; Ur[e + 1] = v.y; Ur[e + 2] = v.z; Ur[e + 3] = v.w;
     }
+  };
+  for (int it = 0; it < nch && !bad; ++it) {
+    const int t0 = bos + it * C;
+    const int L = min(C, eos - t0);
+    const uint32_t par = it & 1;
+    if (tid == 32 && it + 2 < nch) prefetch_chunk(it + 2);  // two chunks ahead
+    load_U(it);
     if (!mbar_wait_bounded(mma1, par)) bad = true;
     bad = __any_sync(0xffffffffu, bad);  // warp-uniform before the aligned loads
     tc::fence_after_sync();
-    if (tid == 0 && !bad && it + 1 < nch) issue_A(it + 1);  // W, Q buffers are free again
+    if (tid == 0 && !bad && it + 1 < nch) issue_A_w(it + 1);  // the W buffers are free again
     const float* vec = reinterpret_cast<const float*>(sm + S::oVec + par * kVecFloats * 4);
     if (!bad) {
       // D = U - raw, D' = D dd_t; both split into the [128 x C] operand tiles
@@ -721,7 +734,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     if (!mbar_wait_bounded(mma2, par)) bad = true;
     bad = __any_sync(0xffffffffu, bad);  // warp-uniform before the aligned loads
     tc::fence_after_sync();
-    if (tid == 0 && !bad && it + 1 < nch) issue_B(it + 1);  // P, k^T buffers are free again
+    if (tid == 0 && !bad && it + 1 < nch) {
+      issue_B(it + 1);    // P, k^T buffers are free again
+      issue_A_q(it + 1);  // and the q buffer (group 2's commit covers group 1's Q products)
+    }
     float Ov[NH];
     if (!bad) {
       // O = f_t O1 + O2 into registers (stored below, while the next chunk's MMAs run)
@@ -745,28 +761,45 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       tc::tmem_wait_ld();
 #pragma unroll
       for (int e = 0; e < NH; ++e) Ov[e] = fmaf(vec[half * NH + e], o1[e], o2[e]);
+      if (!a.out_f32) {  // bf16 output: stage the tile [token][dv] for 16-byte stores below
+        uint16_t* ot = reinterpret_cast<uint16_t*>(sm + S::oO);
+#pragma unroll
+        for (int e = 0; e < NH; ++e) ot[(half * NH + e) * kD + r] = f2bf(Ov[e]);
+      }
       // S <- g_last S + update, 16 columns at a time
       const float gl = vec[128];
 #pragma unroll
-      for (int b0 = 0; b0 < 64; b0 += 16) {
-        float tv[16];
-        tmem_load<16>(tc::taddr(tb, 32 * q, 256 + half * 64 + b0), tv);
+      for (int b0 = 0; b0 < 64; b0 += 32) {  // two loads in flight per wait
+        float tv0[16], tv1[16];
+        tmem_load<16>(tc::taddr(tb, 32 * q, 256 + half * 64 + b0), tv0);
+        tmem_load<16>(tc::taddr(tb, 32 * q, 256 + half * 64 + b0 + 16), tv1);
         tc::tmem_wait_ld();
 #pragma unroll
-        for (int e = 0; e < 16; ++e) Sr[b0 + e] = fmaf(gl, Sr[b0 + e], tv[e]);
+        for (int e = 0; e < 16; ++e) {
+          Sr[b0 + e] = fmaf(gl, Sr[b0 + e], tv0[e]);
+          Sr[b0 + 16 + e] = fmaf(gl, Sr[b0 + 16 + e], tv1[e]);
+        }
       }
       store_S_tiles();
     }
     bad = tc_sync(bad);
     if (bad) break;
     if (tid == 0 && it + 1 < nch && !issue_mma1(it + 1)) bad = true;
+    if (a.out_f32) {
 #pragma unroll
-    for (int e = 0; e < NH; ++e) {
-      const int tt = half * NH + e;
-      if (tt < L) {
-        const int64_t oi = (static_cast<int64_t>(t0 + tt) * a.Hv + h) * kD + r;
-        if (a.out_f32) static_cast<float*>(a.out)[oi] = Ov[e];
-        else static_cast<uint16_t*>(a.out)[oi] = f2bf(Ov[e]);
+      for (int e = 0; e < NH; ++e) {
+        const int tt = half * NH + e;
+        if (tt < L)
+          static_cast<float*>(a.out)[(static_cast<int64_t>(t0 + tt) * a.Hv + h) * kD + r] = Ov[e];
+      }
+    } else if (warp > 0) {
+      // warps 1-7 copy the staged tile out in 16-byte pieces while thread 0 issues the
+      // next chunk's MMAs (the tile is rewritten only after the next chunk's barrier)
+      const uint4* ot = reinterpret_cast<const uint4*>(sm + S::oO);
+      for (int k = tid - 32; k < L * (kD / 8); k += kThreadsTc - 32) {
+        const int tt = k / (kD / 8), col = (k % (kD / 8)) * 8;
+        *reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.out) +
+                                  (static_cast<int64_t>(t0 + tt) * a.Hv + h) * kD + col) = ot[k];
       }
     }
   }
