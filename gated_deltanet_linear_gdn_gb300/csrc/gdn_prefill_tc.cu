@@ -653,8 +653,9 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   };
   if (tid == 32 && nch > 1) prefetch_chunk(1);
 
-  // U^T values this thread needs (row r, tokens half*NH ..) of chunk `it`, loaded while
-  // MMA group 1 runs
+  // U^T values this thread needs (row r, tokens half*NH ..) of chunk `it`: loaded at the
+  // chunk's start while MMA group 1 runs, except by warp 0, whose thread 0 spends that time
+  // issuing the MMAs -- warp 0 loads them a chunk ahead
   float Ur[NH];
   auto load_U = [&](int it) {
     const float* ut = wb.Ut + (static_cast<size_t>(c0 + it) * a.Hv + h) * (kD * C) + r * C + half * NH;
@@ -664,12 +665,13 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       Ur[e] = v.x; Ur[e + 1] = v.y; Ur[e + 2] = v.z; Ur[e + 3] = v.w;
     }
   };
+  if (warp == 0 && nch > 0) load_U(0);
   for (int it = 0; it < nch && !bad; ++it) {
     const int t0 = bos + it * C;
     const int L = min(C, eos - t0);
     const uint32_t par = it & 1;
     if (tid == 32 && it + 2 < nch) prefetch_chunk(it + 2);  // two chunks ahead
-    load_U(it);
+    if (warp != 0) load_U(it);
     if (!mbar_wait_bounded(mma1, par)) bad = true;
     bad = __any_sync(0xffffffffu, bad);  // warp-uniform before the aligned loads
     tc::fence_after_sync();
@@ -784,6 +786,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     }
     bad = tc_sync(bad);
     if (bad) break;
+    if (warp == 0 && it + 1 < nch) load_U(it + 1);
     if (tid == 0 && it + 1 < nch && !issue_mma1(it + 1)) bad = true;
     if (a.out_f32) {
 #pragma unroll
