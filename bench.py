@@ -358,23 +358,78 @@ def run_ours(args, rank, world):
         torch.cuda.empty_cache()
 
     # ---- e2e through the public API with pinned host buffers ----
+    # A step's inputs (x, a, b, slot table) are staged in one pinned host buffer and copied
+    # with one H2D copy into one device buffer whose sections the call reads as tensors;
+    # the output comes back with one D2H copy.
     t = decode_setup(args.batch, args.num_slots, seed=args.batch, state_bf16=args.state_bf16)
-    h_mixed = t["mixed"].cpu().pin_memory()
-    h_a, h_b = t["a"].cpu().pin_memory(), t["b"].cpu().pin_memory()
-    h_slot = t["slot"].cpu().pin_memory()
+    parts = [("mixed", t["mixed"]), ("a", t["a"]), ("b", t["b"]), ("slot", t["slot"])]
+    offs, total = [], 0
+    for _, x in parts:
+        offs.append(total)
+        total += (x.numel() * x.element_size() + 255) // 256 * 256
+    h_buf = torch.empty(total, dtype=torch.uint8).pin_memory()
+    d_buf = torch.empty(total, dtype=torch.uint8, device=dev)
+    for (name, x), o in zip(parts, offs):
+        nb_ = x.numel() * x.element_size()
+        h_buf[o:o + nb_].copy_(x.cpu().contiguous().view(-1).view(torch.uint8))
+        t[name] = d_buf[o:o + nb_].view(x.dtype).view(x.shape)  # the call reads these views
     h_out = torch.empty_like(t["out"], device="cpu").pin_memory()
 
     def e2e_call():
-        t["mixed"].copy_(h_mixed, non_blocking=True)
-        t["a"].copy_(h_a, non_blocking=True)
-        t["b"].copy_(h_b, non_blocking=True)
-        t["slot"].copy_(h_slot, non_blocking=True)
+        d_buf.copy_(h_buf, non_blocking=True)
         decode_call(t)
         h_out.copy_(t["out"], non_blocking=True)
 
-    e2e_ms = float(np.mean(timed(e2e_call, max(5, args.steps // 2), 3)))
-    h2d = sum(x.numel() * x.element_size() for x in (h_mixed, h_a, h_b, h_slot))
+    e2e_serial_ms = float(np.mean(timed(e2e_call, max(5, args.steps // 2), 3)))
+    h2d = total  # the bytes the one H2D copy moves (the sections plus their alignment padding)
     d2h = h_out.numel() * h_out.element_size()
+
+    # Pipelined like a serving loop: step n's inputs are copied in (own stream) while step
+    # n-1 computes, and step n's output is copied out (own stream) while step n+1 computes;
+    # inputs and outputs are double-buffered. Every step's H2D and D2H copies lie inside the
+    # one timed region (start to the last D2H); the state pool (> L2) is not flushed.
+    h2d_s, d2h_s = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    d_in = [d_buf, torch.empty_like(d_buf)]
+    views = []
+    for db in d_in:
+        v = dict(t)
+        for (name, x), o in zip(parts, offs):
+            nb_ = x.numel() * x.element_size()
+            v[name] = db[o:o + nb_].view(x.dtype).view(x.shape)
+        v["out"] = torch.empty_like(t["out"])
+        views.append(v)
+    h_outs = [h_out, torch.empty_like(h_out).pin_memory()]
+    ev = lambda: torch.cuda.Event()
+    in_ready, k_done, out_free = [ev(), ev()], [ev(), ev()], [ev(), ev()]
+
+    def pipelined(steps):
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        h2d_s.wait_event(start)
+        d2h_s.wait_event(start)
+        for n in range(steps):
+            j = n & 1
+            with torch.cuda.stream(h2d_s):
+                if n >= 2:
+                    h2d_s.wait_event(k_done[j])   # step n-2 no longer reads this input buffer
+                d_in[j].copy_(h_buf, non_blocking=True)
+                in_ready[j].record(h2d_s)
+            stream.wait_event(in_ready[j])
+            if n >= 2:
+                stream.wait_event(out_free[j])    # step n-2's output has been copied out
+            decode_call(views[j])
+            k_done[j].record(stream)
+            with torch.cuda.stream(d2h_s):
+                d2h_s.wait_event(k_done[j])
+                h_outs[j].copy_(views[j]["out"], non_blocking=True)
+                out_free[j].record(d2h_s)
+        stream.wait_stream(d2h_s)
+        end.record(stream)
+        torch.cuda.synchronize()
+        return start.elapsed_time(end) / steps
+
+    pipelined(3)
+    e2e_ms = pipelined(max(10, args.steps))
 
     # ---- headline: exactly K timed decode steps ----
     nbytes = decode_bytes(args.batch, geo, state_bytes=2 if args.state_bf16 else 4)
@@ -413,7 +468,11 @@ def run_ours(args, rank, world):
                      "traffic_note": None if traffic is None else traffic.get("note")},
         "e2e": {"value": round(nbytes * world / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": round(e2e_ms, 5)},
+                "ms_per_step": round(e2e_ms, 5),
+                "mode": "pipelined: step n+1's H2D and step n-1's D2H overlap step n's kernel",
+                "serial": {"value": round(nbytes * world / (e2e_serial_ms * 1e-3) / 1e9, 1),
+                           "ms_per_step": round(e2e_serial_ms, 5),
+                           "mode": "H2D, kernel, D2H in sequence per step, L2 flushed between"}},
         "gpu_launches": args.steps,
         "clocks": clk,
         "decode_sweep": sweep,
