@@ -86,3 +86,21 @@ def test_bf16_state_drift_fixture():
     assert drift[0] > 0
     assert drift.max() < 0.05
     assert drift[steps // 2:].max() <= 2 * drift[:steps // 2].max() + 1e-3
+
+
+def test_graph_replay_on_a_bf16_state_pool_equals_the_direct_call():
+    """A captured decode step over a bf16 pool (gdn_decode_graph_create) replays bitwise like
+    the direct call, state included."""
+    import gated_deltanet_linear_gdn_gb300 as gdn
+    from _harness import dims_of
+    inp = gi.make_inputs(gi.QWEN3_NEXT, [1] * 8, 64, seed=41, state_bf16=True)
+    dd, dg = Device(inp), Device(inp)
+    want = gpu_decode(dd, out_f32=False)
+    out = torch.empty_like(want)
+    g = gdn.DecodeGraph(dg.mixed, dg.a, dg.b, dg.A_log, dg.dt_bias, dg.conv_w, dg.conv_b,
+                        dg.conv_state, dg.ssm, dg.slot, out, dims_of(inp.geo), err=dg.err)
+    g.launch()
+    torch.cuda.synchronize()
+    g.close()
+    assert torch.equal(out, want)
+    assert torch.equal(dg.ssm, dd.ssm) and torch.equal(dg.conv_state, dd.conv_state)

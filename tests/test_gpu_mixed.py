@@ -78,18 +78,21 @@ def run_separate(inp, nd, chunk, out_f32=True, gate=None):
 
 
 COMPOSITIONS = [
-    ("decode-only", gi.QWEN3_NEXT, 8, [], 64),
-    ("prefill-only", gi.QWEN3_NEXT, 0, [90, 200], 64),
-    ("one-decode-one-prefill", gi.QWEN3_NEXT, 1, [300], 64),
-    ("b64-three-prefills", gi.QWEN3_NEXT, 64, [130, 1, 77], 64),
-    ("tiny-cuda-core-prefill", gi.TINY, 5, [40, 17], 16),
+    ("decode-only", gi.QWEN3_NEXT, 8, [], 64, False),
+    ("prefill-only", gi.QWEN3_NEXT, 0, [90, 200], 64, False),
+    ("one-decode-one-prefill", gi.QWEN3_NEXT, 1, [300], 64, False),
+    ("b64-three-prefills", gi.QWEN3_NEXT, 64, [130, 1, 77], 64, False),
+    ("tiny-cuda-core-prefill", gi.TINY, 5, [40, 17], 16, False),
+    ("b16-two-prefills-bf16-state", gi.QWEN3_NEXT, 16, [70, 129], 64, True),
 ]
 
 
-@pytest.mark.parametrize("name,geo,nd,lengths,chunk", COMPOSITIONS, ids=[c[0] for c in COMPOSITIONS])
-def test_mixed_step_equals_separate_calls_bitwise(name, geo, nd, lengths, chunk):
+@pytest.mark.parametrize("name,geo,nd,lengths,chunk,sbf16", COMPOSITIONS,
+                         ids=[c[0] for c in COMPOSITIONS])
+def test_mixed_step_equals_separate_calls_bitwise(name, geo, nd, lengths, chunk, sbf16):
     inp = gi.make_inputs(geo, [1] * nd + lengths, 512 if geo is gi.QWEN3_NEXT else 32,
-                         seed=700 + nd + len(lengths), has_init=[1] * nd + [1, 0, 1][:len(lengths)] if lengths else True)
+                         seed=700 + nd + len(lengths), state_bf16=sbf16,
+                         has_init=[1] * nd + [1, 0, 1][:len(lengths)] if lengths else True)
     dm, om = run_mixed(inp, nd, chunk)
     ds, os_ = run_separate(inp, nd, chunk)
     torch.cuda.synchronize()
