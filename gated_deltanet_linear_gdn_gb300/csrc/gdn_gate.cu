@@ -1,7 +1,8 @@
 // gdn_gate.cu -- the GDN block's output gate over stored rows: a gated RMSNorm
-// of each (token, value head) vector of `out`, in place (RL-Kernel PRs
-// #466-#468, "Gated RMSNorm CUDA kernel for the GDN block": SiLU or sigmoid
-// gating and a weight offset). The chunked prefill runs it after its state
+// of each (token, value head) vector of `out`, in place (RL-Kernel PR #469
+// "C6: GDN decode-step goldens and recurrent/conv state contract", Summary by
+// CodeRabbit and Walkthrough, on the stacked gated-RMSNorm PRs #466-#468: SiLU
+// or sigmoid gating and a weight offset). The chunked prefill runs it after its state
 // pass; the decode step fuses the same arithmetic into its own epilogue warp.
 //
 // Per row (dv values o, the matching z):

@@ -89,9 +89,9 @@ typedef struct {
 
 /*
  * Output gate of the GDN block: a gated RMSNorm of the core output o over each
- * value head, before the output projection (RL-Kernel PRs #466-#468, "Gated
- * RMSNorm CUDA kernel for the GDN block": Summary by CodeRabbit -- SiLU or
- * sigmoid gating -- and Walkthrough -- a weight offset). Per token t and value
+ * value head, before the output projection ([P1] Summary by CodeRabbit -- SiLU
+ * or sigmoid gating -- and Walkthrough -- a weight offset -- on the stacked
+ * gated-RMSNorm PRs #466-#468). Per token t and value
  * head h, with o the core output:
  *   out[t, h, i] = o[i] / sqrt(mean_j o[j]^2 + eps) * (weight[i] + weight_offset)
  *                  * act(z[t, h, i]),   act = SiLU (z * sigmoid(z)) or sigmoid,

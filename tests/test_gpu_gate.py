@@ -1,5 +1,6 @@
-"""Output gate of the GDN block fused into the decode step (gated RMSNorm with z; RL-Kernel PRs
-#466-#468, "Gated RMSNorm CUDA kernel for the GDN block": SiLU or sigmoid gating and a weight
+"""Output gate of the GDN block fused into the decode step (gated RMSNorm with z; RL-Kernel PR
+#469 "C6: GDN decode-step goldens and recurrent/conv state contract", Summary by CodeRabbit and
+Walkthrough on the stacked gated-RMSNorm PRs #466-#468: SiLU or sigmoid gating and a weight
 offset). The gated call must leave every state exactly as the ungated call does, and its output
 must be the gate applied to the same fp32 core output.
 

@@ -619,8 +619,8 @@ def _gate_case(seed, shape=(3, 4, 128)):
 @pytest.mark.parametrize("act", ["silu", "sigmoid"])
 @pytest.mark.parametrize("offset", [0.0, 1.0])
 def test_gated_rmsnorm_matches_torch_rms_norm_times_gate(oracle, act, offset):
-    """RL-Kernel PRs #466-#468 (gated RMSNorm, SiLU or sigmoid gating, weight offset): the
-    oracle equals torch's own fp64 rms_norm with weight w + offset, times act(z)."""
+    """RL-Kernel PR #469, Summary by CodeRabbit and Walkthrough (gated RMSNorm with SiLU or
+    sigmoid gating and a weight offset): the oracle equals torch's own fp64 rms_norm with weight w + offset, times act(z)."""
     import torch
     o, z, w = _gate_case(1)
     y = oracle.gated_rmsnorm(o, z, w, offset=offset, eps=1e-6, act=act)
