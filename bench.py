@@ -316,6 +316,20 @@ def run_ours(args, rank, world):
                              "frac_of_bf16_tensor_peak": round(fl / ms / 1e9 / tpk, 4),
                              "peak_kind": tkind, "gpu_launches_per_call": 3 if inp.conv_w is None else 5,
                              "GBps": round(prefill_bytes(T, N, geo, conv=inp.conv_w is not None) / ms / 1e6, 1)}
+            if name.startswith("single"):  # the same call with the output gate (+1 launch)
+                og = gdn.OutputGate(torch.randn(T, geo.Hv, geo.dv, device=dev).to(torch.bfloat16),
+                                    torch.ones(geo.dv, device=dev))
+
+                def pcall_g(tt=tt, ws=ws, og=og):
+                    gdn.gdn_chunked_prefill(tt["mixed"], tt["a"], tt["b"], tt["A_log"],
+                                            tt["dt_bias"], tt["conv_w"], tt["conv_b"], tt["conv"],
+                                            tt["ssm"], tt["cu"], tt["slot"], tt["hi"], tt["out"],
+                                            ws, dims, chunk=64, gate=og, stream=stream)
+                msg = float(np.median(timed(pcall_g, 5, 2)))
+                prefill[name + "_gated"] = {"tokens": T, "ms": round(msg, 3),
+                                            "tokens_per_s": round(T / msg * 1e3, 1),
+                                            "gate_us": round((msg - ms) * 1e3, 1)}
+                del og
             del tt, ws
         torch.cuda.empty_cache()
 

@@ -274,11 +274,6 @@ __device__ __forceinline__ void gate_from_raw(const GateRaw& r, int gate_mode, f
     beta = __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-r.b)));
   }
 }
-__device__ __forceinline__ void gate_values(const void* a, const void* b, int gate_mode,
-                                            const float* A_log, const float* dt_bias, int64_t idx,
-                                            int h, float& alpha, float& beta) {
-  gate_from_raw(gate_load(a, b, gate_mode, A_log, dt_bias, idx, h), gate_mode, alpha, beta);
-}
 
 // log-space variant used by the chunked prefill (it needs g itself).
 __device__ __forceinline__ void gate_log(const void* a, const void* b, int gate_mode,

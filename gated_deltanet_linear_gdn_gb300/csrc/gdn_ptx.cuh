@@ -1,6 +1,6 @@
 // gdn_ptx.cuh -- thin inline-PTX wrappers for sm_100-class asynchronous
 // hardware: mbarriers, bulk (TMA engine) copies between global and shared
-// memory, thread-block-cluster barriers, and a bounded mbarrier wait.
+// memory, an L2 prefetch, and a bounded mbarrier wait.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -91,13 +91,6 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
 // Hint: bring `bytes` (multiple of 16, 16-byte aligned) of global memory into L2.
 __device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
-}
-
-__device__ __forceinline__ void cluster_arrive_release() {
-  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void cluster_wait_acquire() {
-  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 }  // namespace gdn
