@@ -94,11 +94,17 @@ struct TcBufs {
 };
 
 __device__ __forceinline__ void split8(const float (&x)[8], uint4& hi, uint4& lo) {
-  uint16_t h[8], l[8];
+  // pairs converted at once (the same round-to-nearest-even per element as split_bf16)
+  uint32_t h[4], l[4];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) tc::split_bf16(x[i], h[i], l[i]);
-  hi = pack8(h);
-  lo = pack8(l);
+  for (int i = 0; i < 4; ++i) {
+    h[i] = pack_bf2(x[2 * i], x[2 * i + 1]);
+    const float r0 = x[2 * i] - __uint_as_float(h[i] << 16);
+    const float r1 = x[2 * i + 1] - __uint_as_float(h[i] & 0xFFFF0000u);
+    l[i] = pack_bf2(r0, r1);
+  }
+  hi = make_uint4(h[0], h[1], h[2], h[3]);
+  lo = make_uint4(l[0], l[1], l[2], l[3]);
 }
 
 // 8 rows x 8 bf16 (one uint4 per row) -> 8 columns (one uint4 per column)
