@@ -88,10 +88,20 @@ struct TcBufs {
   unsigned char* Kt;  // [chunk][Hk] bf16 k^T tile, K-major [128 x C]
   unsigned char* Wt;  // [chunk][Hv][hi, lo] bf16 W tile, K-major [C x 128]
   unsigned char* Pt;  // [chunk][Hv][hi, lo] bf16 P tile, K-major [C x C]
-  float* Ut;          // [chunk][Hv] fp32 U^T, [128][C]
+  float* Ut;          // [chunk][Hv] fp32 U^T [128 x C], laid out by u_image_offset
   float* vec;         // [chunk][Hv][256]: f[0..C), dd[64..64+C), g_last at [128]
   size_t q_tile, w_tile, p_tile;
 };
+
+// Byte offset of U^T(r, t) (state row r, token t of the chunk) in a U tile. The tile is
+// the byte image of the pass kernel's two bf16 [128 x C] D' operand tiles (hi, then lo):
+// tokens t..t+3 of an 8-token group sit where the hi tile holds (r, group), t+4..t+7
+// where the lo tile does. A bulk copy drops U onto those tiles, and the thread that owns
+// row r and the group reads its 32 bytes before writing its D' operands over them.
+__host__ __device__ __forceinline__ uint32_t u_image_offset(int r, int t, int C) {
+  return static_cast<uint32_t>(((t >> 2) & 1) * (128 * C * 2)) + tc::kmajor_offset(r, t & ~7, C) +
+         static_cast<uint32_t>((t & 3) * 4);
+}
 
 __device__ __forceinline__ void split8(const float (&x)[8], uint4& hi, uint4& lo) {
   // pairs converted at once (the same round-to-nearest-even per element as split_bf16)
@@ -446,14 +456,15 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     phase ^= 1;
     tc::fence_after_sync();
     if (!bad) {
-      // U^T -> workspace (fp32 [128][C]); W -> hi / lo tiles [C x 128]. Every lane
+      // U^T -> workspace (fp32 [128 x C] tile image); W -> hi / lo tiles [C x 128]. Every lane
       // executes the (warp-collective) loads; only rows of existing chunks store.
       const int t = 32 * (warp & 3) + lane, half = warp >> 2;
       const int ci = t / C, tl = t % C;
       const int c = c_first + ci;
       const bool store = c < nchunks;
       {
-        float* ut = wb.Ut + (static_cast<size_t>(store ? c : 0) * a.Hv + h) * (kD * C);
+        unsigned char* ut = reinterpret_cast<unsigned char*>(
+            wb.Ut + (static_cast<size_t>(store ? c : 0) * a.Hv + h) * (kD * C));
         unsigned char* wt = wb.Wt + (static_cast<size_t>(store ? c : 0) * a.Hv + h) * 2 * wb.w_tile;
 #pragma unroll 1
         for (int b0 = 0; b0 < 64; b0 += 16) {
@@ -464,7 +475,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
           tc::tmem_wait_ld();
           if (!store) continue;
 #pragma unroll
-          for (int e = 0; e < 16; ++e) ut[(col + e) * C + tl] = uv[e];
+          for (int e = 0; e < 16; ++e)
+            *reinterpret_cast<float*>(ut + u_image_offset(col + e, tl, C)) = uv[e];
 #pragma unroll
           for (int e8 = 0; e8 < 16; e8 += 8) {
             float x[8];
@@ -495,8 +507,9 @@ struct PassSmem {
   static constexpr int kP = C * C * 2;          // P tiles    [C x C]     bf16
   static constexpr int oSh = 0, oSl = kS;
   static constexpr int oDh = 2 * kS, oDl = oDh + kD_, oEh = oDl + kD_, oEl = oEh + kD_;
-  static constexpr int oWh = oEl + kD_, oWl = oWh + kW, oQ = oWl + kW;
-  static constexpr int oPh = oQ + kW, oPl = oPh + kP, oKt = oPl + kP;
+  // the q tile follows the W hi tile: together they are one [2C x 128] MMA operand
+  static constexpr int oWh = oEl + kD_, oQ = oWh + kW, oWl = oQ + kW;
+  static constexpr int oPh = oWl + kW, oPl = oPh + kP, oKt = oPl + kP;
   static constexpr int oVec = oKt + kD_;        // two vec buffers of kVecFloats
   static constexpr int oO = oVec + 2 * kVecFloats * 4;  // bf16 output tile [C x 128]
   static constexpr int kBytes = oO + C * 128 * 2;
@@ -510,7 +523,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   using S = PassSmem<C>;
   extern __shared__ __align__(1024) unsigned char sm[];
   __shared__ uint32_t s_tmem;
-  __shared__ __align__(8) uint64_t s_bar[4];  // fullA, fullB, mma1, mma2
+  __shared__ __align__(8) uint64_t s_bar[5];  // fullA, fullB, mma1, mma2, fullU
 
   const int i = blockIdx.x, h = blockIdx.y;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -532,26 +545,22 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   const int r = 32 * q + lane;  // state row (dv index) = tensor-memory lane
   const uint32_t fullA = smem_addr(&s_bar[0]), fullB = smem_addr(&s_bar[1]);
   const uint32_t mma1 = smem_addr(&s_bar[2]), mma2 = smem_addr(&s_bar[3]);
+  const uint32_t fullU = smem_addr(&s_bar[4]);
   const size_t wtile = wb.w_tile, ptile = wb.p_tile;
 
-  // W hi/lo, q tile, vec of chunk c0 + it, all on one fullA phase (armed with the total):
-  // W and vec as soon as group 1's W products are done, q once its Q products are
-  auto issue_A_w = [&](int it) {
+  // W hi/lo, q tile, vec of chunk c0 + it on one fullA phase (group 1's operands, and vec)
+  auto issue_A = [&](int it) {
     const int c = c0 + it;
+    const int kh = h / (a.Hv / a.Hk);
     const unsigned char* w = wb.Wt + (static_cast<size_t>(c) * a.Hv + h) * 2 * wtile;
+    const unsigned char* qt = wb.Qt + (static_cast<size_t>(c) * a.Hk + kh) * wb.q_tile;
     const float* vec = wb.vec + (static_cast<size_t>(c) * a.Hv + h) * kVecFloats;
     mbar_arrive_expect_tx(fullA, static_cast<uint32_t>(2 * wtile + wb.q_tile + kVecFloats * 4));
     bulk_g2s(smem_addr(sm + S::oWh), w, static_cast<uint32_t>(wtile), fullA);
     bulk_g2s(smem_addr(sm + S::oWl), w + wtile, static_cast<uint32_t>(wtile), fullA);
+    bulk_g2s(smem_addr(sm + S::oQ), qt, static_cast<uint32_t>(wb.q_tile), fullA);
     bulk_g2s(smem_addr(sm + S::oVec + (it & 1) * kVecFloats * 4), vec, kVecFloats * 4, fullA);
   };
-  auto issue_A_q = [&](int it) {
-    const int c = c0 + it;
-    const int kh = h / (a.Hv / a.Hk);
-    const unsigned char* qt = wb.Qt + (static_cast<size_t>(c) * a.Hk + kh) * wb.q_tile;
-    bulk_g2s(smem_addr(sm + S::oQ), qt, static_cast<uint32_t>(wb.q_tile), fullA);
-  };
-  auto issue_A = [&](int it) { issue_A_w(it); issue_A_q(it); };
   auto issue_B = [&](int it) {  // P hi/lo, k^T tile of chunk c0 + it
     const int c = c0 + it;
     const int kh = h / (a.Hv / a.Hk);
@@ -562,12 +571,17 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     bulk_g2s(smem_addr(sm + S::oPl), pp + ptile, static_cast<uint32_t>(ptile), fullB);
     bulk_g2s(smem_addr(sm + S::oKt), kt, static_cast<uint32_t>(wb.q_tile), fullB);
   };
+  auto issue_U = [&](int it) {  // U^T of chunk c0 + it onto the D' tiles (free once group 2 is done)
+    const float* ut = wb.Ut + (static_cast<size_t>(c0 + it) * a.Hv + h) * (kD * C);
+    mbar_arrive_expect_tx(fullU, static_cast<uint32_t>(kD * C * 4));
+    bulk_g2s(smem_addr(sm + S::oEh), ut, static_cast<uint32_t>(kD * C * 4), fullU);
+  };
 
   if (warp == 0) tc::tmem_alloc(&s_tmem, kTmemCols);
   if (tid == 0) {
-    for (int k = 0; k < 4; ++k) mbar_init(smem_addr(&s_bar[k]), 1);
+    for (int k = 0; k < 5; ++k) mbar_init(smem_addr(&s_bar[k]), 1);
     fence_mbar_init();
-    if (nch > 0) { issue_A(0); issue_B(0); }
+    if (nch > 0) { issue_A(0); issue_B(0); issue_U(0); }
   }
   // state (half a row per thread) -> registers and the split operand tiles
   const int64_t soff = (static_cast<int64_t>(slot) * a.Hv + h) * (kD * kD) + r * kD + half * 64;
@@ -605,7 +619,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   store_S_tiles();
   bool bad = tc_sync(false);
   const uint32_t tb = s_tmem;
-  // tensor-memory columns: D^T raw [0, C), O1^T [64, 64 + C), O2^T [128, 128 + C),
+  // tensor-memory columns: D^T raw [0, C), O1^T [C, 2C), O2^T [128, 128 + C),
   // state update [256, 384)
   constexpr int NH = C / 2;
   constexpr int KS = C / 16;
@@ -614,7 +628,6 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   const uint64_t dSl = tc::kmajor_desc(smem_addr(sm + S::oSl), 128, 0);
   const uint64_t dWh = tc::kmajor_desc(smem_addr(sm + S::oWh), 128, 0);
   const uint64_t dWl = tc::kmajor_desc(smem_addr(sm + S::oWl), 128, 0);
-  const uint64_t dQ = tc::kmajor_desc(smem_addr(sm + S::oQ), 128, 0);
   const uint64_t dDh = tc::kmajor_desc(smem_addr(sm + S::oDh), C, 0);
   const uint64_t dDl = tc::kmajor_desc(smem_addr(sm + S::oDl), C, 0);
   const uint64_t dEh = tc::kmajor_desc(smem_addr(sm + S::oEh), C, 0);
@@ -622,23 +635,20 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   const uint64_t dPh = tc::kmajor_desc(smem_addr(sm + S::oPh), C, 0);
   const uint64_t dPl = tc::kmajor_desc(smem_addr(sm + S::oPl), C, 0);
   const uint64_t dKt = tc::kmajor_desc(smem_addr(sm + S::oKt), C, 0);
-  const uint32_t idC = tc::idesc_bf16_f32(128, C), id128 = tc::idesc_bf16_f32(128, 128);
+  const uint32_t idC = tc::idesc_bf16_f32(128, C), id2C = tc::idesc_bf16_f32(128, 2 * C);
+  const uint32_t id128 = tc::idesc_bf16_f32(128, 128);
 
-  // MMA group 1 of chunk `it` (thread 0): D^T raw = S W^T, committed on its own --
-  // the chain needs only D -- then O1^T = S Q^T, which completes under group 2's commit
+  // MMA group 1 of chunk `it` (thread 0): S [W_hi | Q]^T over N = 2C puts S W_hi^T into
+  // the D^T columns and S Q^T (= O1^T, both S parts) into the next C; S_hi W_lo^T completes D
   auto issue_mma1 = [&](int it) -> bool {
     if (!mbar_wait_bounded(fullA, it & 1)) return false;
 #pragma unroll
-    for (int ks = 0; ks < 8; ++ks) tc::mma_bf16(tb, dSh + 16 * ks, dWh + 16 * ks, idC, ks > 0);
+    for (int ks = 0; ks < 8; ++ks) tc::mma_bf16(tb, dSh + 16 * ks, dWh + 16 * ks, id2C, ks > 0);
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) tc::mma_bf16(tb, dSl + 16 * ks, dWh + 16 * ks, id2C, 1);
 #pragma unroll
     for (int ks = 0; ks < 8; ++ks) tc::mma_bf16(tb, dSh + 16 * ks, dWl + 16 * ks, idC, 1);
-#pragma unroll
-    for (int ks = 0; ks < 8; ++ks) tc::mma_bf16(tb, dSl + 16 * ks, dWh + 16 * ks, idC, 1);
     tc::mma_commit(mma1);
-#pragma unroll
-    for (int ks = 0; ks < 8; ++ks) tc::mma_bf16(tb + 64, dSh + 16 * ks, dQ + 16 * ks, idC, ks > 0);
-#pragma unroll
-    for (int ks = 0; ks < 8; ++ks) tc::mma_bf16(tb + 64, dSl + 16 * ks, dQ + 16 * ks, idC, 1);
     return true;
   };
   // a thread 0 failure leaves an MMA group unissued; the other threads' bounded waits
@@ -659,29 +669,16 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   };
   if (tid == 32 && nch > 1) prefetch_chunk(1);
 
-  // U^T values this thread needs (row r, tokens half*NH ..) of chunk `it`: loaded at the
-  // chunk's start while MMA group 1 runs, except by warp 0, whose thread 0 spends that time
-  // issuing the MMAs -- warp 0 loads them a chunk ahead
-  float Ur[NH];
-  auto load_U = [&](int it) {
-    const float* ut = wb.Ut + (static_cast<size_t>(c0 + it) * a.Hv + h) * (kD * C) + r * C + half * NH;
-#pragma unroll
-    for (int e = 0; e < NH; e += 4) {
-      const float4 v = *reinterpret_cast<const float4*>(ut + e);
-      Ur[e] = v.x; Ur[e + 1] = v.y; Ur[e + 2] = v.z; Ur[e + 3] = v.w;
-    }
-  };
-  if (warp == 0 && nch > 0) load_U(0);
   for (int it = 0; it < nch && !bad; ++it) {
     const int t0 = bos + it * C;
     const int L = min(C, eos - t0);
     const uint32_t par = it & 1;
     if (tid == 32 && it + 2 < nch) prefetch_chunk(it + 2);  // two chunks ahead
-    if (warp != 0) load_U(it);
     if (!mbar_wait_bounded(mma1, par)) bad = true;
+    if (!mbar_wait_bounded(fullU, par)) bad = true;
     bad = __any_sync(0xffffffffu, bad);  // warp-uniform before the aligned loads
     tc::fence_after_sync();
-    if (tid == 0 && !bad && it + 1 < nch) issue_A_w(it + 1);  // the W buffers are free again
+    if (tid == 0 && !bad && it + 1 < nch) issue_A(it + 1);  // the W and q buffers are free again
     const float* vec = reinterpret_cast<const float*>(sm + S::oVec + par * kVecFloats * 4);
     if (!bad) {
       // D = U - raw, D' = D dd_t; both split into the [128 x C] operand tiles
@@ -703,14 +700,18 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       tc::tmem_wait_ld();
 #pragma unroll
       for (int e8 = 0; e8 < NH; e8 += 8) {
+        const uint32_t o = tc::kmajor_offset(r, half * NH + e8, C);
+        // this thread's U^T values of the 8 tokens, read before its D' pieces overwrite them
+        const float4 u0 = *reinterpret_cast<const float4*>(sm + S::oEh + o);
+        const float4 u1 = *reinterpret_cast<const float4*>(sm + S::oEl + o);
+        const float u[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
         float d[8], dd[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-          d[e] = Ur[e8 + e] - raw[e8 + e];
+          d[e] = u[e] - raw[e8 + e];
           dd[e] = d[e] * vec[64 + half * NH + e8 + e];
         }
         uint4 hi, lo;
-        const uint32_t o = tc::kmajor_offset(r, half * NH + e8, C);
         split8(d, hi, lo);
         *reinterpret_cast<uint4*>(sm + S::oDh + o) = hi;
         *reinterpret_cast<uint4*>(sm + S::oDl + o) = lo;
@@ -743,8 +744,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     bad = __any_sync(0xffffffffu, bad);  // warp-uniform before the aligned loads
     tc::fence_after_sync();
     if (tid == 0 && !bad && it + 1 < nch) {
-      issue_B(it + 1);    // P, k^T buffers are free again
-      issue_A_q(it + 1);  // and the q buffer (group 2's commit covers group 1's Q products)
+      issue_B(it + 1);  // P, k^T buffers are free again
+      issue_U(it + 1);  // and the D' tiles
     }
     float Ov[NH];
     if (!bad) {
@@ -754,14 +755,14 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
 #pragma unroll
         for (int b0 = 0; b0 < NH; b0 += 16) {
           float ta[16], tbv[16];
-          tmem_load<16>(tc::taddr(tb, 32 * q, 64 + half * NH + b0), ta);
+          tmem_load<16>(tc::taddr(tb, 32 * q, C + half * NH + b0), ta);
           tmem_load<16>(tc::taddr(tb, 32 * q, 128 + half * NH + b0), tbv);
 #pragma unroll
           for (int e = 0; e < 16; ++e) { o1[b0 + e] = ta[e]; o2[b0 + e] = tbv[e]; }
         }
       } else {
         float ta[8], tbv[8];
-        tmem_load<8>(tc::taddr(tb, 32 * q, 64 + half * NH), ta);
+        tmem_load<8>(tc::taddr(tb, 32 * q, C + half * NH), ta);
         tmem_load<8>(tc::taddr(tb, 32 * q, 128 + half * NH), tbv);
 #pragma unroll
         for (int e = 0; e < 8; ++e) { o1[e] = ta[e]; o2[e] = tbv[e]; }
@@ -792,7 +793,6 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     }
     bad = tc_sync(bad);
     if (bad) break;
-    if (warp == 0 && it + 1 < nch) load_U(it + 1);
     if (tid == 0 && it + 1 < nch && !issue_mma1(it + 1)) bad = true;
     if (a.out_f32) {
 #pragma unroll
