@@ -47,6 +47,11 @@ namespace {
 
 constexpr int kD = 128;          // dk = dv
 constexpr int kThreadsTc = 256;  // 8 warps: warp w reads tensor-memory lanes 32 (w % 4) ..
+// the pass kernel adds two warps: warp 8 (lane 0) issues the MMA groups, warp 9 (lane 0) the
+// bulk copies. The copy warp paces itself on mbarriers alone; the other nine warps meet at
+// a named barrier of kSyncThreads
+constexpr int kPassThreads = kThreadsTc + 64;
+constexpr int kSyncThreads = kThreadsTc + 32;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kVecFloats = 256;  // per (chunk, head): f[C], dd[C], g_last
 
@@ -148,6 +153,21 @@ __device__ __forceinline__ bool tc_sync(bool bad) {
   tc::fence_async_smem();
   tc::fence_before_sync();
   const int any = __syncthreads_or(bad ? 1 : 0);
+  tc::fence_after_sync();
+  return any != 0;
+}
+
+// tc_sync over the compute and MMA warps of the pass kernel (named barrier 1)
+__device__ __forceinline__ bool pass_sync(bool bad) {
+  tc::fence_async_smem();
+  tc::fence_before_sync();
+  uint32_t any;
+  asm volatile(
+      "{\n.reg .pred p, q;\nsetp.ne.u32 p, %1, 0;\nbar.red.or.pred q, 1, %2, p;\n"
+      "selp.u32 %0, 1, 0, q;\n}"
+      : "=r"(any)
+      : "r"(static_cast<uint32_t>(bad)), "n"(kSyncThreads)
+      : "memory");
   tc::fence_after_sync();
   return any != 0;
 }
@@ -517,7 +537,7 @@ struct PassSmem {
 };
 
 template <int C>
-__global__ void __launch_bounds__(kThreadsTc, 1)
+__global__ void __launch_bounds__(kPassThreads, 1)
     pass_tc_kernel(LayerArgs a, PrefillExtra p, const int32_t* seq_ok, const int32_t* chunk_off,
                    TcBufs wb) {
   using S = PassSmem<C>;
@@ -531,7 +551,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   if (!seq_ok[i]) {  // inactive / invalid sequence (or bad cu_seqlens): zero outputs
     int64_t n = static_cast<int64_t>(max(eos - bos, 0));
     if (bos < 0 || eos > p.total_tokens) n = 0;
-    for (int64_t idx = tid; idx < n * kD; idx += kThreadsTc) {
+    for (int64_t idx = tid; idx < n * kD; idx += kPassThreads) {
       const int64_t o = ((bos + idx / kD) * a.Hv + h) * kD + idx % kD;
       if (a.out_f32) static_cast<float*>(a.out)[o] = 0.0f;
       else static_cast<uint16_t*>(a.out)[o] = 0;
@@ -541,7 +561,9 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   const int c0 = chunk_off[i], nch = chunk_off[i + 1] - c0;
   const int32_t slot = a.slot[i];
   const bool init = (p.has_init == nullptr) || (p.has_init[i] != 0);
-  const int q = warp & 3, half = warp >> 2;
+  const bool mma_warp = warp == kThreadsTc / 32, copy_warp = warp == kThreadsTc / 32 + 1;
+  const bool compute = warp < kThreadsTc / 32;
+  const int q = warp & 3, half = warp >> 2;  // compute warps
   const int r = 32 * q + lane;  // state row (dv index) = tensor-memory lane
   const uint32_t fullA = smem_addr(&s_bar[0]), fullB = smem_addr(&s_bar[1]);
   const uint32_t mma1 = smem_addr(&s_bar[2]), mma2 = smem_addr(&s_bar[3]);
@@ -578,29 +600,31 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   };
 
   if (warp == 0) tc::tmem_alloc(&s_tmem, kTmemCols);
-  if (tid == 0) {
+  if (copy_warp && lane == 0) {
     for (int k = 0; k < 5; ++k) mbar_init(smem_addr(&s_bar[k]), 1);
     fence_mbar_init();
     if (nch > 0) { issue_A(0); issue_B(0); issue_U(0); }
   }
-  // state (half a row per thread) -> registers and the split operand tiles
+  // state (half a row per compute thread) -> registers and the split operand tiles
   const int64_t soff = (static_cast<int64_t>(slot) * a.Hv + h) * (kD * kD) + r * kD + half * 64;
   float* Sg = a.ssm + soff;                                          // fp32 state
   uint16_t* Sb = reinterpret_cast<uint16_t*>(a.ssm) + soff;          // bf16 state
   float Sr[64];
-  if (a.ssm_bf16) {
+  if (compute) {
+    if (a.ssm_bf16) {
 #pragma unroll
-    for (int e = 0; e < 64; e += 8) {
-      float f[8];
-      unpack8(init ? *reinterpret_cast<const uint4*>(Sb + e) : make_uint4(0u, 0u, 0u, 0u), f);
+      for (int e = 0; e < 64; e += 8) {
+        float f[8];
+        unpack8(init ? *reinterpret_cast<const uint4*>(Sb + e) : make_uint4(0u, 0u, 0u, 0u), f);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) Sr[e + i] = f[i];
-    }
-  } else {
+        for (int i = 0; i < 8; ++i) Sr[e + i] = f[i];
+      }
+    } else {
 #pragma unroll
-    for (int e = 0; e < 64; e += 4) {
-      float4 v = init ? *reinterpret_cast<const float4*>(Sg + e) : make_float4(0.f, 0.f, 0.f, 0.f);
-      Sr[e] = v.x; Sr[e + 1] = v.y; Sr[e + 2] = v.z; Sr[e + 3] = v.w;
+      for (int e = 0; e < 64; e += 4) {
+        float4 v = init ? *reinterpret_cast<const float4*>(Sg + e) : make_float4(0.f, 0.f, 0.f, 0.f);
+        Sr[e] = v.x; Sr[e + 1] = v.y; Sr[e + 2] = v.z; Sr[e + 3] = v.w;
+      }
     }
   }
   auto store_S_tiles = [&]() {
@@ -616,8 +640,9 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       *reinterpret_cast<uint4*>(sm + S::oSl + o) = lo;
     }
   };
-  store_S_tiles();
+  if (compute) store_S_tiles();
   bool bad = tc_sync(false);
+  bool mine = false;  // this thread's wait failure, reported at the next CTA barrier
   const uint32_t tb = s_tmem;
   // tensor-memory columns: D^T raw [0, C), O1^T [C, 2C), O2^T [128, 128 + C),
   // state update [256, 384)
@@ -638,7 +663,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   const uint32_t idC = tc::idesc_bf16_f32(128, C), id2C = tc::idesc_bf16_f32(128, 2 * C);
   const uint32_t id128 = tc::idesc_bf16_f32(128, 128);
 
-  // MMA group 1 of chunk `it` (thread 0): S [W_hi | Q]^T over N = 2C puts S W_hi^T into
+  // MMA group 1 of chunk `it` (the MMA warp): S [W_hi | Q]^T over N = 2C puts S W_hi^T into
   // the D^T columns and S Q^T (= O1^T, both S parts) into the next C; S_hi W_lo^T completes D
   auto issue_mma1 = [&](int it) -> bool {
     if (!mbar_wait_bounded(fullA, it & 1)) return false;
@@ -651,9 +676,9 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     tc::mma_commit(mma1);
     return true;
   };
-  // a thread 0 failure leaves an MMA group unissued; the other threads' bounded waits
-  // then expire, and every thread learns of it at the next CTA barrier
-  if (tid == 0 && nch > 0 && !bad && !issue_mma1(0)) bad = true;
+  // an MMA-warp failure leaves an MMA group unissued; the compute threads' bounded waits
+  // then expire, and every thread learns of it at the next barrier
+  if (mma_warp && lane == 0 && nch > 0 && !bad) mine = !issue_mma1(0);
 
   auto prefetch_chunk = [&](int it) {  // the workspace tiles of chunk c0 + it -> L2
     const int c = c0 + it;
@@ -667,165 +692,210 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     bulk_prefetch_l2(wb.Qt + ck * wb.q_tile, static_cast<uint32_t>(wb.q_tile));
     bulk_prefetch_l2(wb.Kt + ck * wb.q_tile, static_cast<uint32_t>(wb.q_tile));
   };
-  if (tid == 32 && nch > 1) prefetch_chunk(1);
+  if (copy_warp) {
+    // chunk it + 1's tiles as soon as chunk it's MMA groups release their buffers: W, q,
+    // vec after group 1; P, k^T and U (onto the D' tiles) after group 2. fullA / fullB /
+    // fullU of chunk it + 1 are armed only after this warp has seen group 1 / 2 of chunk it
+    // complete, so no parity wait can alias a later phase
+    bool ok = !bad;
+    if (lane == 0 && ok && nch > 0) {
+      int nA = 1, nBU = 1;  // phases issued (chunk 0's at set-up)
+      if (nch > 1) prefetch_chunk(1);
+      for (int it = 0; it + 1 < nch; ++it) {
+        const uint32_t par = it & 1;
+        if (it + 2 < nch) prefetch_chunk(it + 2);  // two chunks ahead
+        if (!mbar_wait_bounded(mma1, par)) { ok = false; break; }
+        tc::fence_after_sync();
+        issue_A(it + 1);
+        nA = it + 2;
+        if (!mbar_wait_bounded(mma2, par)) { ok = false; break; }
+        tc::fence_after_sync();
+        issue_B(it + 1);
+        issue_U(it + 1);
+        nBU = it + 2;
+      }
+      if (!ok) {
+        if (a.err) atomicOr(a.err, GDN_DEVERR_TIMEOUT);
+        // copies may still be in flight: wait (bounded) for the last issued phase of each
+        // barrier -- one already completed (and consumed) returns at once
+        mbar_wait_bounded(fullA, (nA - 1) & 1);
+        mbar_wait_bounded(fullB, (nBU - 1) & 1);
+        mbar_wait_bounded(fullU, (nBU - 1) & 1);
+      }
+    }
+  }
 
-  for (int it = 0; it < nch && !bad; ++it) {
+  int n1 = (mma_warp && nch > 0 && !mine) ? 1 : 0, n2 = 0;  // MMA groups committed
+  for (int it = 0; it < nch && !bad && !copy_warp; ++it) {
     const int t0 = bos + it * C;
     const int L = min(C, eos - t0);
     const uint32_t par = it & 1;
-    if (tid == 32 && it + 2 < nch) prefetch_chunk(it + 2);  // two chunks ahead
-    if (!mbar_wait_bounded(mma1, par)) bad = true;
-    if (!mbar_wait_bounded(fullU, par)) bad = true;
-    bad = __any_sync(0xffffffffu, bad);  // warp-uniform before the aligned loads
-    tc::fence_after_sync();
-    if (tid == 0 && !bad && it + 1 < nch) issue_A(it + 1);  // the W and q buffers are free again
     const float* vec = reinterpret_cast<const float*>(sm + S::oVec + par * kVecFloats * 4);
-    if (!bad) {
-      // D = U - raw, D' = D dd_t; both split into the [128 x C] operand tiles
-      float raw[NH];
-      if constexpr (NH >= 16) {
-#pragma unroll
-        for (int b0 = 0; b0 < NH; b0 += 16) {
-          float tv[16];
-          tmem_load<16>(tc::taddr(tb, 32 * q, half * NH + b0), tv);
-#pragma unroll
-          for (int e = 0; e < 16; ++e) raw[b0 + e] = tv[e];
-        }
-      } else {
-        float tv[8];
-        tmem_load<8>(tc::taddr(tb, 32 * q, half * NH), tv);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) raw[e] = tv[e];
-      }
-      tc::tmem_wait_ld();
-#pragma unroll
-      for (int e8 = 0; e8 < NH; e8 += 8) {
-        const uint32_t o = tc::kmajor_offset(r, half * NH + e8, C);
-        // this thread's U^T values of the 8 tokens, read before its D' pieces overwrite them
-        const float4 u0 = *reinterpret_cast<const float4*>(sm + S::oEh + o);
-        const float4 u1 = *reinterpret_cast<const float4*>(sm + S::oEl + o);
-        const float u[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
-        float d[8], dd[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          d[e] = u[e] - raw[e8 + e];
-          dd[e] = d[e] * vec[64 + half * NH + e8 + e];
-        }
-        uint4 hi, lo;
-        split8(d, hi, lo);
-        *reinterpret_cast<uint4*>(sm + S::oDh + o) = hi;
-        *reinterpret_cast<uint4*>(sm + S::oDl + o) = lo;
-        split8(dd, hi, lo);
-        *reinterpret_cast<uint4*>(sm + S::oEh + o) = hi;
-        *reinterpret_cast<uint4*>(sm + S::oEl + o) = lo;
-      }
-    }
-    bad = tc_sync(bad);
-    if (bad) break;
-    // ---- MMA group 2: O2^T = D^T P^T (3 products), update = D'^T K (2 products)
-    if (tid == 0) {
-      if (mbar_wait_bounded(fullB, par)) {
-#pragma unroll
-        for (int ks = 0; ks < KS; ++ks) tc::mma_bf16(tb + 128, dDh + 16 * ks, dPh + 16 * ks, idC, ks > 0);
-#pragma unroll
-        for (int ks = 0; ks < KS; ++ks) tc::mma_bf16(tb + 128, dDh + 16 * ks, dPl + 16 * ks, idC, 1);
-#pragma unroll
-        for (int ks = 0; ks < KS; ++ks) tc::mma_bf16(tb + 128, dDl + 16 * ks, dPh + 16 * ks, idC, 1);
-#pragma unroll
-        for (int ks = 0; ks < KS; ++ks) tc::mma_bf16(tb + 256, dEh + 16 * ks, dKt + 16 * ks, id128, ks > 0);
-#pragma unroll
-        for (int ks = 0; ks < KS; ++ks) tc::mma_bf16(tb + 256, dEl + 16 * ks, dKt + 16 * ks, id128, 1);
-        tc::mma_commit(mma2);
-      } else {
-        bad = true;
-      }
-    }
-    if (!mbar_wait_bounded(mma2, par)) bad = true;
-    bad = __any_sync(0xffffffffu, bad);  // warp-uniform before the aligned loads
-    tc::fence_after_sync();
-    if (tid == 0 && !bad && it + 1 < nch) {
-      issue_B(it + 1);  // P, k^T buffers are free again
-      issue_U(it + 1);  // and the D' tiles
-    }
     float Ov[NH];
-    if (!bad) {
-      // O = f_t O1 + O2 into registers (stored below, while the next chunk's MMAs run)
-      float o1[NH], o2[NH];
-      if constexpr (NH >= 16) {
+    if (compute) {
+      if (!mbar_wait_bounded(mma1, par)) mine = true;
+      if (!mbar_wait_bounded(fullU, par)) mine = true;
+      mine = __any_sync(0xffffffffu, mine);  // warp-uniform before the aligned loads
+      tc::fence_after_sync();
+      if (!mine) {
+        // D = U - raw, D' = D dd_t; both split into the [128 x C] operand tiles
+        float raw[NH];
+        if constexpr (NH >= 16) {
 #pragma unroll
-        for (int b0 = 0; b0 < NH; b0 += 16) {
-          float ta[16], tbv[16];
-          tmem_load<16>(tc::taddr(tb, 32 * q, C + half * NH + b0), ta);
-          tmem_load<16>(tc::taddr(tb, 32 * q, 128 + half * NH + b0), tbv);
+          for (int b0 = 0; b0 < NH; b0 += 16) {
+            float tv[16];
+            tmem_load<16>(tc::taddr(tb, 32 * q, half * NH + b0), tv);
 #pragma unroll
-          for (int e = 0; e < 16; ++e) { o1[b0 + e] = ta[e]; o2[b0 + e] = tbv[e]; }
+            for (int e = 0; e < 16; ++e) raw[b0 + e] = tv[e];
+          }
+        } else {
+          float tv[8];
+          tmem_load<8>(tc::taddr(tb, 32 * q, half * NH), tv);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) raw[e] = tv[e];
         }
-      } else {
-        float ta[8], tbv[8];
-        tmem_load<8>(tc::taddr(tb, 32 * q, C + half * NH), ta);
-        tmem_load<8>(tc::taddr(tb, 32 * q, 128 + half * NH), tbv);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) { o1[e] = ta[e]; o2[e] = tbv[e]; }
-      }
-      tc::tmem_wait_ld();
-#pragma unroll
-      for (int e = 0; e < NH; ++e) Ov[e] = fmaf(vec[half * NH + e], o1[e], o2[e]);
-      if (!a.out_f32) {  // bf16 output: stage the tile [token][dv] for 16-byte stores below
-        uint16_t* ot = reinterpret_cast<uint16_t*>(sm + S::oO);
-#pragma unroll
-        for (int e = 0; e < NH; ++e) ot[(half * NH + e) * kD + r] = f2bf(Ov[e]);
-      }
-      // S <- g_last S + update, 16 columns at a time
-      const float gl = vec[128];
-#pragma unroll
-      for (int b0 = 0; b0 < 64; b0 += 32) {  // two loads in flight per wait
-        float tv0[16], tv1[16];
-        tmem_load<16>(tc::taddr(tb, 32 * q, 256 + half * 64 + b0), tv0);
-        tmem_load<16>(tc::taddr(tb, 32 * q, 256 + half * 64 + b0 + 16), tv1);
         tc::tmem_wait_ld();
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          Sr[b0 + e] = fmaf(gl, Sr[b0 + e], tv0[e]);
-          Sr[b0 + 16 + e] = fmaf(gl, Sr[b0 + 16 + e], tv1[e]);
+        for (int e8 = 0; e8 < NH; e8 += 8) {
+          const uint32_t o = tc::kmajor_offset(r, half * NH + e8, C);
+          // this thread's U^T values of the 8 tokens, read before its D' pieces overwrite them
+          const float4 u0 = *reinterpret_cast<const float4*>(sm + S::oEh + o);
+          const float4 u1 = *reinterpret_cast<const float4*>(sm + S::oEl + o);
+          const float u[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+          float d[8], dd[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            d[e] = u[e] - raw[e8 + e];
+            dd[e] = d[e] * vec[64 + half * NH + e8 + e];
+          }
+          uint4 hi, lo;
+          split8(d, hi, lo);
+          *reinterpret_cast<uint4*>(sm + S::oDh + o) = hi;
+          *reinterpret_cast<uint4*>(sm + S::oDl + o) = lo;
+          split8(dd, hi, lo);
+          *reinterpret_cast<uint4*>(sm + S::oEh + o) = hi;
+          *reinterpret_cast<uint4*>(sm + S::oEl + o) = lo;
         }
       }
-      store_S_tiles();
     }
-    bad = tc_sync(bad);
+    bad = pass_sync(mine);
     if (bad) break;
-    if (tid == 0 && it + 1 < nch && !issue_mma1(it + 1)) bad = true;
-    if (a.out_f32) {
+    if (mma_warp) {
+      // ---- MMA group 2: O2^T = D^T P^T (3 products), update = D'^T K (2 products)
+      if (lane == 0) {
+        if (mbar_wait_bounded(fullB, par)) {
+#pragma unroll
+          for (int ks = 0; ks < KS; ++ks)
+            tc::mma_bf16(tb + 128, dDh + 16 * ks, dPh + 16 * ks, idC, ks > 0);
+#pragma unroll
+          for (int ks = 0; ks < KS; ++ks) tc::mma_bf16(tb + 128, dDh + 16 * ks, dPl + 16 * ks, idC, 1);
+#pragma unroll
+          for (int ks = 0; ks < KS; ++ks) tc::mma_bf16(tb + 128, dDl + 16 * ks, dPh + 16 * ks, idC, 1);
+#pragma unroll
+          for (int ks = 0; ks < KS; ++ks)
+            tc::mma_bf16(tb + 256, dEh + 16 * ks, dKt + 16 * ks, id128, ks > 0);
+#pragma unroll
+          for (int ks = 0; ks < KS; ++ks) tc::mma_bf16(tb + 256, dEl + 16 * ks, dKt + 16 * ks, id128, 1);
+          tc::mma_commit(mma2);
+          n2 = it + 1;
+        } else {
+          mine = true;
+        }
+      }
+    } else {  // compute warps
+      if (!mbar_wait_bounded(mma2, par)) mine = true;
+      mine = __any_sync(0xffffffffu, mine);  // warp-uniform before the aligned loads
+      tc::fence_after_sync();
+      if (!mine) {
+        // O = f_t O1 + O2 into registers (stored below, while the next chunk's MMAs run)
+        float o1[NH], o2[NH];
+        if constexpr (NH >= 16) {
+#pragma unroll
+          for (int b0 = 0; b0 < NH; b0 += 16) {
+            float ta[16], tbv[16];
+            tmem_load<16>(tc::taddr(tb, 32 * q, C + half * NH + b0), ta);
+            tmem_load<16>(tc::taddr(tb, 32 * q, 128 + half * NH + b0), tbv);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) { o1[b0 + e] = ta[e]; o2[b0 + e] = tbv[e]; }
+          }
+        } else {
+          float ta[8], tbv[8];
+          tmem_load<8>(tc::taddr(tb, 32 * q, C + half * NH), ta);
+          tmem_load<8>(tc::taddr(tb, 32 * q, 128 + half * NH), tbv);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) { o1[e] = ta[e]; o2[e] = tbv[e]; }
+        }
+        tc::tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < NH; ++e) Ov[e] = fmaf(vec[half * NH + e], o1[e], o2[e]);
+        if (!a.out_f32) {  // bf16 output: stage the tile [token][dv] for 16-byte stores below
+          uint16_t* ot = reinterpret_cast<uint16_t*>(sm + S::oO);
+#pragma unroll
+          for (int e = 0; e < NH; ++e) ot[(half * NH + e) * kD + r] = f2bf(Ov[e]);
+        }
+        // S <- g_last S + update, 16 columns at a time
+        const float gl = vec[128];
+#pragma unroll
+        for (int b0 = 0; b0 < 64; b0 += 32) {  // two loads in flight per wait
+          float tv0[16], tv1[16];
+          tmem_load<16>(tc::taddr(tb, 32 * q, 256 + half * 64 + b0), tv0);
+          tmem_load<16>(tc::taddr(tb, 32 * q, 256 + half * 64 + b0 + 16), tv1);
+          tc::tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            Sr[b0 + e] = fmaf(gl, Sr[b0 + e], tv0[e]);
+            Sr[b0 + 16 + e] = fmaf(gl, Sr[b0 + 16 + e], tv1[e]);
+          }
+        }
+        store_S_tiles();
+      }
+    }
+    bad = pass_sync(mine);
+    if (bad) break;
+    if (mma_warp) {
+      if (lane == 0 && it + 1 < nch) {
+        mine = !issue_mma1(it + 1);
+        if (!mine) n1 = it + 2;
+      }
+    } else if (a.out_f32) {
 #pragma unroll
       for (int e = 0; e < NH; ++e) {
         const int tt = half * NH + e;
         if (tt < L)
           static_cast<float*>(a.out)[(static_cast<int64_t>(t0 + tt) * a.Hv + h) * kD + r] = Ov[e];
       }
-    } else if (warp > 0) {
-      // warps 1-7 copy the staged tile out in 16-byte pieces while thread 0 issues the
-      // next chunk's MMAs (the tile is rewritten only after the next chunk's barrier)
+    } else {
+      // the compute warps copy the staged tile out in 16-byte pieces while the MMA warp
+      // issues the next chunk's MMAs (the tile is rewritten only after the next barrier)
       const uint4* ot = reinterpret_cast<const uint4*>(sm + S::oO);
-      for (int k = tid - 32; k < L * (kD / 8); k += kThreadsTc - 32) {
+      for (int k = tid; k < L * (kD / 8); k += kThreadsTc) {
         const int tt = k / (kD / 8), col = (k % (kD / 8)) * 8;
         *reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.out) +
                                   (static_cast<int64_t>(t0 + tt) * a.Hv + h) * kD + col) = ot[k];
       }
     }
   }
-  bad = tc_sync(bad);
+  if (!copy_warp) bad = pass_sync(bad || mine);
+  if (bad && mma_warp && lane == 0) {
+    // after a failure, let the committed MMA groups finish before tensor memory is freed
+    if (n1 > 0) mbar_wait_bounded(mma1, (n1 - 1) & 1);
+    if (n2 > 0) mbar_wait_bounded(mma2, (n2 - 1) & 1);
+  }
   if (!bad) {
-    if (a.ssm_bf16) {  // rounded to bf16 only here, at the write-back
+    if (compute) {
+      if (a.ssm_bf16) {  // rounded to bf16 only here, at the write-back
 #pragma unroll
-      for (int e = 0; e < 64; e += 8) {
-        uint16_t hb[8];
+        for (int e = 0; e < 64; e += 8) {
+          uint16_t hb[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) hb[i] = f2bf(Sr[e + i]);
-        *reinterpret_cast<uint4*>(Sb + e) = pack8(hb);
+          for (int i = 0; i < 8; ++i) hb[i] = f2bf(Sr[e + i]);
+          *reinterpret_cast<uint4*>(Sb + e) = pack8(hb);
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < 64; e += 4)
+          *reinterpret_cast<float4*>(Sg + e) = make_float4(Sr[e], Sr[e + 1], Sr[e + 2], Sr[e + 3]);
       }
-    } else {
-#pragma unroll
-      for (int e = 0; e < 64; e += 4)
-        *reinterpret_cast<float4*>(Sg + e) = make_float4(Sr[e], Sr[e + 1], Sr[e + 2], Sr[e + 3]);
     }
   } else if (tid == 0 && a.err) {
     atomicOr(a.err, GDN_DEVERR_TIMEOUT);
@@ -866,7 +936,7 @@ cudaError_t launch_tc_c(const LayerArgs& a, const PrefillExtra& p, const TcLayou
   e = cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, PassSmem<C>::kBytes);
   if (e != cudaSuccess) return e;
   if (p.before_pass && (e = cudaEventRecord(p.before_pass, s)) != cudaSuccess) return e;
-  k2<<<dim3(p.num_seqs, a.Hv), kThreadsTc, PassSmem<C>::kBytes, s>>>(a, p, seq_ok, chunk_off, wb);
+  k2<<<dim3(p.num_seqs, a.Hv), kPassThreads, PassSmem<C>::kBytes, s>>>(a, p, seq_ok, chunk_off, wb);
   return cudaGetLastError();
 }
 
