@@ -98,9 +98,10 @@ def kernel_source_digest():
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(state="f32"):
+def ncu_traffic(state="f32", batch=None, num_slots=None):
     """Per-launch DRAM bytes of the headline decode kernel (fp32 or bf16 state) from the
-    committed ncu summary, if it was taken on the current kernel source (else None)."""
+    committed ncu summary, if it was taken on the current kernel source and on this
+    workload (rows, slot pool); else None."""
     p = os.path.join(ROOT, "profiles", "decode_traffic.json")
     if not os.path.exists(p):
         return None
@@ -108,7 +109,10 @@ def ncu_traffic(state="f32"):
         j = json.load(f)
     if j.get("source_digest") != kernel_source_digest():
         return None
-    return j.get("launches", {}).get(state)
+    e = j.get("launches", {}).get(state)
+    if e is None or e.get("batch") != batch or e.get("num_slots") != num_slots:
+        return None
+    return e
 
 
 def aggregate_ranks(mean_ms: float, bytes_per_rank: int, world: int, device=None):
@@ -467,7 +471,7 @@ def run_ours(args, rank, world):
         return None
     peak, peak_kind = load_peaks()
     achieved = nbytes / (mean_ms * 1e-3) / 1e9
-    traffic = ncu_traffic("bf16" if args.state_bf16 else "f32")
+    traffic = ncu_traffic("bf16" if args.state_bf16 else "f32", args.batch, args.num_slots)
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(mean_ms, 5),
