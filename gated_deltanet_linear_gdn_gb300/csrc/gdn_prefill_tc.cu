@@ -98,6 +98,12 @@ struct TcBufs {
   size_t q_tile, w_tile, p_tile;
 };
 
+// Byte offset of O(t, col) (token t, dv column col) in the pass kernel's bf16 output tile
+// [C x 128]: the 16-byte pieces of a token row are XOR-swizzled by t & 7
+__device__ __forceinline__ uint32_t out_tile_offset(int t, int col) {
+  return static_cast<uint32_t>(t * 256 + (((col >> 3) ^ (t & 7)) << 4) + (col & 7) * 2);
+}
+
 // Byte offset of U^T(r, t) (state row r, token t of the chunk) in a U tile. The tile is
 // the byte image of the pass kernel's two bf16 [128 x C] D' operand tiles (hi, then lo):
 // tokens t..t+3 of an 8-token group sit where the hi tile holds (r, group), t+4..t+7
@@ -531,7 +537,7 @@ struct PassSmem {
   static constexpr int oWh = oEl + kD_, oQ = oWh + kW, oWl = oQ + kW;
   static constexpr int oPh = oWl + kW, oPl = oPh + kP, oKt = oPl + kP;
   static constexpr int oVec = oKt + kD_;        // two vec buffers of kVecFloats
-  static constexpr int oO = oVec + 2 * kVecFloats * 4;  // bf16 output tile [C x 128]
+  static constexpr int oO = oVec + 2 * kVecFloats * 4;  // bf16 output tile [C x 128], swizzled
   static constexpr int kBytes = oO + C * 128 * 2;
   static_assert(kBytes <= 227 * 1024, "pass shared memory exceeds the per-CTA limit");
 };
@@ -543,7 +549,7 @@ __global__ void __launch_bounds__(kPassThreads, 1)
   using S = PassSmem<C>;
   extern __shared__ __align__(1024) unsigned char sm[];
   __shared__ uint32_t s_tmem;
-  __shared__ __align__(8) uint64_t s_bar[5];  // fullA, fullB, mma1, mma2, fullU
+  __shared__ __align__(8) uint64_t s_bar[6];  // fullA, fullB, mma1, mma2, fullU, oDone
 
   const int i = blockIdx.x, h = blockIdx.y;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -568,6 +574,10 @@ __global__ void __launch_bounds__(kPassThreads, 1)
   const uint32_t fullA = smem_addr(&s_bar[0]), fullB = smem_addr(&s_bar[1]);
   const uint32_t mma1 = smem_addr(&s_bar[2]), mma2 = smem_addr(&s_bar[3]);
   const uint32_t fullU = smem_addr(&s_bar[4]);
+  // oDone: every compute warp has finished chunk it's output (and with vec[it & 1]); the
+  // copy warp's own arrival for a phase comes only after it has seen the one before, so
+  // no warp's arrivals can run into the next phase
+  const uint32_t oDone = smem_addr(&s_bar[5]);
   const size_t wtile = wb.w_tile, ptile = wb.p_tile;
 
   // W hi/lo, q tile, vec of chunk c0 + it on one fullA phase (group 1's operands, and vec)
@@ -602,6 +612,7 @@ __global__ void __launch_bounds__(kPassThreads, 1)
   if (warp == 0) tc::tmem_alloc(&s_tmem, kTmemCols);
   if (copy_warp && lane == 0) {
     for (int k = 0; k < 5; ++k) mbar_init(smem_addr(&s_bar[k]), 1);
+    mbar_init(oDone, kThreadsTc / 32 + 1);
     fence_mbar_init();
     if (nch > 0) { issue_A(0); issue_B(0); issue_U(0); }
   }
@@ -644,8 +655,9 @@ __global__ void __launch_bounds__(kPassThreads, 1)
   bool bad = tc_sync(false);
   bool mine = false;  // this thread's wait failure, reported at the next CTA barrier
   const uint32_t tb = s_tmem;
-  // tensor-memory columns: D^T raw [0, C), O1^T [C, 2C), O2^T [128, 128 + C),
-  // state update [256, 384)
+  // tensor-memory columns: D^T raw and O1^T at [base, base + C) and [base + C, base + 2C),
+  // base = 0 for even chunks and 384 for odd ones (chunk it's O1 is read while group 1 of
+  // chunk it + 1 runs); O2^T [128, 128 + C); state update [256, 384)
   constexpr int NH = C / 2;
   constexpr int KS = C / 16;
   // operand descriptors are fixed per CTA; a K step adds 256 bytes (16 units) to the start
@@ -667,12 +679,13 @@ __global__ void __launch_bounds__(kPassThreads, 1)
   // the D^T columns and S Q^T (= O1^T, both S parts) into the next C; S_hi W_lo^T completes D
   auto issue_mma1 = [&](int it) -> bool {
     if (!mbar_wait_bounded(fullA, it & 1)) return false;
+    const uint32_t t1 = tb + ((it & 1) ? 384 : 0);
 #pragma unroll
-    for (int ks = 0; ks < 8; ++ks) tc::mma_bf16(tb, dSh + 16 * ks, dWh + 16 * ks, id2C, ks > 0);
+    for (int ks = 0; ks < 8; ++ks) tc::mma_bf16(t1, dSh + 16 * ks, dWh + 16 * ks, id2C, ks > 0);
 #pragma unroll
-    for (int ks = 0; ks < 8; ++ks) tc::mma_bf16(tb, dSl + 16 * ks, dWh + 16 * ks, id2C, 1);
+    for (int ks = 0; ks < 8; ++ks) tc::mma_bf16(t1, dSl + 16 * ks, dWh + 16 * ks, id2C, 1);
 #pragma unroll
-    for (int ks = 0; ks < 8; ++ks) tc::mma_bf16(tb, dSh + 16 * ks, dWl + 16 * ks, idC, 1);
+    for (int ks = 0; ks < 8; ++ks) tc::mma_bf16(t1, dSh + 16 * ks, dWl + 16 * ks, idC, 1);
     tc::mma_commit(mma1);
     return true;
   };
@@ -693,26 +706,41 @@ __global__ void __launch_bounds__(kPassThreads, 1)
     bulk_prefetch_l2(wb.Kt + ck * wb.q_tile, static_cast<uint32_t>(wb.q_tile));
   };
   if (copy_warp) {
-    // chunk it + 1's tiles as soon as chunk it's MMA groups release their buffers: W, q,
-    // vec after group 1; P, k^T and U (onto the D' tiles) after group 2. fullA / fullB /
-    // fullU of chunk it + 1 are armed only after this warp has seen group 1 / 2 of chunk it
-    // complete, so no parity wait can alias a later phase
+    // each chunk's tiles as soon as their buffers are free: P, k^T and U (onto the D'
+    // tiles) of chunk it + 1 once group 2 of chunk it is done; W, q and vec of chunk it + 2
+    // once group 1 of chunk it + 1 is done and every compute warp has finished chunk it's
+    // output (vec[it & 1]). Each barrier of a chunk is armed only after this warp has seen
+    // the phase it waits on for the chunk before, so no parity wait can alias a later phase
     bool ok = !bad;
     if (lane == 0 && ok && nch > 0) {
       int nA = 1, nBU = 1;  // phases issued (chunk 0's at set-up)
       if (nch > 1) prefetch_chunk(1);
-      for (int it = 0; it + 1 < nch; ++it) {
+      mbar_arrive(oDone);  // this warp's share of phase 0
+      if (nch > 1) {
+        if (mbar_wait_bounded(mma1, 0)) {
+          tc::fence_after_sync();
+          issue_A(1);
+          nA = 2;
+        } else {
+          ok = false;
+        }
+      }
+      for (int it = 0; ok && it + 1 < nch; ++it) {
         const uint32_t par = it & 1;
         if (it + 2 < nch) prefetch_chunk(it + 2);  // two chunks ahead
-        if (!mbar_wait_bounded(mma1, par)) { ok = false; break; }
-        tc::fence_after_sync();
-        issue_A(it + 1);
-        nA = it + 2;
         if (!mbar_wait_bounded(mma2, par)) { ok = false; break; }
         tc::fence_after_sync();
         issue_B(it + 1);
         issue_U(it + 1);
         nBU = it + 2;
+        if (it + 2 < nch) {
+          if (!mbar_wait_bounded(oDone, par)) { ok = false; break; }
+          mbar_arrive(oDone);  // share of phase it + 1
+          if (!mbar_wait_bounded(mma1, par ^ 1)) { ok = false; break; }
+          tc::fence_after_sync();
+          issue_A(it + 2);
+          nA = it + 3;
+        }
       }
       if (!ok) {
         if (a.err) atomicOr(a.err, GDN_DEVERR_TIMEOUT);
@@ -731,7 +759,7 @@ __global__ void __launch_bounds__(kPassThreads, 1)
     const int L = min(C, eos - t0);
     const uint32_t par = it & 1;
     const float* vec = reinterpret_cast<const float*>(sm + S::oVec + par * kVecFloats * 4);
-    float Ov[NH];
+    const int base = par ? 384 : 0;  // chunk it's D^T / O1^T columns
     if (compute) {
       if (!mbar_wait_bounded(mma1, par)) mine = true;
       if (!mbar_wait_bounded(fullU, par)) mine = true;
@@ -744,13 +772,13 @@ __global__ void __launch_bounds__(kPassThreads, 1)
 #pragma unroll
           for (int b0 = 0; b0 < NH; b0 += 16) {
             float tv[16];
-            tmem_load<16>(tc::taddr(tb, 32 * q, half * NH + b0), tv);
+            tmem_load<16>(tc::taddr(tb, 32 * q, base + half * NH + b0), tv);
 #pragma unroll
             for (int e = 0; e < 16; ++e) raw[b0 + e] = tv[e];
           }
         } else {
           float tv[8];
-          tmem_load<8>(tc::taddr(tb, 32 * q, half * NH), tv);
+          tmem_load<8>(tc::taddr(tb, 32 * q, base + half * NH), tv);
 #pragma unroll
           for (int e = 0; e < 8; ++e) raw[e] = tv[e];
         }
@@ -807,32 +835,6 @@ __global__ void __launch_bounds__(kPassThreads, 1)
       mine = __any_sync(0xffffffffu, mine);  // warp-uniform before the aligned loads
       tc::fence_after_sync();
       if (!mine) {
-        // O = f_t O1 + O2 into registers (stored below, while the next chunk's MMAs run)
-        float o1[NH], o2[NH];
-        if constexpr (NH >= 16) {
-#pragma unroll
-          for (int b0 = 0; b0 < NH; b0 += 16) {
-            float ta[16], tbv[16];
-            tmem_load<16>(tc::taddr(tb, 32 * q, C + half * NH + b0), ta);
-            tmem_load<16>(tc::taddr(tb, 32 * q, 128 + half * NH + b0), tbv);
-#pragma unroll
-            for (int e = 0; e < 16; ++e) { o1[b0 + e] = ta[e]; o2[b0 + e] = tbv[e]; }
-          }
-        } else {
-          float ta[8], tbv[8];
-          tmem_load<8>(tc::taddr(tb, 32 * q, C + half * NH), ta);
-          tmem_load<8>(tc::taddr(tb, 32 * q, 128 + half * NH), tbv);
-#pragma unroll
-          for (int e = 0; e < 8; ++e) { o1[e] = ta[e]; o2[e] = tbv[e]; }
-        }
-        tc::tmem_wait_ld();
-#pragma unroll
-        for (int e = 0; e < NH; ++e) Ov[e] = fmaf(vec[half * NH + e], o1[e], o2[e]);
-        if (!a.out_f32) {  // bf16 output: stage the tile [token][dv] for 16-byte stores below
-          uint16_t* ot = reinterpret_cast<uint16_t*>(sm + S::oO);
-#pragma unroll
-          for (int e = 0; e < NH; ++e) ot[(half * NH + e) * kD + r] = f2bf(Ov[e]);
-        }
         // S <- g_last S + update, 16 columns at a time
         const float gl = vec[128];
 #pragma unroll
@@ -857,22 +859,57 @@ __global__ void __launch_bounds__(kPassThreads, 1)
         mine = !issue_mma1(it + 1);
         if (!mine) n1 = it + 2;
       }
-    } else if (a.out_f32) {
-#pragma unroll
-      for (int e = 0; e < NH; ++e) {
-        const int tt = half * NH + e;
-        if (tt < L)
-          static_cast<float*>(a.out)[(static_cast<int64_t>(t0 + tt) * a.Hv + h) * kD + r] = Ov[e];
-      }
     } else {
-      // the compute warps copy the staged tile out in 16-byte pieces while the MMA warp
-      // issues the next chunk's MMAs (the tile is rewritten only after the next barrier)
-      const uint4* ot = reinterpret_cast<const uint4*>(sm + S::oO);
-      for (int k = tid; k < L * (kD / 8); k += kThreadsTc) {
-        const int tt = k / (kD / 8), col = (k % (kD / 8)) * 8;
-        *reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.out) +
-                                  (static_cast<int64_t>(t0 + tt) * a.Hv + h) * kD + col) = ot[k];
+      // chunk it's output O = f_t O1 + O2, while group 1 of chunk it + 1 runs
+      float o1[NH], o2[NH];
+      if constexpr (NH >= 16) {
+#pragma unroll
+        for (int b0 = 0; b0 < NH; b0 += 16) {
+          float ta[16], tbv[16];
+          tmem_load<16>(tc::taddr(tb, 32 * q, base + C + half * NH + b0), ta);
+          tmem_load<16>(tc::taddr(tb, 32 * q, 128 + half * NH + b0), tbv);
+#pragma unroll
+          for (int e = 0; e < 16; ++e) { o1[b0 + e] = ta[e]; o2[b0 + e] = tbv[e]; }
+        }
+      } else {
+        float ta[8], tbv[8];
+        tmem_load<8>(tc::taddr(tb, 32 * q, base + C + half * NH), ta);
+        tmem_load<8>(tc::taddr(tb, 32 * q, 128 + half * NH), tbv);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) { o1[e] = ta[e]; o2[e] = tbv[e]; }
       }
+      tc::tmem_wait_ld();
+      if (a.out_f32) {
+#pragma unroll
+        for (int e = 0; e < NH; ++e) {
+          const int tt = half * NH + e;
+          if (tt < L)
+            static_cast<float*>(a.out)[(static_cast<int64_t>(t0 + tt) * a.Hv + h) * kD + r] =
+                fmaf(vec[tt], o1[e], o2[e]);
+        }
+      } else {
+        // stage the warp's [NH tokens x 32 dv] block in the bf16 tile, then copy it out in
+        // 16-byte pieces; the tile's 16-byte pieces are XOR-swizzled by token so both the
+        // 2-byte writes and the 16-byte reads are free of bank conflicts
+        unsigned char* ot = sm + S::oO;
+#pragma unroll
+        for (int e = 0; e < NH; ++e) {
+          const int tt = half * NH + e;
+          *reinterpret_cast<uint16_t*>(ot + out_tile_offset(tt, r)) = f2bf(fmaf(vec[tt], o1[e], o2[e]));
+        }
+        __syncwarp();
+#pragma unroll
+        for (int k = 0; k < NH / 8; ++k) {
+          const int pc = lane + 32 * k;
+          const int tt = half * NH + pc / 4, col = 32 * q + (pc % 4) * 8;
+          if (tt < L)
+            *reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.out) +
+                                      (static_cast<int64_t>(t0 + tt) * a.Hv + h) * kD + col) =
+                *reinterpret_cast<const uint4*>(ot + out_tile_offset(tt, col));
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(oDone);  // this warp is done with chunk it's output and vec
     }
   }
   if (!copy_warp) bad = pass_sync(bad || mine);
