@@ -68,7 +68,7 @@ TcLayout tc_layout(int T, int N, int Hk, int Hv, int C, int D) {
   TcLayout L;
   const int64_t mc = (static_cast<int64_t>(T) + static_cast<int64_t>(N) * (C - 1)) / C;
   L.max_chunks = static_cast<int>(mc);
-  L.q_tile = static_cast<size_t>(C) * kD * 2;  // bf16 [C x 128] (also K^T [128 x C])
+  L.q_tile = static_cast<size_t>(C) * kD * 2;  // bf16 [C x 128] (q and k tiles)
   L.w_tile = static_cast<size_t>(C) * kD * 2;  // one of hi / lo
   L.p_tile = static_cast<size_t>(C) * C * 2;   // one of hi / lo
   L.u_tile = static_cast<size_t>(kD) * C * 4;  // fp32 U^T [128 x C]
@@ -90,7 +90,7 @@ TcLayout tc_layout(int T, int N, int Hk, int Hv, int C, int D) {
 
 struct TcBufs {
   unsigned char* Qt;  // [chunk][Hk] bf16 q tile, K-major [C x 128]
-  unsigned char* Kt;  // [chunk][Hk] bf16 k^T tile, K-major [128 x C]
+  unsigned char* Kt;  // [chunk][Hk] bf16 k tile [C x 128], the q tile's layout (MN-major use)
   unsigned char* Wt;  // [chunk][Hv][hi, lo] bf16 W tile, K-major [C x 128]
   unsigned char* Pt;  // [chunk][Hv][hi, lo] bf16 P tile, K-major [C x C]
   float* Ut;          // [chunk][Hv] fp32 U^T [128 x C], laid out by u_image_offset
@@ -126,24 +126,6 @@ __device__ __forceinline__ void split8(const float (&x)[8], uint4& hi, uint4& lo
   }
   hi = make_uint4(h[0], h[1], h[2], h[3]);
   lo = make_uint4(l[0], l[1], l[2], l[3]);
-}
-
-// 8 rows x 8 bf16 (one uint4 per row) -> 8 columns (one uint4 per column)
-__device__ __forceinline__ void transpose8x8(const uint4 (&in)[8], uint4 (&out)[8]) {
-  uint16_t m[8][8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const uint16_t* p = reinterpret_cast<const uint16_t*>(&in[i]);
-#pragma unroll
-    for (int j = 0; j < 8; ++j) m[i][j] = p[j];
-  }
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    uint16_t col[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) col[i] = m[i][j];
-    out[j] = pack8(col);
-  }
 }
 
 template <int N>
@@ -183,13 +165,19 @@ template <int C>
 struct IntraSmem {
   static constexpr int CPC = 128 / C;                // chunks per CTA
   static constexpr int kTile = 128 * 128 * 2;        // bf16 [128 x 128]
-  // phase 1: sQ, sK (MMA operands), sKtw (k^T tiles for the workspace)
-  // phase 2: sKh, sKl (alias sQ, sK), sTh (aliases sKtw), sTl, sVt, sA
-  static constexpr int oQ = 0, oK = kTile, oKtw = 2 * kTile;
-  static constexpr int oTh = 2 * kTile, oTl = 3 * kTile, oVt = 4 * kTile;
-  static constexpr int oA = 5 * kTile;               // fp32 [128][C+1]
+  // phase 1: sQ, sK: the raw q, k rows [128 tokens x 128] (K-major operands of the Gram
+  //          and QK^T products)
+  // phase 2: sK stays; sKh (aliases sQ) and sKl hold K' hi / lo, sV the V rows -- all three
+  //          MN-major operands over tokens in the same layout -- sTh / sTl the T' operand, sA
+  static constexpr int oQ = 0, oK = kTile, oKl = 2 * kTile;
+  static constexpr int oTh = 3 * kTile, oTl = 4 * kTile, oV = 5 * kTile;
+  static constexpr int oA = 6 * kTile;               // fp32 [128][C+1]
   static constexpr int oVec = oA + 128 * (C + 1) * 4;  // iq, ik, g/G, beta: 4 x 128 floats
-  static constexpr int kBytes = oVec + 4 * 128 * 4;
+  // the mbarrier, the tensor-memory base and the chunk table live here too: static shared
+  // variables would be padded to 1 KB ahead of the 1 KB-aligned dynamic block
+  static constexpr int oBar = oVec + 4 * 128 * 4, oTmem = oBar + 8, oT0 = oTmem + 8;
+  static constexpr int kBytes = oT0 + 2 * CPC * 4;
+  static_assert(kBytes <= 227 * 1024, "intra shared memory exceeds the per-CTA limit");
 };
 
 template <int C>
@@ -205,9 +193,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   float* s_ik = s_iq + 128;
   float* s_G = s_ik + 128;
   float* s_beta = s_G + 128;
-  __shared__ int s_t0[CPC], s_L[CPC];
-  __shared__ uint32_t s_tmem;
-  __shared__ __align__(8) uint64_t s_bar;
+  int* s_t0 = reinterpret_cast<int*>(sm + S::oT0);
+  int* s_L = s_t0 + CPC;
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(sm + S::oTmem);
+  const uint32_t bar = smem_addr(sm + S::oBar);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int kh = blockIdx.y;
@@ -249,13 +238,13 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     const float inv = a.qk_l2norm ? 1.0f / sqrtf(ss + 1e-6f) : 1.0f;
     (which ? s_ik : s_iq)[tok] = inv;
   }
-  if (warp == 0) tc::tmem_alloc(&s_tmem, kTmemCols);
+  if (warp == 0) tc::tmem_alloc(s_tmem, kTmemCols);
   if (tid == 0) {
-    mbar_init(smem_addr(&s_bar), 1);
+    mbar_init(bar, 1);
     fence_mbar_init();
   }
   tc_sync(false);
-  const uint32_t tb = s_tmem;
+  const uint32_t tb = *s_tmem;
   uint32_t phase = 0;
   bool bad = false;
 
@@ -266,29 +255,16 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       tc::mma_bf16(tb, tc::kmajor_desc(ak, kD, ks), tc::kmajor_desc(ak, kD, ks), id, ks > 0);
     for (int ks = 0; ks < kD / 16; ++ks)
       tc::mma_bf16(tb + 128, tc::kmajor_desc(aq, kD, ks), tc::kmajor_desc(ak, kD, ks), id, ks > 0);
-    tc::mma_commit(smem_addr(&s_bar));
+    tc::mma_commit(bar);
   }
-  {  // k^T tiles per chunk: one 8 token x 8 channel block per thread, transposed
-    const int tg = tid >> 4, cg = tid & 15;
-    uint4 in[8], out[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-      in[i] = *reinterpret_cast<const uint4*>(sm + S::oK + tc::kmajor_offset(8 * tg + i, 8 * cg, kD));
-    transpose8x8(in, out);
-    const int ci = (8 * tg) / C, tl0 = (8 * tg) % C;
-    unsigned char* kt = sm + S::oKtw + ci * (kD * C * 2);
-#pragma unroll
-    for (int j = 0; j < 8; ++j)
-      *reinterpret_cast<uint4*>(kt + tc::kmajor_offset(8 * cg + j, tl0, C)) = out[j];
-  }
-  __syncthreads();
-  // q and k^T tiles of each chunk -> workspace (read-only use of the smem tiles)
+  // q and k tiles of each chunk -> workspace (read-only use of the smem tiles; a chunk's
+  // rows are one contiguous slice of either tile)
   for (int ci = 0; ci < CPC; ++ci) {
     const int c = c_first + ci;
     if (c >= nchunks) break;
     const size_t slice = static_cast<size_t>(C) * kD * 2;  // bytes of one chunk's tile
     const uint4* srcq = reinterpret_cast<const uint4*>(sm + S::oQ + ci * slice);
-    const uint4* srck = reinterpret_cast<const uint4*>(sm + S::oKtw + ci * slice);
+    const uint4* srck = reinterpret_cast<const uint4*>(sm + S::oK + ci * slice);
     uint4* dq = reinterpret_cast<uint4*>(wb.Qt + (static_cast<size_t>(c) * a.Hk + kh) * wb.q_tile);
     uint4* dk = reinterpret_cast<uint4*>(wb.Kt + (static_cast<size_t>(c) * a.Hk + kh) * wb.q_tile);
     for (int i = tid; i < static_cast<int>(slice / 16); i += kThreadsTc) {
@@ -296,7 +272,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       dk[i] = srck[i];
     }
   }
-  if (!mbar_wait_bounded(smem_addr(&s_bar), phase)) bad = true;
+  if (!mbar_wait_bounded(bar, phase)) bad = true;
   phase ^= 1;
   bad = tc_sync(bad);
 
@@ -372,6 +348,9 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         sA[t * (C + 1) + j] = (j < tl) ? bt * dec * ikt * s_ik[tj] * gv[e] : 0.0f;
         pv[e] = dec * iqt * s_ik[tj] * qv[e];
       }
+      // the token's K' scale e^{G_t} ik_t, kept in A's spare padding column (the solve reads
+      // columns 0 .. C-1 only)
+      if (half == 0) sA[t * (C + 1) + C] = live ? expf(Gt) * ikt : 0.0f;
       if (c < nchunks) {
         unsigned char* ph = wb.Pt + (static_cast<size_t>(c) * a.Hv + h) * 2 * wb.p_tile;
 #pragma unroll
@@ -422,62 +401,59 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         *reinterpret_cast<uint16_t*>(sm + S::oTl + o) = lo;
       }
     } else {
-      // V^T (raw bf16) and K'^T = (diag(e^G ik) K)^T (split) as [128 x 128 tokens]
-      // operands: 16-byte row loads of 8 tokens x 8 channels, transposed in registers
+      // V (raw bf16) and K' = diag(e^G ik) K (split) as MN-major operands over the 128
+      // tokens, in the k tile's layout: 16-byte pieces of 8 channels of one token. A thread
+      // takes channel group cg of tokens 8i + (u & 7), i = 0..15: the 8 lanes sharing cg hold
+      // 8 consecutive tokens, so each 16-byte store hits its own bank group. All 16 V loads
+      // are issued before the first store
       const int u = tid - 128;
-      const int vc = 2 * a.Hk * kD + h * kD, kc = (a.Hk + kh) * kD;
-      for (int blk = u; blk < 256; blk += 128) {
-        const int tg = blk >> 4, cg = blk & 15;
-        uint4 vin[8], kin[8];
-        float sc[8];
+      const int cg = (u >> 3) & 15, tr = u & 7;
+      const uint16_t* yv = y + 2 * a.Hk * kD + h * kD + 8 * cg;
+      uint4 vb[16];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int tok = 8 * tg + i, ci = tok / C, tl = tok % C;
-          const bool valid = tl < s_L[ci];
-          const uint16_t* rowp = y + static_cast<int64_t>(s_t0[ci] + tl) * a.D;
-          vin[i] = valid ? __ldg(reinterpret_cast<const uint4*>(rowp + vc) + cg) : make_uint4(0u, 0u, 0u, 0u);
-          kin[i] = valid ? __ldg(reinterpret_cast<const uint4*>(rowp + kc) + cg) : make_uint4(0u, 0u, 0u, 0u);
-          sc[i] = valid ? expf(s_G[tok]) * s_ik[tok] : 0.0f;
-        }
-        uint4 vt[8], kt[8];
-        transpose8x8(vin, vt);
-        transpose8x8(kin, kt);
+      for (int i = 0; i < 16; ++i) {
+        const int tok = 8 * i + tr, ci = tok / C, tl = tok % C;
+        vb[i] = tl < s_L[ci]
+                    ? __ldg(reinterpret_cast<const uint4*>(yv + static_cast<int64_t>(s_t0[ci] + tl) * a.D))
+                    : make_uint4(0u, 0u, 0u, 0u);
+      }
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const uint32_t o = tc::kmajor_offset(8 * cg + j, 8 * tg, 128);
-          *reinterpret_cast<uint4*>(sm + S::oVt + o) = vt[j];
-          float kx[8];
-          unpack8(kt[j], kx);
+      for (int i = 0; i < 16; ++i) {
+        const int tok = 8 * i + tr;
+        const uint32_t o = tc::kmajor_offset(tok, 8 * cg, kD);
+        *reinterpret_cast<uint4*>(sm + S::oV + o) = vb[i];
+        const float sc = sA[tok * (C + 1) + C];
+        float kx[8];
+        unpack8(*reinterpret_cast<const uint4*>(sm + S::oK + o), kx);
 #pragma unroll
-          for (int i = 0; i < 8; ++i) kx[i] *= sc[i];
-          uint4 hi, lo;
-          split8(kx, hi, lo);
-          *reinterpret_cast<uint4*>(sm + S::oQ + o) = hi;  // sKh (aliases sQ)
-          *reinterpret_cast<uint4*>(sm + S::oK + o) = lo;  // sKl (aliases sK)
-        }
+        for (int e = 0; e < 8; ++e) kx[e] *= sc;
+        uint4 hi, lo;
+        split8(kx, hi, lo);
+        *reinterpret_cast<uint4*>(sm + S::oQ + o) = hi;  // sKh (aliases sQ)
+        *reinterpret_cast<uint4*>(sm + S::oKl + o) = lo;
       }
     }
     bad = tc_sync(bad);
     if (bad) break;
 
-    if (tid == 0) {  // U = T' V (cols 256..383), W = T' K' (cols 384..511)
-      const uint32_t id = tc::idesc_bf16_f32(128, 128);
+    if (tid == 0) {  // U = T' V (cols 256..383), W = T' K' (cols 384..511); B MN-major
+      const uint32_t id = tc::idesc_bf16_f32_bmn(128, 128);
       const uint32_t th = smem_addr(sm + S::oTh), tl = smem_addr(sm + S::oTl);
-      const uint32_t vt = smem_addr(sm + S::oVt);
-      const uint32_t kh_ = smem_addr(sm + S::oQ), kl = smem_addr(sm + S::oK);
+      const uint32_t v = smem_addr(sm + S::oV);
+      const uint32_t kh_ = smem_addr(sm + S::oQ), kl = smem_addr(sm + S::oKl);
       for (int ks = 0; ks < 8; ++ks)
-        tc::mma_bf16(tb + 256, tc::kmajor_desc(th, 128, ks), tc::kmajor_desc(vt, 128, ks), id, ks > 0);
+        tc::mma_bf16(tb + 256, tc::kmajor_desc(th, 128, ks), tc::mnmajor_desc(v, 128, ks), id, ks > 0);
       for (int ks = 0; ks < 8; ++ks)
-        tc::mma_bf16(tb + 256, tc::kmajor_desc(tl, 128, ks), tc::kmajor_desc(vt, 128, ks), id, 1);
+        tc::mma_bf16(tb + 256, tc::kmajor_desc(tl, 128, ks), tc::mnmajor_desc(v, 128, ks), id, 1);
       for (int ks = 0; ks < 8; ++ks)
-        tc::mma_bf16(tb + 384, tc::kmajor_desc(th, 128, ks), tc::kmajor_desc(kh_, 128, ks), id, ks > 0);
+        tc::mma_bf16(tb + 384, tc::kmajor_desc(th, 128, ks), tc::mnmajor_desc(kh_, 128, ks), id, ks > 0);
       for (int ks = 0; ks < 8; ++ks)
-        tc::mma_bf16(tb + 384, tc::kmajor_desc(th, 128, ks), tc::kmajor_desc(kl, 128, ks), id, 1);
+        tc::mma_bf16(tb + 384, tc::kmajor_desc(th, 128, ks), tc::mnmajor_desc(kl, 128, ks), id, 1);
       for (int ks = 0; ks < 8; ++ks)
-        tc::mma_bf16(tb + 384, tc::kmajor_desc(tl, 128, ks), tc::kmajor_desc(kh_, 128, ks), id, 1);
-      tc::mma_commit(smem_addr(&s_bar));
+        tc::mma_bf16(tb + 384, tc::kmajor_desc(tl, 128, ks), tc::mnmajor_desc(kh_, 128, ks), id, 1);
+      tc::mma_commit(bar);
     }
-    if (!mbar_wait_bounded(smem_addr(&s_bar), phase)) bad = true;
+    if (!mbar_wait_bounded(bar, phase)) bad = true;
     bad = __any_sync(0xffffffffu, bad);  // warp-uniform before the aligned loads
     phase ^= 1;
     tc::fence_after_sync();
@@ -671,9 +647,9 @@ __global__ void __launch_bounds__(kPassThreads, 1)
   const uint64_t dEl = tc::kmajor_desc(smem_addr(sm + S::oEl), C, 0);
   const uint64_t dPh = tc::kmajor_desc(smem_addr(sm + S::oPh), C, 0);
   const uint64_t dPl = tc::kmajor_desc(smem_addr(sm + S::oPl), C, 0);
-  const uint64_t dKt = tc::kmajor_desc(smem_addr(sm + S::oKt), C, 0);
+  const uint64_t dKt = tc::mnmajor_desc(smem_addr(sm + S::oKt), 128, 0);  // k tile, MN-major
   const uint32_t idC = tc::idesc_bf16_f32(128, C), id2C = tc::idesc_bf16_f32(128, 2 * C);
-  const uint32_t id128 = tc::idesc_bf16_f32(128, 128);
+  const uint32_t id128m = tc::idesc_bf16_f32_bmn(128, 128);
 
   // MMA group 1 of chunk `it` (the MMA warp): S [W_hi | Q]^T over N = 2C puts S W_hi^T into
   // the D^T columns and S Q^T (= O1^T, both S parts) into the next C; S_hi W_lo^T completes D
@@ -820,10 +796,10 @@ __global__ void __launch_bounds__(kPassThreads, 1)
 #pragma unroll
           for (int ks = 0; ks < KS; ++ks) tc::mma_bf16(tb + 128, dDl + 16 * ks, dPh + 16 * ks, idC, 1);
 #pragma unroll
-          for (int ks = 0; ks < KS; ++ks)
-            tc::mma_bf16(tb + 256, dEh + 16 * ks, dKt + 16 * ks, id128, ks > 0);
+          for (int ks = 0; ks < KS; ++ks)  // a K step of the MN-major k tile: 4096 bytes (256 units)
+            tc::mma_bf16(tb + 256, dEh + 16 * ks, dKt + 256 * ks, id128m, ks > 0);
 #pragma unroll
-          for (int ks = 0; ks < KS; ++ks) tc::mma_bf16(tb + 256, dEl + 16 * ks, dKt + 16 * ks, id128, 1);
+          for (int ks = 0; ks < KS; ++ks) tc::mma_bf16(tb + 256, dEl + 16 * ks, dKt + 256 * ks, id128m, 1);
           tc::mma_commit(mma2);
           n2 = it + 1;
         } else {

@@ -46,6 +46,16 @@ __device__ __forceinline__ uint64_t kmajor_desc(uint32_t tile_saddr, int K, int 
   return smem_desc(tile_saddr + static_cast<uint32_t>(ks) * 256u, 128u, static_cast<uint32_t>(K) * 16u);
 }
 
+// Descriptor of the K-step `ks` (16 K-rows) of an MN-major tile [K x N] stored in the K-major
+// tile layout with the roles swapped: element (k, n) at kmajor_offset(k, n, N), i.e. core
+// matrices of 8 K-rows x 16 bytes of N, 128 bytes apart along N and N*16 bytes apart along K.
+// For an MN-major operand (no swizzle) the leading byte offset is the K stride and the
+// stride byte offset the N stride (checked against exact integer products before use).
+__device__ __forceinline__ uint64_t mnmajor_desc(uint32_t tile_saddr, int N, int ks) {
+  return smem_desc(tile_saddr + static_cast<uint32_t>(ks) * 32u * static_cast<uint32_t>(N),
+                   static_cast<uint32_t>(N) * 16u, 128u);
+}
+
 // Instruction descriptor, kind::f16: bf16 A and B (both K-major), fp32 D.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
   return (1u << 4)                                   // D format: f32
@@ -53,6 +63,10 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
          | (1u << 10)                                // B format: bf16
          | (static_cast<uint32_t>(N >> 3) << 17)     // N / 8
          | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
+}
+// The same with an MN-major B operand (bit 16: B transposed).
+__host__ __device__ constexpr uint32_t idesc_bf16_f32_bmn(int M, int N) {
+  return idesc_bf16_f32(M, N) | (1u << 16);
 }
 
 // --- tensor memory allocation (executed by one whole warp) ---
