@@ -436,15 +436,18 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     bad = tc_sync(bad);
     if (bad) break;
 
-    if (tid == 0) {  // U = T' V (cols 256..383), W = T' K' (cols 384..511); B MN-major
+    if (tid == 0) {
+      // U^T = V^T T'^T (cols 256..383: a dv row per lane, a token per column), A = V MN-major;
+      // W = T' K' (cols 384..511: a token per lane), B = K' MN-major
+      const uint32_t idu = tc::idesc_bf16_f32_amn(128, 128);
       const uint32_t id = tc::idesc_bf16_f32_bmn(128, 128);
       const uint32_t th = smem_addr(sm + S::oTh), tl = smem_addr(sm + S::oTl);
       const uint32_t v = smem_addr(sm + S::oV);
       const uint32_t kh_ = smem_addr(sm + S::oQ), kl = smem_addr(sm + S::oKl);
       for (int ks = 0; ks < 8; ++ks)
-        tc::mma_bf16(tb + 256, tc::kmajor_desc(th, 128, ks), tc::mnmajor_desc(v, 128, ks), id, ks > 0);
+        tc::mma_bf16(tb + 256, tc::mnmajor_desc(v, 128, ks), tc::kmajor_desc(th, 128, ks), idu, ks > 0);
       for (int ks = 0; ks < 8; ++ks)
-        tc::mma_bf16(tb + 256, tc::kmajor_desc(tl, 128, ks), tc::mnmajor_desc(v, 128, ks), id, 1);
+        tc::mma_bf16(tb + 256, tc::mnmajor_desc(v, 128, ks), tc::kmajor_desc(tl, 128, ks), idu, 1);
       for (int ks = 0; ks < 8; ++ks)
         tc::mma_bf16(tb + 384, tc::kmajor_desc(th, 128, ks), tc::mnmajor_desc(kh_, 128, ks), id, ks > 0);
       for (int ks = 0; ks < 8; ++ks)
@@ -458,27 +461,36 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     phase ^= 1;
     tc::fence_after_sync();
     if (!bad) {
-      // U^T -> workspace (fp32 [128 x C] tile image); W -> hi / lo tiles [C x 128]. Every lane
-      // executes the (warp-collective) loads; only rows of existing chunks store.
-      const int t = 32 * (warp & 3) + lane, half = warp >> 2;
+      // U^T -> workspace (fp32 [128 x C] tile image per chunk, 16-byte pieces of a dv row);
+      // W -> hi / lo tiles [C x 128]. Every lane executes the (warp-collective) loads; only
+      // existing chunks store. Lane = dv row r of U^T and token row t of W alike
+      const int r = 32 * (warp & 3) + lane, half = warp >> 2;
+      const int t = r;
       const int ci = t / C, tl = t % C;
       const int c = c_first + ci;
       const bool store = c < nchunks;
       {
-        unsigned char* ut = reinterpret_cast<unsigned char*>(
-            wb.Ut + (static_cast<size_t>(store ? c : 0) * a.Hv + h) * (kD * C));
         unsigned char* wt = wb.Wt + (static_cast<size_t>(store ? c : 0) * a.Hv + h) * 2 * wb.w_tile;
 #pragma unroll 1
         for (int b0 = 0; b0 < 64; b0 += 16) {
           const int col = half * 64 + b0;
           float uv[16], wv[16];
-          tmem_load<16>(tc::taddr(tb, 32 * (warp & 3), 256 + col), uv);
-          tmem_load<16>(tc::taddr(tb, 32 * (warp & 3), 384 + col), wv);
+          tmem_load<16>(tc::taddr(tb, 32 * (warp & 3), 256 + col), uv);  // U^T[r][col ..]
+          tmem_load<16>(tc::taddr(tb, 32 * (warp & 3), 384 + col), wv);  // W[t][col ..]
           tc::tmem_wait_ld();
-          if (!store) continue;
 #pragma unroll
-          for (int e = 0; e < 16; ++e)
-            *reinterpret_cast<float*>(ut + u_image_offset(col + e, tl, C)) = uv[e];
+          for (int g = 0; g < 16; g += 8) {  // 8 tokens of one chunk: two 16-byte image pieces
+            const int T = col + g, cu = c_first + T / C, tu = T % C;
+            if (cu < nchunks) {
+              unsigned char* ub = reinterpret_cast<unsigned char*>(
+                  wb.Ut + (static_cast<size_t>(cu) * a.Hv + h) * (kD * C));
+              *reinterpret_cast<float4*>(ub + u_image_offset(r, tu, C)) =
+                  make_float4(uv[g], uv[g + 1], uv[g + 2], uv[g + 3]);
+              *reinterpret_cast<float4*>(ub + u_image_offset(r, tu + 4, C)) =
+                  make_float4(uv[g + 4], uv[g + 5], uv[g + 6], uv[g + 7]);
+            }
+          }
+          if (!store) continue;
 #pragma unroll
           for (int e8 = 0; e8 < 16; e8 += 8) {
             float x[8];

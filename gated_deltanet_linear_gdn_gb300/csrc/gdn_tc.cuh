@@ -68,6 +68,11 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
 __host__ __device__ constexpr uint32_t idesc_bf16_f32_bmn(int M, int N) {
   return idesc_bf16_f32(M, N) | (1u << 16);
 }
+// The same with an MN-major A operand (bit 15: A transposed); its descriptor takes the same
+// strides as an MN-major B (mnmajor_desc with M in place of N).
+__host__ __device__ constexpr uint32_t idesc_bf16_f32_amn(int M, int N) {
+  return idesc_bf16_f32(M, N) | (1u << 15);
+}
 
 // --- tensor memory allocation (executed by one whole warp) ---
 __device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
