@@ -216,7 +216,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   }
   __syncthreads();
 
-  // ---- phase 1: raw q, k rows -> tensor-core tiles; norms; k^T tiles ----
+  // ---- phase 1: raw q, k rows -> tensor-core tiles; norms ----
   {
     const int tok = tid & 127, which = tid >> 7;  // 0: q, 1: k
     const int ci = tok / C, tl = tok % C;
@@ -523,11 +523,13 @@ struct PassSmem {
   static constexpr int oDh = 2 * kS, oDl = oDh + kD_, oEh = oDl + kD_, oEl = oEh + kD_;
   // the q tile follows the W hi tile: together they are one [2C x 128] MMA operand
   static constexpr int oWh = oEl + kD_, oQ = oWh + kW, oWl = oQ + kW;
-  static constexpr int oPh = oWl + kW, oPl = oPh + kP, oKt = oPl + kP;
-  static constexpr int oVec = oKt + kD_;        // two vec buffers of kVecFloats
+  static constexpr int oPh = oWl + kW, oPl = oPh + kP, oKtile = oPl + kP;  // k tile [C x 128]
+  static constexpr int oVec = oKtile + kD_;     // two vec buffers of kVecFloats
   static constexpr int oO = oVec + 2 * kVecFloats * 4;  // bf16 output tile [C x 128], swizzled
   static constexpr int kBytes = oO + C * 128 * 2;
-  static_assert(kBytes <= 227 * 1024, "pass shared memory exceeds the per-CTA limit");
+  // the kernel's static variables (tensor-memory base, mbarriers) are padded to 1 KB ahead of
+  // the 1 KB-aligned dynamic block
+  static_assert(kBytes + 1024 <= 227 * 1024, "pass shared memory exceeds the per-CTA limit");
 };
 
 template <int C>
@@ -581,7 +583,7 @@ __global__ void __launch_bounds__(kPassThreads, 1)
     bulk_g2s(smem_addr(sm + S::oQ), qt, static_cast<uint32_t>(wb.q_tile), fullA);
     bulk_g2s(smem_addr(sm + S::oVec + (it & 1) * kVecFloats * 4), vec, kVecFloats * 4, fullA);
   };
-  auto issue_B = [&](int it) {  // P hi/lo, k^T tile of chunk c0 + it
+  auto issue_B = [&](int it) {  // P hi/lo, k tile of chunk c0 + it
     const int c = c0 + it;
     const int kh = h / (a.Hv / a.Hk);
     const unsigned char* pp = wb.Pt + (static_cast<size_t>(c) * a.Hv + h) * 2 * ptile;
@@ -589,7 +591,7 @@ __global__ void __launch_bounds__(kPassThreads, 1)
     mbar_arrive_expect_tx(fullB, static_cast<uint32_t>(2 * ptile + wb.q_tile));
     bulk_g2s(smem_addr(sm + S::oPh), pp, static_cast<uint32_t>(ptile), fullB);
     bulk_g2s(smem_addr(sm + S::oPl), pp + ptile, static_cast<uint32_t>(ptile), fullB);
-    bulk_g2s(smem_addr(sm + S::oKt), kt, static_cast<uint32_t>(wb.q_tile), fullB);
+    bulk_g2s(smem_addr(sm + S::oKtile), kt, static_cast<uint32_t>(wb.q_tile), fullB);
   };
   auto issue_U = [&](int it) {  // U^T of chunk c0 + it onto the D' tiles (free once group 2 is done)
     const float* ut = wb.Ut + (static_cast<size_t>(c0 + it) * a.Hv + h) * (kD * C);
@@ -659,7 +661,7 @@ __global__ void __launch_bounds__(kPassThreads, 1)
   const uint64_t dEl = tc::kmajor_desc(smem_addr(sm + S::oEl), C, 0);
   const uint64_t dPh = tc::kmajor_desc(smem_addr(sm + S::oPh), C, 0);
   const uint64_t dPl = tc::kmajor_desc(smem_addr(sm + S::oPl), C, 0);
-  const uint64_t dKt = tc::mnmajor_desc(smem_addr(sm + S::oKt), 128, 0);  // k tile, MN-major
+  const uint64_t dKtile = tc::mnmajor_desc(smem_addr(sm + S::oKtile), 128, 0);  // k tile, MN-major
   const uint32_t idC = tc::idesc_bf16_f32(128, C), id2C = tc::idesc_bf16_f32(128, 2 * C);
   const uint32_t id128m = tc::idesc_bf16_f32_bmn(128, 128);
 
@@ -694,7 +696,7 @@ __global__ void __launch_bounds__(kPassThreads, 1)
     bulk_prefetch_l2(wb.Kt + ck * wb.q_tile, static_cast<uint32_t>(wb.q_tile));
   };
   if (copy_warp) {
-    // each chunk's tiles as soon as their buffers are free: P, k^T and U (onto the D'
+    // each chunk's tiles as soon as their buffers are free: P, k and U (onto the D'
     // tiles) of chunk it + 1 once group 2 of chunk it is done; W, q and vec of chunk it + 2
     // once group 1 of chunk it + 1 is done and every compute warp has finished chunk it's
     // output (vec[it & 1]). Each barrier of a chunk is armed only after this warp has seen
@@ -809,9 +811,9 @@ __global__ void __launch_bounds__(kPassThreads, 1)
           for (int ks = 0; ks < KS; ++ks) tc::mma_bf16(tb + 128, dDl + 16 * ks, dPh + 16 * ks, idC, 1);
 #pragma unroll
           for (int ks = 0; ks < KS; ++ks)  // a K step of the MN-major k tile: 4096 bytes (256 units)
-            tc::mma_bf16(tb + 256, dEh + 16 * ks, dKt + 256 * ks, id128m, ks > 0);
+            tc::mma_bf16(tb + 256, dEh + 16 * ks, dKtile + 256 * ks, id128m, ks > 0);
 #pragma unroll
-          for (int ks = 0; ks < KS; ++ks) tc::mma_bf16(tb + 256, dEl + 16 * ks, dKt + 256 * ks, id128m, 1);
+          for (int ks = 0; ks < KS; ++ks) tc::mma_bf16(tb + 256, dEl + 16 * ks, dKtile + 256 * ks, id128m, 1);
           tc::mma_commit(mma2);
           n2 = it + 1;
         } else {
