@@ -160,6 +160,24 @@ __device__ __forceinline__ bool pass_sync(bool bad) {
   return any != 0;
 }
 
+// acc[i][j] += sum_k a[i][k] b[k][j] for 4 x 4 fp32 blocks held as float4 rows
+__device__ __forceinline__ void fma4x4(float (&acc)[4][4], const float4 (&a)[4], const float4 (&b)[4]) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float ai[4] = {a[i].x, a[i].y, a[i].z, a[i].w};
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+      acc[i][0] = fmaf(ai[kk], b[kk].x, acc[i][0]);
+      acc[i][1] = fmaf(ai[kk], b[kk].y, acc[i][1]);
+      acc[i][2] = fmaf(ai[kk], b[kk].z, acc[i][2]);
+      acc[i][3] = fmaf(ai[kk], b[kk].w, acc[i][3]);
+    }
+  }
+}
+
+// barrier of the intra kernel's four solver warps (warps 0-3; named barrier 1)
+__device__ __forceinline__ void solver_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
 // ============================================================== intra kernel
 template <int C>
 struct IntraSmem {
@@ -171,11 +189,14 @@ struct IntraSmem {
   //          MN-major operands over tokens in the same layout -- sTh / sTl the T' operand, sA
   static constexpr int oQ = 0, oK = kTile, oKl = 2 * kTile;
   static constexpr int oTh = 3 * kTile, oTl = 4 * kTile, oV = 5 * kTile;
-  static constexpr int oA = 6 * kTile;               // fp32 [128][C+1]
-  static constexpr int oVec = oA + 128 * (C + 1) * 4;  // iq, ik, g/G, beta: 4 x 128 floats
+  // fp32 A [128][C + 4] (16-byte rows), then T in place; a row's 4 padding floats hold its
+  // token's K' scale, beta and q / k norm factors
+  static constexpr int kSA = C + 4;
+  static constexpr int oA = 6 * kTile;
+  static constexpr int oG = oA + 128 * kSA * 4;      // cumulative log-gates G: 128 floats
   // the mbarrier, the tensor-memory base and the chunk table live here too: static shared
   // variables would be padded to 1 KB ahead of the 1 KB-aligned dynamic block
-  static constexpr int oBar = oVec + 4 * 128 * 4, oTmem = oBar + 8, oT0 = oTmem + 8;
+  static constexpr int oBar = oG + 128 * 4, oTmem = oBar + 8, oT0 = oTmem + 8;
   static constexpr int kBytes = oT0 + 2 * CPC * 4;
   static_assert(kBytes <= 227 * 1024, "intra shared memory exceeds the per-CTA limit");
 };
@@ -189,10 +210,11 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   constexpr int CPC = S::CPC;
   extern __shared__ __align__(1024) unsigned char sm[];
   float* sA = reinterpret_cast<float*>(sm + S::oA);
-  float* s_iq = reinterpret_cast<float*>(sm + S::oVec);
-  float* s_ik = s_iq + 128;
-  float* s_G = s_ik + 128;
-  float* s_beta = s_G + 128;
+  constexpr int SA = S::kSA;
+  float* s_G = reinterpret_cast<float*>(sm + S::oG);
+  // per-token values in A's row padding
+  constexpr int kSc = 0, kBeta = 1, kIq = 2, kIk = 3;
+  auto pad = [&](int t, int k) -> float& { return sA[t * SA + C + k]; };
   int* s_t0 = reinterpret_cast<int*>(sm + S::oT0);
   int* s_L = s_t0 + CPC;
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(sm + S::oTmem);
@@ -236,7 +258,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       *reinterpret_cast<uint4*>(tile + tc::kmajor_offset(tok, 8 * k8, kD)) = v;
     }
     const float inv = a.qk_l2norm ? 1.0f / sqrtf(ss + 1e-6f) : 1.0f;
-    (which ? s_ik : s_iq)[tok] = inv;
+    pad(tok, which ? kIk : kIq) = inv;
   }
   if (warp == 0) tc::tmem_alloc(s_tmem, kTmemCols);
   if (tid == 0) {
@@ -292,7 +314,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         gate_log(a.a, a.b, a.gate_mode, a.A_log, a.dt_bias,
                  static_cast<int64_t>(s_t0[ci] + tl) * a.Hv + h, h, g, be);
       s_G[tid] = g;
-      s_beta[tid] = be;
+      pad(tid, kBeta) = be;
     }
     __syncthreads();
     if (tid < CPC) {
@@ -307,7 +329,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       const int ci = t / C, tl = t % C;
       const int c = c_first + ci;
       const bool live = c < nchunks && tl < s_L[ci];
-      const float Gt = s_G[t], bt = s_beta[t], ikt = s_ik[t], iqt = s_iq[t] * a.scale;
+      const float Gt = s_G[t], bt = pad(t, kBeta), ikt = pad(t, kIk), iqt = pad(t, kIq) * a.scale;
       constexpr int NH = C / 2;  // columns per thread
       // tcgen05.ld is warp-collective with one column address per warp, so the
       // columns must not depend on the lane: for C >= 32 the warp's 32 rows lie
@@ -339,18 +361,22 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         }
       }
       tc::tmem_wait_ld();
-      float pv[NH];
+      float pv[NH], av[NH];
 #pragma unroll
       for (int e = 0; e < NH; ++e) {
         const int j = half * NH + e;
         const int tj = ci * C + j;
         const float dec = (live && j <= tl) ? expf(Gt - s_G[tj]) : 0.0f;
-        sA[t * (C + 1) + j] = (j < tl) ? bt * dec * ikt * s_ik[tj] * gv[e] : 0.0f;
-        pv[e] = dec * iqt * s_ik[tj] * qv[e];
+        const float iktj = pad(tj, kIk);
+        av[e] = (j < tl) ? bt * dec * ikt * iktj * gv[e] : 0.0f;
+        pv[e] = dec * iqt * iktj * qv[e];
       }
-      // the token's K' scale e^{G_t} ik_t, kept in A's spare padding column (the solve reads
-      // columns 0 .. C-1 only)
-      if (half == 0) sA[t * (C + 1) + C] = live ? expf(Gt) * ikt : 0.0f;
+#pragma unroll
+      for (int e = 0; e < NH; e += 4)  // the thread's half row of A, 16 bytes at a time
+        *reinterpret_cast<float4*>(sA + t * SA + half * NH + e) =
+            make_float4(av[e], av[e + 1], av[e + 2], av[e + 3]);
+      // the token's K' scale e^{G_t} ik_t (the solve reads columns 0 .. C-1 only)
+      if (half == 0) pad(t, kSc) = live ? expf(Gt) * ikt : 0.0f;
       if (c < nchunks) {
         unsigned char* ph = wb.Pt + (static_cast<size_t>(c) * a.Hv + h) * 2 * wb.p_tile;
 #pragma unroll
@@ -376,29 +402,104 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     __syncthreads();
 
     if (tid < 128) {
-      // exact fp32 forward substitution for column j of T = (I + A)^-1 (one chunk)
-      const int ci = tid / C, j = tid % C;
-      const float* Ab = sA + ci * C * (C + 1);
-      float Tc[C];
+      // exact fp32 T = (I + A)^-1 of every chunk, written over A in place (A is strictly lower
+      // triangular, so its upper part already holds T's zeros)
+      // 1) diagonal blocks of B1 = min(C, 32) rows: forward substitution, a column per thread,
+      //    A's rows read 16 bytes at a time (the same address across the warp's block)
+      constexpr int B1 = C < 32 ? C : 32;
+      {
+        const int row0 = (tid / B1) * B1, c = tid % B1;
+        float* Ab = sA + row0 * SA + row0 % C;  // block entry (r, l): Ab[r * SA + l]
+        float x[B1];
 #pragma unroll
-      for (int r = 0; r < C; ++r) {
-        float s0 = 0.0f, s1 = 0.0f;
+        for (int r = 0; r < B1; ++r) {
+          float s0 = 0.0f, s1 = 0.0f;
 #pragma unroll
-        for (int l = 0; l < r; l += 2) {
-          s0 = fmaf(Ab[r * (C + 1) + l], Tc[l], s0);
-          if (l + 1 < r) s1 = fmaf(Ab[r * (C + 1) + l + 1], Tc[l + 1], s1);
+          for (int l = 0; l < r; l += 4) {
+            const float4 a4 = *reinterpret_cast<const float4*>(Ab + r * SA + l);
+            s0 = fmaf(a4.x, x[l], s0);
+            if (l + 1 < r) s1 = fmaf(a4.y, x[l + 1], s1);
+            if (l + 2 < r) s0 = fmaf(a4.z, x[l + 2], s0);
+            if (l + 3 < r) s1 = fmaf(a4.w, x[l + 3], s1);
+          }
+          x[r] = (r < c) ? 0.0f : (r == c ? 1.0f : -(s0 + s1));
         }
-        Tc[r] = (r < j) ? 0.0f : (r == j ? 1.0f : -(s0 + s1));
-      }
-      // T' = T diag(beta) into the block-diagonal bf16 hi / lo tiles
-      const float bj = s_beta[ci * C + j];
+        solver_sync();  // every block of A read
 #pragma unroll
-      for (int r = 0; r < C; ++r) {
-        uint16_t hi, lo;
-        tc::split_bf16(Tc[r] * bj, hi, lo);
-        const uint32_t o = tc::kmajor_offset(ci * C + r, ci * C + j, 128);
-        *reinterpret_cast<uint16_t*>(sm + S::oTh + o) = hi;
-        *reinterpret_cast<uint16_t*>(sm + S::oTl + o) = lo;
+        for (int r = 0; r < B1; ++r) Ab[r * SA + c] = x[r];
+      }
+      if constexpr (C == 64) {
+        // 2) the off-diagonal block T21 = -T22 (A21 T11) of each chunk (T11, T22 now in place
+        //    of A11, A22): 64 threads per chunk, 4 x 4 outputs each from 16-byte row loads
+        const int k = tid & 63, r0 = 4 * (k >> 3), c0 = 4 * (k & 7);
+        float* Ac = sA + (tid >> 6) * C * SA;
+        float acc[4][4];
+        solver_sync();
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj) acc[i][jj] = 0.0f;
+#pragma unroll
+        for (int l = 0; l < 32; l += 4) {  // X = A21 T11
+          float4 av4[4], tv4[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            av4[i] = *reinterpret_cast<const float4*>(Ac + (32 + r0 + i) * SA + l);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            tv4[kk] = *reinterpret_cast<const float4*>(Ac + (l + kk) * SA + c0);
+          fma4x4(acc, av4, tv4);
+        }
+        solver_sync();  // A21 read: X takes its place
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          *reinterpret_cast<float4*>(Ac + (32 + r0 + i) * SA + c0) =
+              make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+        solver_sync();
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj) acc[i][jj] = 0.0f;
+#pragma unroll
+        for (int l = 0; l < 32; l += 4) {  // T22 X; rows r0 .. r0+3 of T22 vanish past column r0+3
+          if (l < r0 + 4) {
+            float4 av4[4], xv4[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              av4[i] = *reinterpret_cast<const float4*>(Ac + (32 + r0 + i) * SA + 32 + l);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              xv4[kk] = *reinterpret_cast<const float4*>(Ac + (32 + l + kk) * SA + c0);
+            fma4x4(acc, av4, xv4);
+          }
+        }
+        solver_sync();  // X read: T21 takes its place
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          *reinterpret_cast<float4*>(Ac + (32 + r0 + i) * SA + c0) =
+              make_float4(-acc[i][0], -acc[i][1], -acc[i][2], -acc[i][3]);
+      }
+      solver_sync();
+      // 3) T' = T diag(beta) into the block-diagonal bf16 hi / lo tiles: row tid, 8 columns at a
+      //    time, 16-byte stores (the warp's lanes on consecutive rows)
+      {
+        const int t = tid, ci = t / C;
+        const float* Tr = sA + t * SA;
+#pragma unroll
+        for (int g = 0; g < C / 8; ++g) {
+          const float4 u0 = *reinterpret_cast<const float4*>(Tr + 8 * g);
+          const float4 u1 = *reinterpret_cast<const float4*>(Tr + 8 * g + 4);
+          const int jb = ci * C + 8 * g;
+          const float x[8] = {u0.x * pad(jb, kBeta),     u0.y * pad(jb + 1, kBeta),
+                              u0.z * pad(jb + 2, kBeta), u0.w * pad(jb + 3, kBeta),
+                              u1.x * pad(jb + 4, kBeta), u1.y * pad(jb + 5, kBeta),
+                              u1.z * pad(jb + 6, kBeta), u1.w * pad(jb + 7, kBeta)};
+          uint4 hi, lo;
+          split8(x, hi, lo);
+          const uint32_t o = tc::kmajor_offset(t, jb, 128);
+          *reinterpret_cast<uint4*>(sm + S::oTh + o) = hi;
+          *reinterpret_cast<uint4*>(sm + S::oTl + o) = lo;
+        }
       }
     } else {
       // V (raw bf16) and K' = diag(e^G ik) K (split) as MN-major operands over the 128
@@ -422,7 +523,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         const int tok = 8 * i + tr;
         const uint32_t o = tc::kmajor_offset(tok, 8 * cg, kD);
         *reinterpret_cast<uint4*>(sm + S::oV + o) = vb[i];
-        const float sc = sA[tok * (C + 1) + C];
+        const float sc = pad(tok, kSc);
         float kx[8];
         unpack8(*reinterpret_cast<const uint4*>(sm + S::oK + o), kx);
 #pragma unroll
