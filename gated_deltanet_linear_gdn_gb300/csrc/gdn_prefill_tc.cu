@@ -114,8 +114,10 @@ __host__ __device__ __forceinline__ uint32_t u_image_offset(int r, int t, int C)
          static_cast<uint32_t>((t & 3) * 4);
 }
 
+// fp32 -> bf16 hi + lo, 8 values (element i in bf16 slot i of each uint4): hi = bf16(x) and
+// lo = bf16(x - hi), both round-to-nearest-even, so x ~= hi + lo to about 2^-17 relative.
+// Pairs are converted at once.
 __device__ __forceinline__ void split8(const float (&x)[8], uint4& hi, uint4& lo) {
-  // pairs converted at once (the same round-to-nearest-even per element as split_bf16)
   uint32_t h[4], l[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {

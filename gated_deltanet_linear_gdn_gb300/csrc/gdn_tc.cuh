@@ -152,14 +152,5 @@ __device__ __forceinline__ uint32_t taddr(uint32_t base, int lane, int col) {
   return base + (static_cast<uint32_t>(lane) << 16) + static_cast<uint32_t>(col);
 }
 
-// fp32 -> bf16 hi + lo (x ~= hi + lo to about 2^-17 relative)
-__device__ __forceinline__ void split_bf16(float x, uint16_t& hi, uint16_t& lo) {
-  __nv_bfloat16 h = __float2bfloat16_rn(x);
-  const float r = x - __bfloat162float(h);
-  __nv_bfloat16 l = __float2bfloat16_rn(r);
-  hi = *reinterpret_cast<uint16_t*>(&h);
-  lo = *reinterpret_cast<uint16_t*>(&l);
-}
-
 }  // namespace tc
 }  // namespace gdn
