@@ -157,6 +157,59 @@ def test_prefill_argument_errors(L):
     assert call(mixed=None) == gdn.GDN_ERR_INVALID_ARG
 
 
+def test_mixed_step_argument_errors(L):
+    """The mixed step's own checks, then each part's, all before any launch."""
+    d = gdn.Dims(2, 4, 32, 32)
+
+    def call(**kw):
+        args = dict(nd=1, nseq=1, T=8, cu=FAKE, slot=FAKE, ssm=FAKE, chunk=16, ws=FAKE,
+                    nbytes=1 << 30)
+        args.update(kw)
+        return L.gdn_mixed_step(FAKE, FAKE, FAKE, 0, FAKE, FAKE, None, None, 1, None, 0, 0,
+                                args["ssm"], args["slot"], args["nd"], args["cu"], None,
+                                args["nseq"], args["T"], 8, d.c(), 0.1, 1, args["chunk"], None,
+                                FAKE, 1, args["ws"], args["nbytes"], None, None)
+
+    assert call(nd=0, nseq=0, T=0) == gdn.GDN_OK              # nothing to do
+    assert call(nd=-1) == gdn.GDN_ERR_INVALID_ARG
+    assert call(nseq=-1) == gdn.GDN_ERR_INVALID_ARG
+    assert call(nseq=0, T=4) == gdn.GDN_ERR_INVALID_ARG       # tokens without sequences
+    assert call(ssm=None) == gdn.GDN_ERR_INVALID_ARG          # the decode part's check
+    assert call(nseq=0, T=0, slot=None) == gdn.GDN_ERR_INVALID_ARG
+    assert call(nd=0, cu=None) == gdn.GDN_ERR_INVALID_ARG     # the prefill part's checks
+    assert call(nd=0, ws=None) == gdn.GDN_ERR_INVALID_ARG
+    assert call(chunk=48) == gdn.GDN_ERR_UNSUPPORTED
+
+
+def test_noalloc_prefill_argument_errors(L):
+    """Size checks of the fixed-scratch entry point: all before it looks up its array."""
+    d = gdn.Dims(16, 32, 128, 128)
+
+    def call(N=1, T=8, chunk=64):
+        return L.gdn_chunked_prefill_noalloc(FAKE, FAKE, FAKE, 0, FAKE, FAKE, None, None, 1, None,
+                                             0, 0, FAKE, FAKE, FAKE, None, N, T, 8, d.c(), 0.1, 1,
+                                             chunk, None, FAKE, 1, None, None)
+
+    assert call(N=-1) == gdn.GDN_ERR_INVALID_ARG
+    assert call(T=-1) == gdn.GDN_ERR_INVALID_ARG
+    assert call(T=200_000) == gdn.GDN_ERR_SCRATCH_LIMIT       # ~13 GB of workspace > 64 MiB
+    assert call(chunk=48) == gdn.GDN_ERR_UNSUPPORTED          # the ordinary entry point's verdict
+
+
+def test_graph_create_argument_errors(L):
+    d = gdn.Dims(2, 4, 32, 32)
+    h = ctypes.c_void_p(0x1234)
+
+    def call(batch=1, out=True):
+        return L.gdn_decode_graph_create(FAKE, FAKE, FAKE, 0, FAKE, FAKE, None, None, 1, None, 0,
+                                         0, FAKE, FAKE, batch, 8, d.c(), 0.1, 1, None, FAKE, 1,
+                                         None, ctypes.byref(h) if out else None)
+
+    assert call(out=False) == gdn.GDN_ERR_INVALID_ARG
+    assert call(batch=0) == gdn.GDN_ERR_INVALID_ARG
+    assert h.value is None                                     # cleared on failure
+
+
 def test_binding_refuses_missing_library(monkeypatch, tmp_path):
     """No CPU fallback: without the shared library every entry point raises."""
     monkeypatch.setattr(gdn, "_lib", None)
