@@ -154,6 +154,10 @@ gdn_status prepare_prefill(const void* mixed_qkv, const void* a, const void* b,
   st = check_gate(gate, la);
   if (st != GDN_OK) return st;
   if (la.gated && total_tokens > 0 && !aligned(out, 16)) return GDN_ERR_INVALID_ARG;
+  // the tensor-core state pass (dk = dv = 128) writes a bf16 output in 16-byte pieces
+  if (!la.out_f32 && dims.head_k_dim == 128 && dims.head_v_dim == 128 && total_tokens > 0 &&
+      !aligned(out, 16))
+    return GDN_ERR_INVALID_ARG;
   const size_t need = gdn_chunked_prefill_workspace_size(total_tokens, num_seqs, dims, chunk);
   if (!workspace || workspace_bytes < need || !aligned(workspace, 16)) return GDN_ERR_INVALID_ARG;
   p = PrefillExtra{cu_seqlens, has_initial_state, num_seqs, total_tokens, chunk, workspace,

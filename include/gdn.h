@@ -215,7 +215,8 @@ size_t gdn_chunked_prefill_workspace_size(int32_t total_tokens, int32_t num_seqs
  *   a, b        [total_tokens, Hv] gate inputs (gdn_gate_mode)
  *   cu_seqlens  [num_seqs + 1] int32, device: 0 = c0 <= c1 <= ... = total_tokens
  *   slot        [num_seqs] int32;  has_initial_state [num_seqs] uint8 or NULL
- *   out         [total_tokens, Hv, dv] of out_dtype
+ *   out         [total_tokens, Hv, dv] of out_dtype; 16-byte aligned when gated, or when bf16
+ *               with dk = dv = 128
  *   gate        NULL, or the output gate applied to every token's o (as in
  *               gdn_decode_step)
  *   chunk       chunk size C in {16, 32, 64}

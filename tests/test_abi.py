@@ -157,6 +157,18 @@ def test_prefill_argument_errors(L):
     assert call(mixed=None) == gdn.GDN_ERR_INVALID_ARG
 
 
+def test_prefill_bf16_output_alignment(L):
+    """The dk = dv = 128 state pass stores a bf16 output 16 bytes at a time."""
+    d = gdn.Dims(16, 32, 128, 128)
+
+    def call(out, out_dtype):
+        return L.gdn_chunked_prefill(FAKE, FAKE, FAKE, 0, FAKE, FAKE, None, None, 1, None, 0, 0,
+                                     FAKE, FAKE, FAKE, None, 1, 8, 8, d.c(), 0.1, 1, 64, None,
+                                     out, out_dtype, FAKE, 1 << 40, None, None)
+
+    assert call(P(0x10004), 0) == gdn.GDN_ERR_INVALID_ARG   # bf16, 4-byte aligned
+
+
 def test_mixed_step_argument_errors(L):
     """The mixed step's own checks, then each part's, all before any launch."""
     d = gdn.Dims(2, 4, 32, 32)
