@@ -246,8 +246,8 @@ def run_ours(args, rank, world):
             sweep[str(B)] = {"us": round(ms * 1e3, 2), "GBps": round(nb / ms / 1e6, 1)}
             del t
         # CUDA-graph buckets (one replay = one graph launch of the fused step)
-        for B in (1, 16):
-            t = decode_setup(B, NUM_SLOTS, seed=B)
+        for B in (1, 4, 16, 64, 256, 1024):
+            t = decode_setup(B, NUM_SLOTS if B <= 256 else 2048, seed=B)
             g = gdn.DecodeGraph(t["mixed"], t["a"], t["b"], t["A_log"], t["dt_bias"], t["conv_w"],
                                 t["conv_b"], t["conv"], t["ssm"], t["slot"], t["out"], dims)
             ms = float(np.median(timed(lambda: g.launch(stream), 20, 3)))
@@ -284,10 +284,7 @@ def run_ours(args, rank, world):
 
     # ---- chunked prefill ----
     prefill = {}
-    cases = [(f"single_{args.prefill_tokens}_bypass",
-              lambda: gi.prefill_single(args.prefill_tokens, seed=0))]
-    if not args.no_varlen:
-        cases.append(("varlen_8seq_conv", lambda: gi.prefill_varlen(8, 8192, seed=0)))
+    cases = prefill_cases(args)
     if not args.no_prefill:
         for name, make in cases:
             inp = make()
@@ -503,9 +500,39 @@ def run_ours(args, rank, world):
         "context": {"pages_gb10_c16_GBps": 175.14,
                     "note": "GB10 (SM121) whole GDN transition incl. W4A4 projections; context only"},
     }
+    # prefill figures as flat keys beside the headline (the nested dict keeps the detail)
+    for name, key in ((f"single_{args.prefill_tokens}_bypass", "prefill"),
+                      ("varlen_8seq_conv", "prefill_varlen")):
+        e = prefill.get(name)
+        if e:
+            line[f"{key}_tokens_per_s"] = e["tokens_per_s"]
+            line[f"{key}_ms"] = e["ms"]
+            line[f"{key}_tflops"] = e["TFLOPs"]
+            line[f"{key}_frac_of_bf16_tensor_peak"] = e["frac_of_bf16_tensor_peak"]
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(seconds=args.cpu_seconds)
+        line["cpu_baseline_1thread"] = cpu_baseline(seconds=args.cpu_seconds / 2, nthreads=1)
+        if not args.no_prefill:
+            pb = {}
+            for name, make in prefill_cases(args):
+                pb[name] = cpu_prefill_baseline(make(), name)
+            line["cpu_baseline_prefill"] = pb
+            for name, key in ((f"single_{args.prefill_tokens}_bypass", "prefill"),
+                              ("varlen_8seq_conv", "prefill_varlen")):
+                if name in pb:
+                    line[f"{key}_oracle_tokens_per_s"] = pb[name]["value"]
     return line
+
+
+def prefill_cases(args):
+    """The chunked-prefill workloads: one sequence (conv bypassed), then ~32k varlen tokens."""
+    from gated_deltanet_linear_gdn_gb300 import inputs as gi
+
+    cases = [(f"single_{args.prefill_tokens}_bypass",
+              lambda: gi.prefill_single(args.prefill_tokens, seed=0))]
+    if not args.no_varlen:
+        cases.append(("varlen_8seq_conv", lambda: gi.prefill_varlen(8, 8192, seed=0)))
+    return cases
 
 
 # --------------------------------------------------------------------------- oracle arm
@@ -528,11 +555,11 @@ def _oracle_call(inp, conv, ssm, nthreads):
                         g.Hk, g.Hv, g.dk, g.dv, g.W, inp.scale, True, None, nthreads)
 
 
-def cpu_baseline(seconds=10.0, rows=32):
+def cpu_baseline(seconds=10.0, rows=32, nthreads=None):
     import oracle
 
     oracle.lib()
-    nthreads = os.cpu_count() or 1
+    nthreads = nthreads or os.cpu_count() or 1
     inp = oracle_decode_sample(rows)
     conv = inp.conv_state.copy()
     ssm = inp.ssm_state.astype(np.float64)
@@ -548,6 +575,37 @@ def cpu_baseline(seconds=10.0, rows=32):
     return {"value": round(nb / el / 1e9, 4), "unit": "GB/s", "cores": nthreads, "kind": "oracle",
             "sample": f"{rows} rows of the B=256 decode workload (Qwen3-Next geometry), "
                       f"{runs} oracle calls in {el:.1f} s, fp64, {nthreads} threads"}
+
+
+def cpu_prefill_baseline(inp, name, head_stride=None, nthreads=None):
+    """The oracle on one prefill workload, the same inputs as the GPU call. The token-by-token
+    recurrence costs ~6 dv dk fp64 operations per token and value head, so long workloads are
+    sampled by value head (every head_stride-th head; the conv runs in full) and the time is
+    scaled to all heads -- which also scales the conv's share, so the figure slightly
+    understates the oracle."""
+    import oracle
+
+    oracle.lib()
+    nthreads = nthreads or os.cpu_count() or 1
+    g = inp.geo
+    T = inp.total_tokens
+    if head_stride is None:
+        head_stride = 1 if T <= 4096 else 4
+    mask = (np.arange(g.Hv) % head_stride) == 0
+    conv = None if inp.conv_state is None else inp.conv_state.copy()
+    ssm = inp.ssm_state.astype(np.float64)
+    t0 = time.perf_counter()
+    oracle.layer(inp.mixed, inp.a, inp.b, inp.gate_direct, inp.A_log, inp.dt_bias, inp.conv_w,
+                 inp.conv_b, inp.silu, conv, inp.conv_f32, inp.conv_layout, ssm, inp.cu_seqlens,
+                 inp.slot, inp.has_init, g.Hk, g.Hv, g.dk, g.dv, g.W, inp.scale, inp.qk_l2norm,
+                 mask, nthreads)
+    el = time.perf_counter() - t0
+    frac = float(mask.sum()) / g.Hv
+    return {"value": round(T * frac / el, 1), "unit": "tokens/s", "cores": nthreads,
+            "kind": "oracle",
+            "sample": f"{name}: {T} tokens, {int(mask.sum())} of {g.Hv} value heads "
+                      f"(time scaled to all heads), fp64 token-by-token oracle, {el:.1f} s, "
+                      f"{nthreads} threads"}
 
 
 def run_reference(args, rank, world):

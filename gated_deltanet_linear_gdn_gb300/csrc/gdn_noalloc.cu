@@ -16,9 +16,14 @@
 //    GDN_ERR_SCRATCH_LIMIT before anything is enqueued;
 //  - all calls on one device share the one array, so calls that can overlap on
 //    the GPU (different streams without ordering between them) race on it;
-//  - the first call on a device looks up the array's device address with
-//    cudaGetSymbolAddress (which may load the module), so make that first call
-//    before any stream capture.
+//  - the first call under each CUDA context looks up the array's device address
+//    with cudaGetSymbolAddress (which may load the module), so make that first
+//    call before any stream capture. The address is kept per context; a context
+//    destroyed and recreated under the same handle (cudaDeviceReset on the
+//    primary context) is not detected, so a caller that resets the device does
+//    not use this entry point afterwards.
+// Arguments are checked in full before the look-up: a bad call returns its
+// status without touching the CUDA runtime.
 // The prefill writes every scratch word before it reads it, so the array keeps
 // whatever the previous call left and is never cleared.
 #include <mutex>
@@ -29,26 +34,56 @@ namespace {
 
 static __device__ __align__(256) unsigned char g_prefill_scratch[GDN_NOALLOC_SCRATCH_BYTES];
 
-constexpr int kMaxDevices = 256;
-std::mutex g_mu;
-void* g_scratch_ptr[kMaxDevices] = {};
+// cuCtxGetCurrent, fetched through the runtime (so the library links no driver library)
+typedef int (*CtxGetCurrentFn)(void** ctx);
 
-// Device address of g_prefill_scratch on the current device (looked up once per
-// device; the host-side symbol itself is only a stand-in and must never be
-// passed to a kernel).
+constexpr int kMaxContexts = 64;
+struct ScratchEntry {
+  void* ctx;
+  void* ptr;
+};
+std::mutex g_mu;
+ScratchEntry g_table[kMaxContexts] = {};
+int g_used = 0;
+CtxGetCurrentFn g_ctx_get = nullptr;
+bool g_ctx_get_tried = false;
+
+// The current context's handle, or null if it cannot be had (then nothing is cached).
+void* current_context() {
+  if (!g_ctx_get_tried) {
+    g_ctx_get_tried = true;
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_ctx_get = reinterpret_cast<CtxGetCurrentFn>(fn);
+  }
+  void* ctx = nullptr;
+  if (!g_ctx_get || g_ctx_get(&ctx) != 0) return nullptr;
+  return ctx;
+}
+
+// Device address of g_prefill_scratch in the current context (looked up once per context;
+// the host-side symbol itself is only a stand-in and must never be passed to a kernel).
 cudaError_t scratch_address(void** out) {
   int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  cudaError_t e = cudaGetDevice(&dev);  // makes the device's primary context current if none is
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> lock(g_mu);
-  if (g_scratch_ptr[dev] == nullptr) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_prefill_scratch);
-    if (e != cudaSuccess) return e;
-    g_scratch_ptr[dev] = p;
+  void* ctx = current_context();
+  if (ctx) {
+    for (int i = 0; i < g_used; ++i)
+      if (g_table[i].ctx == ctx) {
+        *out = g_table[i].ptr;
+        return cudaSuccess;
+      }
   }
-  *out = g_scratch_ptr[dev];
+  void* p = nullptr;
+  e = cudaGetSymbolAddress(&p, g_prefill_scratch);
+  if (e != cudaSuccess) return e;
+  if (ctx && g_used < kMaxContexts) g_table[g_used++] = ScratchEntry{ctx, p};
+  *out = p;
   return cudaSuccess;
 }
 
@@ -63,21 +98,25 @@ extern "C" gdn_status gdn_chunked_prefill_noalloc(
     gdn_dims dims, float scale, int32_t qk_l2norm, int32_t chunk, const gdn_output_gate* gate,
     void* out, gdn_dtype out_dtype, int32_t* err, void* stream) {
   if (num_seqs < 0 || total_tokens < 0) return GDN_ERR_INVALID_ARG;
+  if (num_seqs == 0 && total_tokens == 0 && (chunk == 16 || chunk == 32 || chunk == 64))
+    return GDN_OK;  // the ordinary entry point's no-op
   const size_t need = gdn_chunked_prefill_workspace_size(total_tokens, num_seqs, dims, chunk);
-  if (need == 0) {
-    // sizes the ordinary entry point rejects: let it report the same status
-    return gdn_chunked_prefill(mixed_qkv, a, b, gate_mode, A_log, dt_bias, conv_weight,
-                               conv_bias, silu, conv_state, conv_dtype, conv_layout, ssm_state,
-                               cu_seqlens, slot, has_initial_state, num_seqs, total_tokens,
-                               num_slots, dims, scale, qk_l2norm, chunk, gate, out, out_dtype,
-                               nullptr, 0, err, stream);
-  }
   if (need > static_cast<size_t>(GDN_NOALLOC_SCRATCH_BYTES)) return GDN_ERR_SCRATCH_LIMIT;
+  // every argument check of the ordinary entry point, with a stand-in workspace of the
+  // scratch's size (an aligned non-null value that is never dereferenced)
+  gdn::LayerArgs la;
+  gdn::PrefillExtra p;
+  const gdn_status st = gdn::prepare_prefill(
+      mixed_qkv, a, b, gate_mode, A_log, dt_bias, conv_weight, conv_bias, silu, conv_state,
+      conv_dtype, conv_layout, ssm_state, cu_seqlens, slot, has_initial_state, num_seqs,
+      total_tokens, num_slots, dims, scale, qk_l2norm, chunk, gate, out, out_dtype,
+      reinterpret_cast<void*>(static_cast<uintptr_t>(256)),
+      static_cast<size_t>(GDN_NOALLOC_SCRATCH_BYTES), err, la, p);
+  if (st != GDN_OK) return st;
   void* ws = nullptr;
   if (scratch_address(&ws) != cudaSuccess) return GDN_ERR_CUDA;
-  return gdn_chunked_prefill(mixed_qkv, a, b, gate_mode, A_log, dt_bias, conv_weight, conv_bias,
-                             silu, conv_state, conv_dtype, conv_layout, ssm_state, cu_seqlens,
-                             slot, has_initial_state, num_seqs, total_tokens, num_slots, dims,
-                             scale, qk_l2norm, chunk, gate, out, out_dtype, ws,
-                             static_cast<size_t>(GDN_NOALLOC_SCRATCH_BYTES), err, stream);
+  p.workspace = ws;
+  return gdn::launch_prefill(la, p, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? GDN_OK
+             : GDN_ERR_CUDA;
 }

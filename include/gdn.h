@@ -38,8 +38,9 @@
  *     gdn_validate_slots on the host where that matters.
  *   - Errors: argument errors return before any launch and leave every buffer
  *     untouched. A failed launch returns GDN_ERR_CUDA. Nothing traps.
- *   - Results are deterministic: no atomics, no batch-dependent reduction
- *     order; each row / sequence depends only on its own inputs and slot.
+ *   - Results are deterministic: no atomic arithmetic (atomics only set bits of
+ *     the error word), no batch-dependent reduction order; each row / sequence
+ *     depends only on its own inputs and slot.
  */
 #ifndef GDN_H
 #define GDN_H
@@ -115,8 +116,8 @@ typedef struct {
   int32_t act; /* gdn_gate_act */
 } gdn_output_gate;
 
-/* Bits of the device error word (int32, caller-zeroed; the kernels only OR
- * bits into it with plain stores). */
+/* Bits of the device error word (int32, caller-zeroed; the kernels only set
+ * bits in it, with atomicOr, and never clear one). */
 #define GDN_DEVERR_SLOT_RANGE 1 /* an active slot >= num_slots */
 #define GDN_DEVERR_SEQLENS 2    /* cu_seqlens not non-decreasing or not ending at total_tokens */
 #define GDN_DEVERR_TIMEOUT 4    /* a bounded wait for an asynchronous copy gave up (the
@@ -260,9 +261,13 @@ gdn_status gdn_chunked_prefill(const void* mixed_qkv, const void* a, const void*
  *     at chunk 64);
  *   - all calls on a device share the array: calls that may run at the same
  *     time on the GPU (streams without ordering between them) race on it;
- *   - the first call on each device looks up the array's device address
- *     (cudaGetSymbolAddress), which may load the module: make that first call
- *     before any stream capture.
+ *   - the first call under each CUDA context looks up the array's device
+ *     address (cudaGetSymbolAddress), which may load the module: make that
+ *     first call before any stream capture. The address is kept per context;
+ *     cudaDeviceReset is not supported after the first call (the primary
+ *     context comes back under the same handle, with the array elsewhere).
+ * Arguments are checked exactly as gdn_chunked_prefill checks them, and before
+ * the look-up, so a bad call returns its status without any CUDA call.
  * Allocates nothing: no cudaMalloc, no cudaFree, no allocating library call.
  */
 #define GDN_NOALLOC_SCRATCH_BYTES (64u << 20)

@@ -197,12 +197,17 @@ def test_noalloc_prefill_argument_errors(L):
     """Size checks of the fixed-scratch entry point: all before it looks up its array."""
     d = gdn.Dims(16, 32, 128, 128)
 
-    def call(N=1, T=8, chunk=64):
-        return L.gdn_chunked_prefill_noalloc(FAKE, FAKE, FAKE, 0, FAKE, FAKE, None, None, 1, None,
-                                             0, 0, FAKE, FAKE, FAKE, None, N, T, 8, d.c(), 0.1, 1,
-                                             chunk, None, FAKE, 1, None, None)
+    def call(N=1, T=8, chunk=64, mixed=FAKE, cu=FAKE):
+        return L.gdn_chunked_prefill_noalloc(mixed, FAKE, FAKE, 0, FAKE, FAKE, None, None, 1,
+                                             None, 0, 0, FAKE, cu, FAKE, None, N, T, 8, d.c(),
+                                             0.1, 1, chunk, None, FAKE, 1, None, None)
 
     assert call(N=-1) == gdn.GDN_ERR_INVALID_ARG
+    # sizes that fit the scratch, but a null pointer: refused before the array's look-up
+    # (no CUDA call, so this runs without a GPU)
+    assert call(mixed=None) == gdn.GDN_ERR_INVALID_ARG
+    assert call(cu=None) == gdn.GDN_ERR_INVALID_ARG
+    assert call(N=0, T=0) == gdn.GDN_OK                        # the ordinary no-op
     assert call(T=-1) == gdn.GDN_ERR_INVALID_ARG
     assert call(T=200_000) == gdn.GDN_ERR_SCRATCH_LIMIT       # ~13 GB of workspace > 64 MiB
     assert call(chunk=48) == gdn.GDN_ERR_UNSUPPORTED          # the ordinary entry point's verdict

@@ -154,18 +154,28 @@ def test_prefill_bitwise_replay():
     assert len(hashes) == 1
 
 
-def test_prefill_packing_invariance():
+@pytest.mark.parametrize("geo,chunk,lens", [
+    (gi.TINY, 16, [37, 64, 1, 150, 9]),
+    # dk = dv = 128, the tensor-core path: the intra kernel packs 128 / C chunks into one
+    # 128-row MMA tile, so odd chunk counts move every later sequence's chunks to another
+    # tile position between compositions
+    (gi.QWEN3_NEXT, 64, [37, 64, 1, 150, 9, 200]),
+    (gi.QWEN3_NEXT, 16, [37, 64, 1, 150, 9, 200]),
+])
+def test_prefill_packing_invariance(geo, chunk, lens):
     """Each sequence alone, packed with the others, and packed in another order (with
-    shuffled cache blocks) gives bitwise the same outputs and final states."""
-    lens = [37, 64, 1, 150, 9]
-    inp = gi.make_inputs(gi.TINY, lens, 16, seed=8)
+    shuffled cache blocks) gives bitwise the same outputs, final recurrent states and final
+    conv windows."""
+    inp = gi.make_inputs(geo, lens, 16, seed=8)
     d = Device(inp)
-    full = gpu_prefill(d, chunk=16, out_f32=False)
+    full = gpu_prefill(d, chunk=chunk, out_f32=False)
     torch.cuda.synchronize()
+    assert int(d.err.item()) == 0
     full_bits = torch_to_bits(full)
     cu = inp.cu_seqlens
     rng = np.random.default_rng(1)
-    orders = [[i] for i in range(len(lens))] + [list(rng.permutation(len(lens)))]
+    orders = ([[i] for i in range(len(lens))] + [list(rng.permutation(len(lens)))]
+              + [list(rng.permutation(len(lens)))[:3]])
     for order in orders:
         perm = np.concatenate([[0], 1 + rng.permutation(inp.num_slots - 1)])  # 0 stays null
         inv = np.argsort(perm)
@@ -177,8 +187,9 @@ def test_prefill_packing_invariance():
         sub.conv_state = np.ascontiguousarray(inp.conv_state[perm])
         sub.ssm_state = np.ascontiguousarray(inp.ssm_state[perm])
         ds = Device(sub)
-        o = gpu_prefill(ds, chunk=16, out_f32=False)
+        o = gpu_prefill(ds, chunk=chunk, out_f32=False)
         torch.cuda.synchronize()
+        assert int(ds.err.item()) == 0
         assert np.array_equal(torch_to_bits(o), full_bits[toks])
         sl = inp.slot[order]
         assert torch.equal(ds.ssm.cpu()[inv[sl]], d.ssm.cpu()[sl])

@@ -474,6 +474,61 @@ def test_prefill_final_conv_state_is_last_inputs(oracle, cache_f32, has_init):
         assert np.array_equal(got, expect)
 
 
+def test_prefill_without_initial_state_ignores_the_slot(oracle):
+    """has_initial_state = 0: the sequence starts from a zero recurrent state and a zero conv
+    window whatever its slot holds, and its final state is written to the slot.
+
+    (a) Conv bypassed, direct gates, no QK norm, scale 1: every head's outputs and final state
+        equal the single-head recurrence (pinned above by closed forms and hand fixtures) run
+        from S0 = 0, although the slot holds a non-zero state; the sequence beside it, which
+        has an initial state, equals the recurrence from its slot's state.
+    (b) Conv on: the call equals one that reads slots whose state and conv window were
+        zeroed beforehand, and differs from one that reads the slots as they are."""
+    geo = gi.TINY
+    dk, dv, Hk, Hv = geo.dk, geo.dv, geo.Hk, geo.Hv
+    case = gi.make_inputs(geo, [9, 5], 6, seed=13, conv=False, gate_direct=True,
+                          has_init=[0, 1], state_std=0.5)
+    case.qk_l2norm = False
+    ssm0 = case.ssm_state.astype(np.float64)
+    ssm = ssm0.copy()
+    out, _, _ = oracle.layer(case.mixed, case.a, case.b, True, case.A_log, case.dt_bias, None,
+                             None, 0, None, 0, 0, ssm, case.cu_seqlens, case.slot, case.has_init,
+                             Hk, Hv, dk, dv, scale=1.0, qk_l2norm=False)
+    x = bfv(case.mixed)
+    for i, s in enumerate(case.slot):
+        assert np.abs(ssm0[s]).max() > 0.1          # the slot holds a state worth ignoring
+        bos, eos = case.cu_seqlens[i], case.cu_seqlens[i + 1]
+        for h in range(Hv):
+            kh = h // (Hv // Hk)
+            q = x[bos:eos, kh * dk:(kh + 1) * dk]
+            k = x[bos:eos, (Hk + kh) * dk:(Hk + kh + 1) * dk]
+            v = x[bos:eos, 2 * Hk * dk + h * dv:2 * Hk * dk + (h + 1) * dv]
+            S0 = np.zeros((dv, dk)) if case.has_init[i] == 0 else ssm0[s, h]
+            o_ref, S_ref = oracle.recurrent_head(q, k, v, case.a[bos:eos, h], case.b[bos:eos, h],
+                                                 S0)
+            assert np.allclose(out[bos:eos, h], o_ref, rtol=0, atol=1e-14)
+            assert np.allclose(ssm[s, h], S_ref, rtol=0, atol=1e-14)
+
+    case = gi.make_inputs(geo, [6, 4], 6, seed=14, has_init=[0, 0])
+    runs = []
+    for mode in ("no_init", "zeroed_slots", "read_slots"):
+        conv = case.conv_state.copy()
+        ssm = case.ssm_state.astype(np.float64)
+        hi = case.has_init
+        if mode != "no_init":
+            hi = None
+        if mode == "zeroed_slots":
+            conv[case.slot] = 0
+            ssm[case.slot] = 0.0
+        o, _, _ = oracle.layer(case.mixed, case.a, case.b, False, case.A_log, case.dt_bias,
+                               case.conv_w, case.conv_b, 1, conv, 0, 0, ssm, case.cu_seqlens,
+                               case.slot, hi, Hk, Hv, dk, dv)
+        runs.append((o, conv, ssm))
+    (o0, c0, s0), (o1, c1, s1), (o2, _, _) = runs
+    assert np.array_equal(o0, o1) and np.array_equal(c0, c1) and np.array_equal(s0, s1)
+    assert not np.allclose(o0, o2)
+
+
 def test_prefill_equals_decode_steps(oracle):
     """A sequence prefilled at once equals the same tokens fed as successive decode steps."""
     geo = gi.TINY
