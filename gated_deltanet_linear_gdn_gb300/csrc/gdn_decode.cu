@@ -123,7 +123,7 @@ struct StateIO<1, true> {
 template <int VPL>
 __device__ __forceinline__ float lane_dot(const float (&s)[VPL], const float (&x)[VPL]) {
   if constexpr (VPL == 1) {
-    return s[0] * x[0];
+    return __fmul_rn(s[0], x[0]);
   } else {
     float2 acc = __fmul2_rn(make_float2(s[0], s[1]), make_float2(x[0], x[1]));
 #pragma unroll
@@ -170,6 +170,49 @@ __device__ __forceinline__ void transposed_warp_sum(float (&red)[V], int lane) {
   }
 #pragma unroll
   for (int m = LPV / 2; m >= 1; m >>= 1) red[0] += __shfl_xor_sync(0xffffffffu, red[0], m);
+}
+
+// The dot products of a warp's RPW state rows (held in sv, a lane owning VPL consecutive
+// elements of each) with k and q, summed in one transposed butterfly; then for row
+// ri = lane / (2 LPV): d = b (v - a (S k)) and o = a (S q) + d (k . q). Lanes with
+// `writer` set hold the row's o. Both decode kernels run a row through this one function.
+template <int VPL, int RPW>
+__device__ __forceinline__ void rows_predict(const float (&sv)[RPW][VPL], const float (&qv)[VPL],
+                                             const float (&kv)[VPL], const float* vb, int row0,
+                                             float al, float be, float kq, int lane,
+                                             float& delta, float& ov, int& ri, bool& writer) {
+  float red[2 * RPW];
+#pragma unroll
+  for (int i = 0; i < RPW; ++i) {
+    red[2 * i] = lane_dot<VPL>(sv[i], kv);
+    red[2 * i + 1] = lane_dot<VPL>(sv[i], qv);
+  }
+  transposed_warp_sum<2 * RPW>(red, lane);
+  // lanes of value pair i (row i) swap halves: both then hold (S k)_i and (S q)_i
+  constexpr int LPV = 32 / (2 * RPW);
+  const float other = __shfl_xor_sync(0xffffffffu, red[0], LPV);
+  const bool is_q = ((lane / LPV) & 1) != 0;
+  const float pk = is_q ? other : red[0], pq = is_q ? red[0] : other;
+  ri = lane / (2 * LPV);
+  // explicit roundings: no compiled copy of this code may contract it differently
+  delta = __fmul_rn(be, __fmaf_rn(-al, pk, vb[row0 + ri]));
+  writer = lane % (2 * LPV) == 0;
+  ov = __fmaf_rn(delta, kq, __fmul_rn(al, pq));  // o_i = a (S q)_i + d_i (k . q)
+}
+
+// The warp's rows after the predict step: S <- a S + d k^T row by row (d of row i from the
+// lanes that computed it), each stored as soon as it is updated.
+template <int VPL, int RPW, bool kBf16State>
+__device__ __forceinline__ void rows_update_store(float (&sv)[RPW][VPL], const float (&kv)[VPL],
+                                                  float al, float delta, unsigned char* dst,
+                                                  int row_bytes, int lane) {
+  constexpr int LPV = 32 / (2 * RPW);
+#pragma unroll
+  for (int i = 0; i < RPW; ++i) {
+    const float d = __shfl_sync(0xffffffffu, delta, i * 2 * LPV);
+    lane_update<VPL>(sv[i], kv, al, d);
+    StateIO<VPL, kBf16State>::store(dst + static_cast<int64_t>(i) * row_bytes, lane, sv[i]);
+  }
 }
 
 template <int DK, int R, bool kBf16State>
@@ -588,7 +631,7 @@ __global__ void __launch_bounds__(DecodeCfg<DK, R, kBf16State>::kThreads, 1)
         for (int e = 0; e < 8; ++e) ss = fmaf(ov[e], ov[e], ss);
 #pragma unroll
         for (int m = LPH / 2; m >= 1; m >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, m);
-        const float den = ss / static_cast<float>(DV) + a.gate_eps;
+        const float den = __fadd_rn(__fdiv_rn(ss, static_cast<float>(DV)), a.gate_eps);
         const float inv = den > 0.0f ? 1.0f / sqrtf(den) : 0.0f;  // all-zero head, eps 0
         float z8[8], y[8];
         unpack8(zr[j], z8);
@@ -679,33 +722,18 @@ __global__ void __launch_bounds__(DecodeCfg<DK, R, kBf16State>::kThreads, 1)
       for (int i = 0; i < RPW; ++i) IO::load(src + i * Cfg::kRowBytes, lane, sv[i]);
       __syncwarp();
       if (lane == 0) mbar_arrive(empty0 + 8 * r);
-      // (S k)_i and (S q)_i of the warp's rows, as values 2i and 2i+1
-      float red[2 * RPW];
-#pragma unroll
-      for (int i = 0; i < RPW; ++i) {
-        red[2 * i] = lane_dot<VPL>(sv[i], kv);
-        red[2 * i + 1] = lane_dot<VPL>(sv[i], qv);
-      }
-      transposed_warp_sum<2 * RPW>(red, lane);
-      // lanes of value pair i (row i) swap halves: both then hold (S k)_i and (S q)_i
-      constexpr int LPV = 32 / (2 * RPW);
-      const float other = __shfl_xor_sync(0xffffffffu, red[0], LPV);
-      const bool is_q = ((lane / LPV) & 1) != 0;
-      const float pk = is_q ? other : red[0], pq = is_q ? red[0] : other;
-      const int ri = lane / (2 * LPV);
-      const float delta = be * (vb[row0 + ri] - al * pk);
-      if (lane % (2 * LPV) == 0) {  // o_i = a (S q)_i + d_i (k . q)
-        const float ov = fmaf(delta, kq, al * pq);
+      float delta, ov;
+      int ri;
+      bool writer;
+      rows_predict<VPL, RPW>(sv, qv, kv, vb, row0, al, be, kq, lane, delta, ov, ri, writer);
+      if (writer) {
         if (a.gated) ob[row0 + ri] = ov;  // the epilogue warp gates and stores it
         else if (a.out_f32) static_cast<float*>(a.out)[out_base + row0 + ri] = ov;
         else static_cast<uint16_t*>(a.out)[out_base + row0 + ri] = f2bf(ov);
       }
-#pragma unroll
-      for (int i = 0; i < RPW; ++i) {
-        const float d = __shfl_sync(0xffffffffu, delta, i * 2 * LPV);
-        lane_update<VPL>(sv[i], kv, al, d);
-        IO::store(dst_base + static_cast<int64_t>(row0 + i) * Cfg::kRowBytes, lane, sv[i]);
-      }
+      rows_update_store<VPL, RPW, kBf16State>(
+          sv, kv, al, delta, dst_base + static_cast<int64_t>(row0) * Cfg::kRowBytes,
+          Cfg::kRowBytes, lane);
     }
     __syncwarp();
     if (lane == 0) {
@@ -717,9 +745,193 @@ __global__ void __launch_bounds__(DecodeCfg<DK, R, kBf16State>::kThreads, 1)
 }
 
 
+// ------------------------------------------------------------------ small batches
+// With fewer units than SMs the persistent kernel leaves most SMs idle and each busy one
+// streams a whole unit. Here a unit (row b, k-head kh) is split over the P CTAs of a
+// thread-block cluster instead: CTA p takes the unit's rows [p NR, (p + 1) NR), NR = R dv / P,
+// as many rows per warp as the persistent kernel's consumers take, loaded straight into
+// registers before anything else. Every CTA runs the
+// conv of the unit's q and k channels itself, from the old windows, and the conv of its own
+// rows' v channels, whose windows it rolls. CTA 0 rolls the q and k windows, after a
+// cluster barrier that every CTA of the cluster arrives at once its window reads are done.
+// The arithmetic of a row is the persistent kernel's (conv8_step, finish_setup,
+// rows_predict, lane_update), so its results do not depend on which kernel ran it.
+template <int DK, int R, bool kBf16State, int P>
+struct SplitCfg {
+  using Cfg = DecodeCfg<DK, R, kBf16State>;
+  static constexpr int RPW = Cfg::kRowsPerWarp;  // the persistent kernel's rows per warp
+  static constexpr int NR = R * DK / P;          // rows per CTA
+  static constexpr int kThreads = NR / RPW * 32;
+};
+
+template <int DK, int R, bool kF32Cache, bool kBf16State, int P>
+__global__ void __launch_bounds__(SplitCfg<DK, R, kBf16State, P>::kThreads, 1)
+    split_decode_kernel(LayerArgs a) {
+  using SC = SplitCfg<DK, R, kBf16State, P>;
+  using Cfg = typename SC::Cfg;
+  constexpr int DV = DK, VPL = DK / 32, UR = R * DV, NR = SC::NR, RPW = SC::RPW;
+  constexpr int NW = NR / RPW;
+  constexpr int QG = DK / 8, VG = NR / 8, NG = 2 * QG + VG;
+  static_assert(NR % RPW == 0 && NR % 8 == 0 && NW * 32 >= NG, "one conv group per thread");
+  __shared__ __align__(16) float buf[Cfg::kSetupStride];  // the persistent kernel's layout
+  __shared__ float qkwin[2 * QG][8][kConvW - 1];           // rolled q, k windows (CTA 0)
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int part = blockIdx.x;  // the CTA's rank in its cluster (cluster = P x 1 x 1)
+  const int u = blockIdx.y, b = u / a.Hk, kh = u % a.Hk;
+  const int32_t s = a.slot[b];
+  const int64_t out_base = (static_cast<int64_t>(b) * a.Hv + kh * R) * DV + part * NR;
+  if (!unit_active(s, a.num_slots)) {  // the same for the whole cluster: no barrier is used
+    if (s >= a.num_slots && part == 0 && kh == 0 && tid == 0 && a.err)
+      atomicOr(a.err, GDN_DEVERR_SLOT_RANGE);
+    for (int i = tid; i < NR; i += NW * 32) {
+      if (a.out_f32) static_cast<float*>(a.out)[out_base + i] = 0.0f;
+      else static_cast<uint16_t*>(a.out)[out_base + i] = 0;
+    }
+    return;
+  }
+  const int row0 = part * NR + warp * RPW;  // the warp's first row within the unit
+  unsigned char* rows = reinterpret_cast<unsigned char*>(a.ssm) +
+                        ((static_cast<int64_t>(s) * a.Hv + kh * R) * DV + row0) * Cfg::kRowBytes;
+  float sv[RPW][VPL];
+#pragma unroll
+  for (int i = 0; i < RPW; ++i)
+    StateIO<VPL, kBf16State>::load(rows + i * Cfg::kRowBytes, lane, sv[i]);
+  GateRaw gr{};
+  if (warp == 0 && lane < R) {
+    const int h = kh * R + lane;
+    gr = gate_load(a.a, a.b, a.gate_mode, a.A_log, a.dt_bias, static_cast<int64_t>(b) * a.Hv + h, h);
+  }
+  // one conv group per thread: q and k groups 0 .. 2 QG - 1, then this CTA's v groups
+  if (tid < NG) {
+    const bool qk = tid < 2 * QG;
+    int c0;
+    float* dst;
+    if (qk) {
+      group_channels<DK, R>(tid, kh, a.Hk, buf, c0, dst);
+    } else {
+      const int j = part * NR + 8 * (tid - 2 * QG);  // unit-relative v channel
+      c0 = 2 * a.Hk * DK + kh * UR + j;
+      dst = buf + 2 * DK + j;
+    }
+    float x8[8];
+    unpack8(__ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.mixed) +
+                                                 static_cast<int64_t>(b) * a.D + c0)),
+            x8);
+    if (a.conv_w) {
+      float win[8][kConvW - 1], y8[8];
+      load_conv8<kF32Cache>(a.conv_state, a.conv_layout, s, a.D, c0, win);
+      conv8_step<kF32Cache>(win, x8, static_cast<const uint16_t*>(a.conv_w),
+                            static_cast<const uint16_t*>(a.conv_b), c0, a.silu != 0, y8);
+      if (qk) {
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch)
+#pragma unroll
+          for (int j = 0; j < kConvW - 1; ++j) qkwin[tid][ch][j] = win[ch][j];
+      } else {
+        store_conv8<kF32Cache>(a.conv_state, a.conv_layout, s, a.D, c0, win);
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) dst[i] = y8[i];
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) dst[i] = x8[i];
+    }
+  }
+  cluster_arrive();  // this CTA has read every window it needs
+  __syncthreads();
+  if (warp == 0) finish_setup<DK, R>(a, buf, gr, lane);
+  __syncthreads();
+  {
+    float qv[VPL], kv[VPL];
+#pragma unroll
+    for (int e = 0; e < VPL; ++e) {
+      qv[e] = buf[lane * VPL + e];
+      kv[e] = buf[DK + lane * VPL + e];
+    }
+    const float* vb = buf + 2 * DK;
+    const float* gb = buf + 2 * DK + UR;
+    const int hl = row0 / DV;
+    const float al = gb[hl], be = gb[R + hl], kq = gb[2 * R];
+    float delta, ov;
+    int ri;
+    bool writer;
+    rows_predict<VPL, RPW>(sv, qv, kv, vb, row0, al, be, kq, lane, delta, ov, ri, writer);
+    if (writer) {
+      const int64_t o = out_base + warp * RPW + ri;
+      if (a.out_f32) static_cast<float*>(a.out)[o] = ov;
+      else static_cast<uint16_t*>(a.out)[o] = f2bf(ov);
+    }
+    rows_update_store<VPL, RPW, kBf16State>(sv, kv, al, delta, rows, Cfg::kRowBytes, lane);
+  }
+  cluster_wait();  // every CTA of the cluster is past its window reads
+  if (part == 0 && a.conv_w && tid < 2 * QG) {
+    int c0;
+    float* dst;
+    group_channels<DK, R>(tid, kh, a.Hk, buf, c0, dst);
+    float win[8][kConvW - 1];
+#pragma unroll
+    for (int ch = 0; ch < 8; ++ch)
+#pragma unroll
+      for (int j = 0; j < kConvW - 1; ++j) win[ch][j] = qkwin[tid][ch][j];
+    store_conv8<kF32Cache>(a.conv_state, a.conv_layout, s, a.D, c0, win);
+  }
+}
+
+// CTAs per unit for a call: 1 runs the persistent kernel. Calls that fill the GPU, gated
+// calls (the gate needs a whole head's o) and calls capped to part of the GPU (the mixed
+// step) take the persistent kernel.
+// Measured on GB300 (Qwen3-Next geometry, L2 flushed): the split kernel wins while a call
+// has at most half as many units as SMs (B <= 4: 10.4-12.2 us against 12.7-13.7 us for the
+// persistent kernel, fp32 state; ~10.3 against ~14 us with a bf16 state), P = 4 and P = 8
+// within 0.3 us of each other; from B = 8 the persistent kernel, which overlaps its setup
+// and streaming, is faster (14.6 against 17-18.5 us). Rows per CTA stay within [16, 128].
+template <int DK, int R>
+constexpr bool split_ok(int P) {
+  return R * DK / P >= 16 && R * DK / P <= 128 && P <= 8;
+}
+template <int DK, int R>
+int split_parts(const LayerArgs& a, int B) {
+  if (a.gated || a.max_ctas > 0) return 1;
+  const int64_t units = static_cast<int64_t>(B) * a.Hk;
+  if (units * 2 > sm_count()) return 1;
+  for (int p : {4, 8, 2})
+    if (split_ok<DK, R>(p)) return p;
+  return 1;
+}
+
+template <int DK, int R, bool kF32Cache, bool kBf16State, int P>
+cudaError_t launch_split(const LayerArgs& a, int B, cudaStream_t s) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(P, static_cast<unsigned>(B) * a.Hk, 1);
+  cfg.blockDim = dim3(SplitCfg<DK, R, kBf16State, P>::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = P;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, split_decode_kernel<DK, R, kF32Cache, kBf16State, P>, a);
+}
+
 template <int DK, int R, bool kF32Cache, bool kBf16State>
 cudaError_t launch_one(const LayerArgs& a, int B, cudaStream_t s) {
   using Cfg = DecodeCfg<DK, R, kBf16State>;
+  switch (split_parts<DK, R>(a, B)) {
+    case 2:
+      if constexpr (split_ok<DK, R>(2)) return launch_split<DK, R, kF32Cache, kBf16State, 2>(a, B, s);
+      break;
+    case 4:
+      if constexpr (split_ok<DK, R>(4)) return launch_split<DK, R, kF32Cache, kBf16State, 4>(a, B, s);
+      break;
+    case 8:
+      if constexpr (split_ok<DK, R>(8)) return launch_split<DK, R, kF32Cache, kBf16State, 8>(a, B, s);
+      break;
+    default: break;
+  }
   auto kern = decode_kernel<DK, R, kF32Cache, kBf16State>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        Cfg::kSmemBytes);

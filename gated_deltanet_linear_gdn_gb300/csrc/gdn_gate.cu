@@ -87,7 +87,7 @@ __global__ void __launch_bounds__(32 * kGateWarps)
 #pragma unroll
     for (int e = 0; e < VPL; ++e) ss = fmaf(o[e], o[e], ss);
     ss = warp_sum(ss);
-    const float den = ss / static_cast<float>(DV) + a.gate_eps;
+    const float den = __fadd_rn(__fdiv_rn(ss, static_cast<float>(DV)), a.gate_eps);
     const float inv = den > 0.0f ? 1.0f / sqrtf(den) : 0.0f;  // all-zero row, eps 0
     float y[VPL];
 #pragma unroll

@@ -93,4 +93,15 @@ __device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
+// Thread-block cluster barrier, split into its two halves. Every thread of every CTA of
+// the cluster executes arrive once, then wait once (warp-uniformly). arrive releases the
+// thread's earlier memory accesses; wait returns once every thread of the cluster has
+// arrived, and acquires what they released.
+__device__ __forceinline__ void cluster_arrive() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 }  // namespace gdn
