@@ -138,6 +138,7 @@ gdn_status prepare_prefill(const void* mixed_qkv, const void* a, const void* b,
   if (chunk != 16 && chunk != 32 && chunk != 64) return GDN_ERR_UNSUPPORTED;
   if (num_seqs == 0) return GDN_ERR_INVALID_ARG;  // (an empty call is the callers' no-op)
   if (num_seqs > 65535) return GDN_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(num_seqs) * dims.num_v_heads > 0x7fffffff) return GDN_ERR_UNSUPPORTED;
   if (!cu_seqlens) return GDN_ERR_INVALID_ARG;
   if (total_tokens == 0) {
     // no token is read or written: empty per-token arrays may be null

@@ -64,6 +64,24 @@ __device__ __forceinline__ float conv_tap_sum(const float (&win)[kConvW], const 
   return acc;
 }
 
+// conv_tap_sum for two channels at once, in packed f32x2 operations: per channel the same
+// roundings in the same order (so the same results), half the instructions for the taps.
+template <bool kF32Cache>
+__device__ __forceinline__ float2 conv_tap_sum2(const float2 (&win)[kConvW], const float2 (&w)[kConvW],
+                                                float2 bias) {
+  float2 acc = bias;
+#pragma unroll
+  for (int j = 0; j < kConvW; ++j) {
+    float2 p = __fmul2_rn(w[j], win[j]);
+    if (!kF32Cache) {
+      const uint32_t h = pack_bf2(p.x, p.y);
+      p = make_float2(__uint_as_float(h << 16), __uint_as_float(h & 0xFFFF0000u));
+    }
+    acc = __fadd2_rn(acc, p);
+  }
+  return acc;
+}
+
 __device__ __forceinline__ float silu_f(float x) { return __fdiv_rn(x, __fadd_rn(1.0f, expf(-x))); }
 
 // ---------------------------------------------------------------------------

@@ -44,16 +44,6 @@ __global__ void __launch_bounds__(kConvThreads) conv_update_kernel(ConvUpdateArg
   *out = pack8(h);
 }
 
-__device__ __forceinline__ int find_seq(const int32_t* cu, int n, int t) {
-  // largest i with cu[i] <= t (cu non-decreasing; cu[0] = 0 <= t < cu[n])
-  int lo = 0, hi = n - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (cu[mid] <= t) lo = mid; else hi = mid - 1;
-  }
-  return lo;
-}
-
 // Window tap j of token t: position p = t - (W-1) + j of its sequence; before
 // the sequence start it comes from the initial conv state (or zero).
 template <bool kF32Cache>
@@ -85,31 +75,110 @@ __device__ __forceinline__ void window8(const LayerArgs& a, const PrefillExtra& 
   unpack8(__ldg(reinterpret_cast<const uint4*>(x + static_cast<int64_t>(t) * a.D + c0)), x8);
 }
 
-// y[t, :] = conv output of token t (bf16). One block per token.
+// y[t, :] = conv output of token t (bf16) for every token of an active sequence (the
+// tokens of inactive ones are never read). A CTA covers a run of min(kConvRun, C) tokens
+// inside one chunk (so within one sequence, found in the chunk table) and 2 kConvRunThreads
+// channels; a thread keeps one channel pair for the run, so a warp reads 128 contiguous
+// bytes of each input row: the conv parameters are loaded once, the window is built once
+// (from x or, before the sequence start, the initial conv state) and then rolled in
+// registers, and the input rows come kConvBatch at a time with the next batch in flight
+// (the loads, 4 bytes each, need that depth to keep the memory system busy). The
+// per-channel arithmetic is conv_tap_sum and silu_f, as in the decode conv.
+constexpr int kConvRun = 32;
+constexpr int kConvBatch = 8;
+constexpr int kConvRunThreads = 256;
+
+// The W-1 taps before token t0 of channels c0, c0 + 1 (t0 in sequence i starting at bos):
+// positions before bos come from the initial conv state, or are zero without one.
 template <bool kF32Cache>
-__global__ void __launch_bounds__(kConvThreads)
-    prefill_conv_kernel(LayerArgs a, PrefillExtra p, const int32_t* seq_ok, uint16_t* y) {
-  __shared__ int s_seq;
-  const int t = blockIdx.x;
-  if (threadIdx.x == 0) s_seq = find_seq(p.cu_seqlens, p.num_seqs, t);
-  __syncthreads();
-  const int i = s_seq;
-  const int c0 = (blockIdx.y * kConvThreads + threadIdx.x) * 8;
-  if (c0 >= a.D) return;
-  uint4* yo = reinterpret_cast<uint4*>(y + static_cast<int64_t>(t) * a.D + c0);
-  if (!seq_ok[i]) {
-    *yo = make_uint4(0u, 0u, 0u, 0u);
-    return;
-  }
-  const int bos = p.cu_seqlens[i];
-  float win[8][kConvW - 1], x8[8], y8[8];
-  window8<kF32Cache>(a, p, i, bos, t, c0, win, x8);
-  conv8_step<kF32Cache>(win, x8, static_cast<const uint16_t*>(a.conv_w),
-                        static_cast<const uint16_t*>(a.conv_b), c0, a.silu != 0, y8);
-  uint16_t h[8];
+__device__ __forceinline__ void window2(const LayerArgs& a, const PrefillExtra& p, int i, int bos,
+                                        int t0, int c0, float (&win)[2][kConvW - 1]) {
+  const uint16_t* x = static_cast<const uint16_t*>(a.mixed);
+  const bool init = (p.has_init == nullptr) || (p.has_init[i] != 0);
+  const int64_t s = a.slot[i];
 #pragma unroll
-  for (int k = 0; k < 8; ++k) h[k] = f2bf(y8[k]);
-  *yo = pack8(h);
+  for (int j = 0; j < kConvW - 1; ++j) {
+    const int pos = t0 - (kConvW - 1) + j;
+    if (pos >= bos) {
+      const uint32_t v = *reinterpret_cast<const uint32_t*>(x + static_cast<int64_t>(pos) * a.D + c0);
+      win[0][j] = __uint_as_float(v << 16);
+      win[1][j] = __uint_as_float(v & 0xFFFF0000u);
+    } else if (!init) {
+      win[0][j] = win[1][j] = 0.0f;
+    } else {
+      const int jj = (kConvW - 1) + (pos - bos);  // tap of the initial window
+#pragma unroll
+      for (int ch = 0; ch < 2; ++ch) {
+        const int64_t idx = a.conv_layout == GDN_CONV_DIM_FIRST
+                                ? (s * a.D + c0 + ch) * (kConvW - 1) + jj
+                                : (s * (kConvW - 1) + jj) * a.D + c0 + ch;
+        win[ch][j] = kF32Cache ? static_cast<const float*>(a.conv_state)[idx]
+                               : bf2f(static_cast<const uint16_t*>(a.conv_state)[idx]);
+      }
+    }
+  }
+}
+
+template <bool kF32Cache>
+__global__ void __launch_bounds__(kConvRunThreads)
+    prefill_conv_kernel(LayerArgs a, PrefillExtra p, const int32_t* meta,
+                        const int32_t* chunk_off, const int32_t* chunk_seq, uint16_t* y) {
+  const int run = min(kConvRun, p.chunk), runs = p.chunk / run;
+  const int c = blockIdx.x / runs;
+  if (c >= meta[0]) return;
+  const int i = chunk_seq[c];
+  const int bos = p.cu_seqlens[i], eos = p.cu_seqlens[i + 1];
+  const int t0 = bos + (c - chunk_off[i]) * p.chunk + (blockIdx.x % runs) * run;
+  const int n = min(run, eos - t0);
+  const int c0 = (blockIdx.y * kConvRunThreads + threadIdx.x) * 2;
+  if (n <= 0 || c0 >= a.D) return;
+  const uint16_t* x = static_cast<const uint16_t*>(a.mixed) + c0;
+  float2 w[kConvW], bias;  // (channel c0, channel c0 + 1) pairs
+  {
+    const uint16_t* wp = static_cast<const uint16_t*>(a.conv_w) + static_cast<int64_t>(c0) * kConvW;
+    const uint4 wv = __ldg(reinterpret_cast<const uint4*>(wp));  // [2 channels][4 taps]
+    float wf[8];
+    unpack8(wv, wf);
+#pragma unroll
+    for (int j = 0; j < kConvW; ++j) w[j] = make_float2(wf[j], wf[kConvW + j]);
+    const uint16_t* bp = static_cast<const uint16_t*>(a.conv_b);
+    bias = bp ? make_float2(bf2f(bp[c0]), bf2f(bp[c0 + 1])) : make_float2(0.0f, 0.0f);
+  }
+  auto load_x = [&](int k) {  // input row t0 + k (zeros past the run)
+    return k < n ? __ldg(reinterpret_cast<const unsigned int*>(x + static_cast<int64_t>(t0 + k) * a.D))
+                 : 0u;
+  };
+  uint32_t xn[kConvBatch];
+#pragma unroll
+  for (int k = 0; k < kConvBatch; ++k) xn[k] = load_x(k);
+  float2 win[kConvW];  // taps 0 .. W-2 of the current token, then its input
+  {
+    float w2[2][kConvW - 1];
+    window2<kF32Cache>(a, p, i, bos, t0, c0, w2);
+#pragma unroll
+    for (int j = 0; j < kConvW - 1; ++j) win[j] = make_float2(w2[0][j], w2[1][j]);
+  }
+  uint16_t* yo = y + static_cast<int64_t>(t0) * a.D + c0;
+  const bool silu = a.silu != 0;
+#pragma unroll 1
+  for (int kb = 0; kb < n; kb += kConvBatch) {
+    uint32_t xc[kConvBatch];
+#pragma unroll
+    for (int k = 0; k < kConvBatch; ++k) {
+      xc[k] = xn[k];
+      xn[k] = load_x(kb + kConvBatch + k);
+    }
+#pragma unroll
+    for (int k = 0; k < kConvBatch; ++k) {
+      if (kb + k >= n) break;
+      win[kConvW - 1] = make_float2(__uint_as_float(xc[k] << 16), __uint_as_float(xc[k] & 0xFFFF0000u));
+      float2 acc = conv_tap_sum2<kF32Cache>(win, w, bias);
+      if (silu) acc = make_float2(silu_f(acc.x), silu_f(acc.y));
+#pragma unroll
+      for (int j = 0; j < kConvW - 1; ++j) win[j] = win[j + 1];
+      *reinterpret_cast<uint32_t*>(yo + static_cast<int64_t>(kb + k) * a.D) = pack_bf2(acc.x, acc.y);
+    }
+  }
 }
 
 // Final conv window of each sequence = last W-1 entries of (initial ++ x).
@@ -156,14 +225,19 @@ cudaError_t launch_conv_update(const ConvUpdateArgs& a, cudaStream_t s) {
   return cudaGetLastError();
 }
 
-cudaError_t launch_prefill_conv(const LayerArgs& a, const PrefillExtra& p, const int32_t* seq_ok,
-                                uint16_t* y, cudaStream_t s) {
+cudaError_t launch_prefill_conv(const LayerArgs& a, const PrefillExtra& p, const int32_t* meta,
+                                const int32_t* seq_ok, const int32_t* chunk_off,
+                                const int32_t* chunk_seq, int max_chunks, uint16_t* y,
+                                cudaStream_t s) {
   const int groups = a.D / 8;
   const int gy = (groups + kConvThreads - 1) / kConvThreads;
-  if (p.total_tokens > 0) {
-    dim3 grid(p.total_tokens, gy);
-    if (a.conv_f32) prefill_conv_kernel<true><<<grid, kConvThreads, 0, s>>>(a, p, seq_ok, y);
-    else prefill_conv_kernel<false><<<grid, kConvThreads, 0, s>>>(a, p, seq_ok, y);
+  if (max_chunks > 0) {
+    dim3 grid(static_cast<unsigned>(max_chunks) * (p.chunk / min(kConvRun, p.chunk)),
+              (a.D / 2 + kConvRunThreads - 1) / kConvRunThreads);
+    if (a.conv_f32)
+      prefill_conv_kernel<true><<<grid, kConvRunThreads, 0, s>>>(a, p, meta, chunk_off, chunk_seq, y);
+    else
+      prefill_conv_kernel<false><<<grid, kConvRunThreads, 0, s>>>(a, p, meta, chunk_off, chunk_seq, y);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }

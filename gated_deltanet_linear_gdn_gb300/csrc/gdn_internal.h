@@ -101,16 +101,21 @@ size_t prefill_workspace_bytes(int total_tokens, int num_seqs, int Hk, int Hv, i
                                int chunk, int conv);
 
 // chunk table + sequence checks (gdn_prefill.cu): meta[0] = number of chunks,
-// seq_ok[i], chunk_off[N+1] (first chunk of each sequence), chunk_seq[chunk]
+// seq_ok[i], chunk_off[N+1] (first chunk of each sequence), chunk_seq[chunk], and (when
+// seq_order is not null) seq_order[N], the sequences by descending chunk count
 cudaError_t launch_prefill_prep(const LayerArgs& a, const PrefillExtra& p, int32_t* meta,
                                 int32_t* seq_ok, int32_t* chunk_off, int32_t* chunk_seq,
-                                cudaStream_t s);
+                                int32_t* seq_order, cudaStream_t s);
 // tensor-core path for dk = dv = 128 (gdn_prefill_tc.cu)
 size_t prefill_tc_workspace_bytes(int total_tokens, int num_seqs, int Hk, int Hv, int chunk);
 cudaError_t launch_prefill_tc(const LayerArgs& a, const PrefillExtra& p, cudaStream_t s);
 
-// prefill helpers implemented in gdn_conv.cu
-cudaError_t launch_prefill_conv(const LayerArgs& a, const PrefillExtra& p, const int32_t* seq_ok,
-                                uint16_t* y, cudaStream_t s);
+// prefill helpers implemented in gdn_conv.cu: the conv output y of every token of an active
+// sequence (over the chunk table of launch_prefill_prep), then each active sequence's final
+// conv window
+cudaError_t launch_prefill_conv(const LayerArgs& a, const PrefillExtra& p, const int32_t* meta,
+                                const int32_t* seq_ok, const int32_t* chunk_off,
+                                const int32_t* chunk_seq, int max_chunks, uint16_t* y,
+                                cudaStream_t s);
 
 }  // namespace gdn

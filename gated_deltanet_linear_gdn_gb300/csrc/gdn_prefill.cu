@@ -66,9 +66,12 @@ WsLayout ws_layout(int T, int N, int Hv, int dk, int dv, int C, int conv, int D)
 }
 
 // ---------------------------------------------------------------- prep
+constexpr int kOrderMaxSeqs = 1024;  // sequences ranked by length; identity order beyond
+
 __global__ void prep_kernel(LayerArgs a, PrefillExtra p, int32_t* meta, int32_t* seq_ok,
-                            int32_t* chunk_off, int32_t* chunk_seq) {
+                            int32_t* chunk_off, int32_t* chunk_seq, int32_t* seq_order) {
   __shared__ int s_valid;
+  __shared__ int s_cnt[kOrderMaxSeqs];
   const int N = p.num_seqs, C = p.chunk;
   if (threadIdx.x == 0) {
     int valid = p.cu_seqlens[0] == 0 && p.cu_seqlens[N] == p.total_tokens;
@@ -97,6 +100,21 @@ __global__ void prep_kernel(LayerArgs a, PrefillExtra p, int32_t* meta, int32_t*
   __syncthreads();
   for (int i = threadIdx.x; i < N; i += blockDim.x)
     for (int c = chunk_off[i]; c < chunk_off[i + 1]; ++c) chunk_seq[c] = i;
+  if (seq_order == nullptr) return;
+  // seq_order[r] = the sequence of rank r by descending chunk count (ties by index): a state
+  // pass launched in this order starts its longest chains first
+  if (N > kOrderMaxSeqs) {
+    for (int i = threadIdx.x; i < N; i += blockDim.x) seq_order[i] = i;
+    return;
+  }
+  for (int i = threadIdx.x; i < N; i += blockDim.x) s_cnt[i] = chunk_off[i + 1] - chunk_off[i];
+  __syncthreads();
+  for (int i = threadIdx.x; i < N; i += blockDim.x) {
+    const int ci = s_cnt[i];
+    int r = 0;
+    for (int j = 0; j < N; ++j) r += (s_cnt[j] > ci) || (s_cnt[j] == ci && j < i);
+    seq_order[r] = i;
+  }
 }
 
 // ---------------------------------------------------------------- intra-chunk
@@ -432,12 +450,12 @@ cudaError_t launch_prefill_dk(const LayerArgs& a, const PrefillExtra& p, cudaStr
   float* Pb = reinterpret_cast<float*>(ws + L.P);
   float* Gb = reinterpret_cast<float*>(ws + L.G);
 
-  prep_kernel<<<1, 256, 0, s>>>(a, p, meta, seq_ok, chunk_off, chunk_seq);
+  prep_kernel<<<1, 256, 0, s>>>(a, p, meta, seq_ok, chunk_off, chunk_seq, nullptr);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const uint16_t* y = static_cast<const uint16_t*>(a.mixed);
   if (a.conv_w) {
-    e = launch_prefill_conv(a, p, seq_ok, ybuf, s);
+    e = launch_prefill_conv(a, p, meta, seq_ok, chunk_off, chunk_seq, L.max_chunks, ybuf, s);
     if (e != cudaSuccess) return e;
     y = ybuf;
   }
@@ -463,8 +481,8 @@ cudaError_t launch_prefill_dk(const LayerArgs& a, const PrefillExtra& p, cudaStr
 
 cudaError_t launch_prefill_prep(const LayerArgs& a, const PrefillExtra& p, int32_t* meta,
                                 int32_t* seq_ok, int32_t* chunk_off, int32_t* chunk_seq,
-                                cudaStream_t s) {
-  prep_kernel<<<1, 256, 0, s>>>(a, p, meta, seq_ok, chunk_off, chunk_seq);
+                                int32_t* seq_order, cudaStream_t s) {
+  prep_kernel<<<1, 256, 0, s>>>(a, p, meta, seq_ok, chunk_off, chunk_seq, seq_order);
   return cudaGetLastError();
 }
 

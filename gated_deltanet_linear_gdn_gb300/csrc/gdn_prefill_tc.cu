@@ -56,7 +56,7 @@ constexpr uint32_t kTmemCols = 512;
 constexpr int kVecFloats = 256;  // per (chunk, head): f[C], dd[C], g_last
 
 struct TcLayout {
-  size_t meta, seq_ok, chunk_off, chunk_seq, ybuf, Qt, Kt, Wt, Pt, Ut, vec, total;
+  size_t meta, seq_ok, chunk_off, chunk_seq, seq_order, ybuf, Qt, Kt, Wt, Pt, Ut, vec, total;
   int max_chunks;
   // per-tile byte sizes
   size_t q_tile, w_tile, p_tile, u_tile;
@@ -77,6 +77,7 @@ TcLayout tc_layout(int T, int N, int Hk, int Hv, int C, int D) {
   L.seq_ok = off; off = align256(off + static_cast<size_t>(N) * sizeof(int32_t));
   L.chunk_off = off; off = align256(off + static_cast<size_t>(N + 1) * sizeof(int32_t));
   L.chunk_seq = off; off = align256(off + static_cast<size_t>(mc + 1) * sizeof(int32_t));
+  L.seq_order = off; off = align256(off + static_cast<size_t>(N) * sizeof(int32_t));
   L.ybuf = off; off = align256(off + static_cast<size_t>(T) * D * sizeof(uint16_t));
   L.Qt = off; off = align256(off + static_cast<size_t>(mc) * Hk * L.q_tile);
   L.Kt = off; off = align256(off + static_cast<size_t>(mc) * Hk * L.q_tile);
@@ -638,13 +639,14 @@ struct PassSmem {
 template <int C>
 __global__ void __launch_bounds__(kPassThreads, 1)
     pass_tc_kernel(LayerArgs a, PrefillExtra p, const int32_t* seq_ok, const int32_t* chunk_off,
-                   TcBufs wb) {
+                   const int32_t* seq_order, TcBufs wb) {
   using S = PassSmem<C>;
   extern __shared__ __align__(1024) unsigned char sm[];
   __shared__ uint32_t s_tmem;
   __shared__ __align__(8) uint64_t s_bar[6];  // fullA, fullB, mma1, mma2, fullU, oDone
 
-  const int i = blockIdx.x, h = blockIdx.y;
+  // CTAs in launch order take the sequences longest first, all value heads of one together
+  const int i = seq_order[blockIdx.x / a.Hv], h = blockIdx.x % a.Hv;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int bos = p.cu_seqlens[i], eos = p.cu_seqlens[i + 1];
   if (!seq_ok[i]) {  // inactive / invalid sequence (or bad cu_seqlens): zero outputs
@@ -1041,6 +1043,7 @@ cudaError_t launch_tc_c(const LayerArgs& a, const PrefillExtra& p, const TcLayou
   const int32_t* seq_ok = reinterpret_cast<const int32_t*>(ws + L.seq_ok);
   const int32_t* chunk_off = reinterpret_cast<const int32_t*>(ws + L.chunk_off);
   const int32_t* chunk_seq = reinterpret_cast<const int32_t*>(ws + L.chunk_seq);
+  const int32_t* seq_order = reinterpret_cast<const int32_t*>(ws + L.seq_order);
   TcBufs wb;
   wb.Qt = reinterpret_cast<unsigned char*>(ws + L.Qt);
   wb.Kt = reinterpret_cast<unsigned char*>(ws + L.Kt);
@@ -1066,7 +1069,8 @@ cudaError_t launch_tc_c(const LayerArgs& a, const PrefillExtra& p, const TcLayou
   e = cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, PassSmem<C>::kBytes);
   if (e != cudaSuccess) return e;
   if (p.before_pass && (e = cudaEventRecord(p.before_pass, s)) != cudaSuccess) return e;
-  k2<<<dim3(p.num_seqs, a.Hv), kPassThreads, PassSmem<C>::kBytes, s>>>(a, p, seq_ok, chunk_off, wb);
+  k2<<<static_cast<unsigned>(p.num_seqs) * a.Hv, kPassThreads, PassSmem<C>::kBytes, s>>>(
+      a, p, seq_ok, chunk_off, seq_order, wb);
   return cudaGetLastError();
 }
 
@@ -1083,12 +1087,13 @@ cudaError_t launch_prefill_tc(const LayerArgs& a, const PrefillExtra& p, cudaStr
   int32_t* seq_ok = reinterpret_cast<int32_t*>(ws + L.seq_ok);
   int32_t* chunk_off = reinterpret_cast<int32_t*>(ws + L.chunk_off);
   int32_t* chunk_seq = reinterpret_cast<int32_t*>(ws + L.chunk_seq);
-  cudaError_t e = launch_prefill_prep(a, p, meta, seq_ok, chunk_off, chunk_seq, s);
+  int32_t* seq_order = reinterpret_cast<int32_t*>(ws + L.seq_order);
+  cudaError_t e = launch_prefill_prep(a, p, meta, seq_ok, chunk_off, chunk_seq, seq_order, s);
   if (e != cudaSuccess) return e;
   const uint16_t* y = static_cast<const uint16_t*>(a.mixed);
   if (a.conv_w) {
     uint16_t* ybuf = reinterpret_cast<uint16_t*>(ws + L.ybuf);
-    e = launch_prefill_conv(a, p, seq_ok, ybuf, s);
+    e = launch_prefill_conv(a, p, meta, seq_ok, chunk_off, chunk_seq, L.max_chunks, ybuf, s);
     if (e != cudaSuccess) return e;
     y = ybuf;
   }
