@@ -178,43 +178,61 @@ __device__ __forceinline__ void fma4x4(float (&acc)[4][4], const float4 (&a)[4],
   }
 }
 
-// barrier of the intra kernel's four solver warps (warps 0-3; named barrier 1)
-__device__ __forceinline__ void solver_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+// barrier of the intra kernel's two solver warps (warps 0-1; named barrier 1)
+__device__ __forceinline__ void solver_sync() { asm volatile("bar.sync 1, 64;" ::: "memory"); }
 
 // ============================================================== intra kernel
+// A CTA takes 64 token rows (64 / C chunks) of one k-head, so that two CTAs fit on an SM
+// (shared memory and 256 tensor-memory columns each) and each hides the other's latency.
+// The raw products k_t . k_j and q_t . k_j do not depend on the value head, so one MMA over
+// the stacked operand [K; Q] (M = 128) computes both once per CTA: tensor-memory lanes 0..63
+// hold G = K K^T and lanes 64..127 QK = Q K^T, columns [0, 64). Per value head:
+//   A rows (warps on lanes 0..63) and P rows (warps on lanes 64..127) from them,
+//   the fp32 solve of T = (I + A)^-1 per chunk,
+//   T' = T diag(beta) and T'' = T diag(beta e^G ik), both split into bf16 hi + lo,
+//   U^T = V^T T'^T (columns [64, 128), a dv row per lane) with V raw bf16, and
+//   W = T'' K (columns [128, 256), a token per lane) with K raw bf16 -- W = T diag(beta)
+//   diag(e^G ik) K, the diagonal scaling moved onto T, so K enters exactly.
+// The W MMA keeps M = 128: rows 64..127 of its A operand read the next buffer in shared
+// memory, and those accumulator lanes are never read.
 template <int C>
 struct IntraSmem {
-  static constexpr int CPC = 128 / C;                // chunks per CTA
-  static constexpr int kTile = 128 * 128 * 2;        // bf16 [128 x 128]
-  // phase 1: sQ, sK: the raw q, k rows [128 tokens x 128] (K-major operands of the Gram
-  //          and QK^T products)
-  // phase 2: sK stays; sKh (aliases sQ) and sKl hold K' hi / lo, sV the V rows -- all three
-  //          MN-major operands over tokens in the same layout -- sTh / sTl the T' operand, sA
-  static constexpr int oQ = 0, oK = kTile, oKl = 2 * kTile;
-  static constexpr int oTh = 3 * kTile, oTl = 4 * kTile, oV = 5 * kTile;
-  // fp32 A [128][C + 4] (16-byte rows), then T in place; a row's 4 padding floats hold its
-  // token's K' scale, beta and q / k norm factors
+  static constexpr int kRows = 64;                   // token rows per CTA
+  static constexpr int CPC = kRows / C;              // chunks per CTA
+  static constexpr int kTile = kRows * 128 * 2;      // bf16 [64 x 128]
+  static constexpr int kTT = kRows * kRows * 2;      // bf16 [64 x 64]
+  // sK, sQ: raw k, q rows (K-major [64 x 128]), adjacent: together the [K; Q] operand;
+  // sV: V rows (MN-major use, the same layout); sT2h/l: T'' (A operand of W), sT1h/l: T'
+  // (B operand of U^T), K-major [64 x 64]. The W operands sT2h and sT2l are read 64 rows
+  // past their ends, which must stay inside this block.
+  static constexpr int oK = 0, oQ = kTile, oV = 2 * kTile;
+  static constexpr int oT2h = 3 * kTile, oT2l = oT2h + kTT, oT1h = oT2l + kTT, oT1l = oT1h + kTT;
+  // fp32 A [64][C + 4] (16-byte rows), then T in place; a row's 4 padding floats hold its
+  // token's e^G ik, beta and q / k norm factors
   static constexpr int kSA = C + 4;
-  static constexpr int oA = 6 * kTile;
-  static constexpr int oG = oA + 128 * kSA * 4;      // cumulative log-gates G: 128 floats
-  // the mbarrier, the tensor-memory base and the chunk table live here too: static shared
-  // variables would be padded to 1 KB ahead of the 1 KB-aligned dynamic block
-  static constexpr int oBar = oG + 128 * 4, oTmem = oBar + 8, oT0 = oTmem + 8;
+  static constexpr int oA = oT1l + kTT;
+  static constexpr int oG = oA + kRows * kSA * 4;    // cumulative log-gates G: 64 floats
+  static constexpr int oPart = oG + kRows * 4;       // partial squared norms [2][2][64]
+  static constexpr int oBar = oPart + 4 * kRows * 4, oTmem = oBar + 8, oT0 = oTmem + 8;
   static constexpr int kBytes = oT0 + 2 * CPC * 4;
-  static_assert(kBytes <= 227 * 1024, "intra shared memory exceeds the per-CTA limit");
+  static_assert(oT1h - oT2h >= kTT && oT1l - oT2l >= kTT, "M = 128 reads stay in the block");
+  static_assert(kBytes <= 113 * 1024, "two intra CTAs must fit on an SM");
 };
+constexpr uint32_t kIntraTmemCols = 256;
+constexpr int kColGQ = 0, kColU = 64, kColW = 128;  // tensor-memory columns of G|QK, U^T, W
 
 template <int C>
-__global__ void __launch_bounds__(kThreadsTc, 1)
+__global__ void __launch_bounds__(kThreadsTc, 2)
     intra_tc_kernel(LayerArgs a, PrefillExtra p, const uint16_t* __restrict__ y,
                     const int32_t* meta, const int32_t* chunk_off, const int32_t* chunk_seq,
                     TcBufs wb) {
   using S = IntraSmem<C>;
-  constexpr int CPC = S::CPC;
+  constexpr int CPC = S::CPC, NR = S::kRows;
   extern __shared__ __align__(1024) unsigned char sm[];
   float* sA = reinterpret_cast<float*>(sm + S::oA);
   constexpr int SA = S::kSA;
   float* s_G = reinterpret_cast<float*>(sm + S::oG);
+  float* s_part = reinterpret_cast<float*>(sm + S::oPart);
   // per-token values in A's row padding
   constexpr int kSc = 0, kBeta = 1, kIq = 2, kIk = 3;
   auto pad = [&](int t, int k) -> float& { return sA[t * SA + C + k]; };
@@ -241,76 +259,67 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   }
   __syncthreads();
 
-  // ---- phase 1: raw q, k rows -> tensor-core tiles; norms ----
+  // ---- phase 1: raw q, k rows -> tensor-core tiles; norms. Thread: token row tok, q or k,
+  // half of the 128 channels ----
   {
-    const int tok = tid & 127, which = tid >> 7;  // 0: q, 1: k
+    const int tok = tid & 63, which = (tid >> 6) & 1, hf = tid >> 7;
     const int ci = tok / C, tl = tok % C;
     const bool valid = tl < s_L[ci];
-    const int col0 = which ? (a.Hk + kh) * kD : kh * kD;
+    const int col0 = (which ? (a.Hk + kh) * kD : kh * kD) + 64 * hf;
     unsigned char* tile = sm + (which ? S::oK : S::oQ);
     const uint16_t* row = y + static_cast<int64_t>(s_t0[ci] + tl) * a.D + col0;
+    uint4 v[8];
+#pragma unroll
+    for (int k8 = 0; k8 < 8; ++k8)
+      v[k8] = valid ? __ldg(reinterpret_cast<const uint4*>(row) + k8) : make_uint4(0u, 0u, 0u, 0u);
     float ss = 0.0f;
-#pragma unroll 4
-    for (int k8 = 0; k8 < kD / 8; ++k8) {
-      uint4 v = make_uint4(0u, 0u, 0u, 0u);
-      if (valid) v = __ldg(reinterpret_cast<const uint4*>(row) + k8);
+#pragma unroll
+    for (int k8 = 0; k8 < 8; ++k8) {
       float f[8];
-      unpack8(v, f);
+      unpack8(v[k8], f);
 #pragma unroll
       for (int e = 0; e < 8; ++e) ss = fmaf(f[e], f[e], ss);
-      *reinterpret_cast<uint4*>(tile + tc::kmajor_offset(tok, 8 * k8, kD)) = v;
+      *reinterpret_cast<uint4*>(tile + tc::kmajor_offset(tok, 64 * hf + 8 * k8, kD)) = v[k8];
     }
-    const float inv = a.qk_l2norm ? 1.0f / sqrtf(ss + 1e-6f) : 1.0f;
-    pad(tok, which ? kIk : kIq) = inv;
+    s_part[(hf * 2 + which) * NR + tok] = ss;
   }
-  if (warp == 0) tc::tmem_alloc(s_tmem, kTmemCols);
+  if (CPC > 1) {  // block-diagonal T' and T'': the off-diagonal blocks stay zero
+    for (int i = tid; i < 4 * S::kTT / 16; i += kThreadsTc)
+      reinterpret_cast<uint4*>(sm + S::oT2h)[i] = make_uint4(0u, 0u, 0u, 0u);
+  }
+  if (warp == 0) {
+    tc::tmem_alloc(s_tmem, kIntraTmemCols);
+    // gives up this CTA's right to allocate again: until a CTA that may still allocate tensor
+    // memory has done so, the SM starts no other such CTA (measured: one CTA per SM without
+    // this, two with it)
+    tc::tmem_relinquish();
+  }
   if (tid == 0) {
     mbar_init(bar, 1);
     fence_mbar_init();
   }
   tc_sync(false);
   const uint32_t tb = *s_tmem;
+  if (tid == 0) {  // [K; Q] K^T: G in lanes 0..63, QK in lanes 64..127, once per CTA
+    const uint32_t id = tc::idesc_bf16_f32(128, NR);
+    const uint32_t ak = smem_addr(sm + S::oK);
+    for (int ks = 0; ks < kD / 16; ++ks)
+      tc::mma_bf16(tb + kColGQ, tc::kmajor_desc(ak, kD, ks), tc::kmajor_desc(ak, kD, ks), id, ks > 0);
+    tc::mma_commit(bar);
+  }
+  if (tid < 2 * NR) {  // the two halves' sums, in a fixed order
+    const int tok = tid & 63, which = tid >> 6;
+    const float ss = s_part[which * NR + tok] + s_part[(2 + which) * NR + tok];
+    pad(tok, which ? kIk : kIq) = a.qk_l2norm ? 1.0f / sqrtf(ss + 1e-6f) : 1.0f;
+  }
   uint32_t phase = 0;
   bool bad = false;
 
-  if (tid == 0) {  // G = K K^T (cols 0..127), QK = Q K^T (cols 128..255)
-    const uint32_t id = tc::idesc_bf16_f32(128, 128);
-    const uint32_t aq = smem_addr(sm + S::oQ), ak = smem_addr(sm + S::oK);
-    for (int ks = 0; ks < kD / 16; ++ks)
-      tc::mma_bf16(tb, tc::kmajor_desc(ak, kD, ks), tc::kmajor_desc(ak, kD, ks), id, ks > 0);
-    for (int ks = 0; ks < kD / 16; ++ks)
-      tc::mma_bf16(tb + 128, tc::kmajor_desc(aq, kD, ks), tc::kmajor_desc(ak, kD, ks), id, ks > 0);
-    tc::mma_commit(bar);
-  }
-  // q and k tiles of each chunk -> workspace (read-only use of the smem tiles; a chunk's
-  // rows are one contiguous slice of either tile)
-  for (int ci = 0; ci < CPC; ++ci) {
-    const int c = c_first + ci;
-    if (c >= nchunks) break;
-    const size_t slice = static_cast<size_t>(C) * kD * 2;  // bytes of one chunk's tile
-    const uint4* srcq = reinterpret_cast<const uint4*>(sm + S::oQ + ci * slice);
-    const uint4* srck = reinterpret_cast<const uint4*>(sm + S::oK + ci * slice);
-    uint4* dq = reinterpret_cast<uint4*>(wb.Qt + (static_cast<size_t>(c) * a.Hk + kh) * wb.q_tile);
-    uint4* dk = reinterpret_cast<uint4*>(wb.Kt + (static_cast<size_t>(c) * a.Hk + kh) * wb.q_tile);
-    for (int i = tid; i < static_cast<int>(slice / 16); i += kThreadsTc) {
-      dq[i] = srcq[i];
-      dk[i] = srck[i];
-    }
-  }
-  if (!mbar_wait_bounded(bar, phase)) bad = true;
-  phase ^= 1;
-  bad = tc_sync(bad);
-
-  // ---- phase 2: per value head ----
-  if (!bad) {
-    for (int i = tid; i < 2 * S::kTile / 16; i += kThreadsTc)  // block-diagonal T: zero all
-      reinterpret_cast<uint4*>(sm + S::oTh)[i] = make_uint4(0u, 0u, 0u, 0u);
-  }
   const int R = a.Hv / a.Hk;
   for (int hr = 0; hr < R && !bad; ++hr) {
     const int h = kh * R + hr;
-    // gates of the 128 token rows, then the running sums per chunk
-    if (tid < 128) {
+    // gates of the 64 token rows, then the running sums per chunk
+    if (tid < NR) {
       const int ci = tid / C, tl = tid % C;
       float g = 0.0f, be = 0.0f;
       if (tl < s_L[ci])
@@ -324,63 +333,75 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       float run = 0.0f;
       for (int t = 0; t < C; ++t) { run += s_G[tid * C + t]; s_G[tid * C + t] = run; }
     }
+    if (hr == 0) {  // the G | QK product (issued once)
+      if (!mbar_wait_bounded(bar, phase)) bad = true;
+      bad = __any_sync(0xffffffffu, bad);
+      phase ^= 1;
+      tc::fence_after_sync();
+    }
     __syncthreads();
 
-    // A and P rows from tensor memory. Thread: row t, column half `half`.
-    {
-      const int t = 32 * (warp & 3) + lane, half = warp >> 2;
+    // A rows (warps on lanes 0..63, G) and P rows (warps on lanes 64..127, QK) from tensor
+    // memory; thread: row t, column half `half`
+    if (!bad) {
+      const int q4 = warp & 3, half = warp >> 2;
+      const bool is_p = q4 >= 2;
+      const int t = 32 * (q4 & 1) + lane;
       const int ci = t / C, tl = t % C;
       const int c = c_first + ci;
       const bool live = c < nchunks && tl < s_L[ci];
-      const float Gt = s_G[t], bt = pad(t, kBeta), ikt = pad(t, kIk), iqt = pad(t, kIq) * a.scale;
+      const float Gt = s_G[t];
       constexpr int NH = C / 2;  // columns per thread
       // tcgen05.ld is warp-collective with one column address per warp, so the
       // columns must not depend on the lane: for C >= 32 the warp's 32 rows lie
       // in one chunk; for C = 16 they span two chunks, both are loaded and each
       // lane keeps its own.
-      float gv[NH], qv[NH];
+      float xv[NH];
       if constexpr (C >= 32) {
-        const int cw = (32 * (warp & 3)) / C;  // the warp's chunk
+        const int cw = (32 * (q4 & 1)) / C;  // the warp's chunk
 #pragma unroll
         for (int b0 = 0; b0 < NH; b0 += 16) {
-          float tg[16], tq[16];
-          tmem_load<16>(tc::taddr(tb, 32 * (warp & 3), cw * C + half * NH + b0), tg);
-          tmem_load<16>(tc::taddr(tb, 32 * (warp & 3), 128 + cw * C + half * NH + b0), tq);
+          float tv[16];
+          tmem_load<16>(tc::taddr(tb, 32 * q4, kColGQ + cw * C + half * NH + b0), tv);
 #pragma unroll
-          for (int e = 0; e < 16; ++e) { gv[b0 + e] = tg[e]; qv[b0 + e] = tq[e]; }
+          for (int e = 0; e < 16; ++e) xv[b0 + e] = tv[e];
         }
       } else {
-        const int col0 = 32 * (warp & 3) + half * NH;  // chunk 2q's half; +16: chunk 2q+1
-        float ga[8], gb[8], qa[8], qb[8];
-        tmem_load<8>(tc::taddr(tb, 32 * (warp & 3), col0), ga);
-        tmem_load<8>(tc::taddr(tb, 32 * (warp & 3), col0 + 16), gb);
-        tmem_load<8>(tc::taddr(tb, 32 * (warp & 3), 128 + col0), qa);
-        tmem_load<8>(tc::taddr(tb, 32 * (warp & 3), 128 + col0 + 16), qb);
+        const int col0 = 32 * (q4 & 1) + half * NH;  // chunk 2q's half; +16: chunk 2q+1
+        float xa[8], xb[8];
+        tmem_load<8>(tc::taddr(tb, 32 * q4, kColGQ + col0), xa);
+        tmem_load<8>(tc::taddr(tb, 32 * q4, kColGQ + col0 + 16), xb);
         const bool second = lane >= 16;
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          gv[e] = second ? gb[e] : ga[e];
-          qv[e] = second ? qb[e] : qa[e];
-        }
+        for (int e = 0; e < 8; ++e) xv[e] = second ? xb[e] : xa[e];
       }
       tc::tmem_wait_ld();
-      float pv[NH], av[NH];
+      if (!is_p) {
+        const float bt = pad(t, kBeta), ikt = pad(t, kIk);
+        float av[NH];
 #pragma unroll
-      for (int e = 0; e < NH; ++e) {
-        const int j = half * NH + e;
-        const int tj = ci * C + j;
-        const float dec = (live && j <= tl) ? expf(Gt - s_G[tj]) : 0.0f;
-        const float iktj = pad(tj, kIk);
-        av[e] = (j < tl) ? bt * dec * ikt * iktj * gv[e] : 0.0f;
-        pv[e] = dec * iqt * iktj * qv[e];
-      }
+        for (int e = 0; e < NH; ++e) {
+          const int j = half * NH + e;
+          const int tj = ci * C + j;
+          const float dec = (live && j < tl) ? expf(Gt - s_G[tj]) : 0.0f;
+          av[e] = (j < tl) ? bt * dec * ikt * pad(tj, kIk) * xv[e] : 0.0f;
+        }
 #pragma unroll
-      for (int e = 0; e < NH; e += 4)  // the thread's half row of A, 16 bytes at a time
-        *reinterpret_cast<float4*>(sA + t * SA + half * NH + e) =
-            make_float4(av[e], av[e + 1], av[e + 2], av[e + 3]);
-      // the token's K' scale e^{G_t} ik_t (the solve reads columns 0 .. C-1 only)
-      if (half == 0) pad(t, kSc) = live ? expf(Gt) * ikt : 0.0f;
-      if (c < nchunks) {
+        for (int e = 0; e < NH; e += 4)  // the thread's half row of A, 16 bytes at a time
+          *reinterpret_cast<float4*>(sA + t * SA + half * NH + e) =
+              make_float4(av[e], av[e + 1], av[e + 2], av[e + 3]);
+        // the token's W scale e^{G_t} ik_t (the solve reads columns 0 .. C-1 only)
+        if (half == 0) pad(t, kSc) = live ? expf(Gt) * ikt : 0.0f;
+      } else if (c < nchunks) {
+        const float iqt = pad(t, kIq) * a.scale;
+        float pv[NH];
+#pragma unroll
+        for (int e = 0; e < NH; ++e) {
+          const int j = half * NH + e;
+          const int tj = ci * C + j;
+          const float dec = (live && j <= tl) ? expf(Gt - s_G[tj]) : 0.0f;
+          pv[e] = dec * iqt * pad(tj, kIk) * xv[e];
+        }
         unsigned char* ph = wb.Pt + (static_cast<size_t>(c) * a.Hv + h) * 2 * wb.p_tile;
 #pragma unroll
         for (int e8 = 0; e8 < NH; e8 += 8) {
@@ -396,15 +417,17 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         if (half == 0) {
           float* vec = wb.vec + (static_cast<size_t>(c) * a.Hv + h) * kVecFloats;
           const float Glast = s_G[ci * C + max(s_L[ci] - 1, 0)];
-          vec[tl] = live ? expf(Gt) * iqt : 0.0f;            // f_t
+          const float ikt = pad(t, kIk);
+          vec[tl] = live ? expf(Gt) * iqt : 0.0f;               // f_t
           vec[64 + tl] = live ? expf(Glast - Gt) * ikt : 0.0f;  // dd_t
-          if (tl == 0) vec[128] = expf(Glast);               // g_last
+          if (tl == 0) vec[128] = expf(Glast);                  // g_last
         }
       }
     }
-    __syncthreads();
+    bad = tc_sync(bad);
+    if (bad) break;
 
-    if (tid < 128) {
+    if (tid < NR) {
       // exact fp32 T = (I + A)^-1 of every chunk, written over A in place (A is strictly lower
       // triangular, so its upper part already holds T's zeros)
       // 1) diagonal blocks of B1 = min(C, 32) rows: forward substitution, a column per thread,
@@ -432,10 +455,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         for (int r = 0; r < B1; ++r) Ab[r * SA + c] = x[r];
       }
       if constexpr (C == 64) {
-        // 2) the off-diagonal block T21 = -T22 (A21 T11) of each chunk (T11, T22 now in place
-        //    of A11, A22): 64 threads per chunk, 4 x 4 outputs each from 16-byte row loads
-        const int k = tid & 63, r0 = 4 * (k >> 3), c0 = 4 * (k & 7);
-        float* Ac = sA + (tid >> 6) * C * SA;
+        // 2) the off-diagonal block T21 = -T22 (A21 T11) (T11, T22 now in place of A11, A22):
+        //    64 threads, 4 x 4 outputs each from 16-byte row loads
+        const int k = tid, r0 = 4 * (k >> 3), c0 = 4 * (k & 7);
+        float* Ac = sA;
         float acc[4][4];
         solver_sync();
 #pragma unroll
@@ -483,8 +506,9 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
               make_float4(-acc[i][0], -acc[i][1], -acc[i][2], -acc[i][3]);
       }
       solver_sync();
-      // 3) T' = T diag(beta) into the block-diagonal bf16 hi / lo tiles: row tid, 8 columns at a
-      //    time, 16-byte stores (the warp's lanes on consecutive rows)
+      // 3) T' = T diag(beta) and T'' = T diag(beta e^G ik) into the block-diagonal bf16 hi / lo
+      //    tiles: row tid, 8 columns at a time, 16-byte stores (the warp's lanes on consecutive
+      //    rows)
       {
         const int t = tid, ci = t / C;
         const float* Tr = sA + t * SA;
@@ -492,72 +516,82 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         for (int g = 0; g < C / 8; ++g) {
           const float4 u0 = *reinterpret_cast<const float4*>(Tr + 8 * g);
           const float4 u1 = *reinterpret_cast<const float4*>(Tr + 8 * g + 4);
+          const float tv[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
           const int jb = ci * C + 8 * g;
-          const float x[8] = {u0.x * pad(jb, kBeta),     u0.y * pad(jb + 1, kBeta),
-                              u0.z * pad(jb + 2, kBeta), u0.w * pad(jb + 3, kBeta),
-                              u1.x * pad(jb + 4, kBeta), u1.y * pad(jb + 5, kBeta),
-                              u1.z * pad(jb + 6, kBeta), u1.w * pad(jb + 7, kBeta)};
+          float x1[8], x2[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const float be = pad(jb + e, kBeta);
+            x1[e] = tv[e] * be;
+            x2[e] = tv[e] * (be * pad(jb + e, kSc));
+          }
           uint4 hi, lo;
-          split8(x, hi, lo);
-          const uint32_t o = tc::kmajor_offset(t, jb, 128);
-          *reinterpret_cast<uint4*>(sm + S::oTh + o) = hi;
-          *reinterpret_cast<uint4*>(sm + S::oTl + o) = lo;
+          const uint32_t o = tc::kmajor_offset(t, jb, NR);
+          split8(x1, hi, lo);
+          *reinterpret_cast<uint4*>(sm + S::oT1h + o) = hi;
+          *reinterpret_cast<uint4*>(sm + S::oT1l + o) = lo;
+          split8(x2, hi, lo);
+          *reinterpret_cast<uint4*>(sm + S::oT2h + o) = hi;
+          *reinterpret_cast<uint4*>(sm + S::oT2l + o) = lo;
         }
       }
-    } else {
-      // V (raw bf16) and K' = diag(e^G ik) K (split) as MN-major operands over the 128
-      // tokens, in the k tile's layout: 16-byte pieces of 8 channels of one token. A thread
-      // takes channel group cg of tokens 8i + (u & 7), i = 0..15: the 8 lanes sharing cg hold
-      // 8 consecutive tokens, so each 16-byte store hits its own bank group. All 16 V loads
-      // are issued before the first store
-      const int u = tid - 128;
+    } else if (tid < NR + 128) {
+      // V (raw bf16) as an MN-major operand over the 64 tokens, in the k tile's layout:
+      // 16-byte pieces of 8 channels of one token. A thread takes channel group cg of tokens
+      // 8i + (u & 7), i = 0..7: the 8 lanes sharing cg hold 8 consecutive tokens, so each
+      // 16-byte store hits its own bank group. All 8 loads are issued before the first store
+      const int u = tid - NR;
       const int cg = (u >> 3) & 15, tr = u & 7;
       const uint16_t* yv = y + 2 * a.Hk * kD + h * kD + 8 * cg;
-      uint4 vb[16];
+      uint4 vb[8];
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
+      for (int i = 0; i < 8; ++i) {
         const int tok = 8 * i + tr, ci = tok / C, tl = tok % C;
         vb[i] = tl < s_L[ci]
                     ? __ldg(reinterpret_cast<const uint4*>(yv + static_cast<int64_t>(s_t0[ci] + tl) * a.D))
                     : make_uint4(0u, 0u, 0u, 0u);
       }
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const int tok = 8 * i + tr;
-        const uint32_t o = tc::kmajor_offset(tok, 8 * cg, kD);
-        *reinterpret_cast<uint4*>(sm + S::oV + o) = vb[i];
-        const float sc = pad(tok, kSc);
-        float kx[8];
-        unpack8(*reinterpret_cast<const uint4*>(sm + S::oK + o), kx);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) kx[e] *= sc;
-        uint4 hi, lo;
-        split8(kx, hi, lo);
-        *reinterpret_cast<uint4*>(sm + S::oQ + o) = hi;  // sKh (aliases sQ)
-        *reinterpret_cast<uint4*>(sm + S::oKl + o) = lo;
+      for (int i = 0; i < 8; ++i)
+        *reinterpret_cast<uint4*>(sm + S::oV + tc::kmajor_offset(8 * i + tr, 8 * cg, kD)) = vb[i];
+    } else if (hr == 0) {
+      // the last two warps, idle during the solve: the q and k tiles of each chunk ->
+      // workspace (a chunk's rows are one contiguous slice of either smem tile)
+      const int u = tid - (NR + 128);
+      for (int ci = 0; ci < CPC; ++ci) {
+        const int c = c_first + ci;
+        if (c >= nchunks) break;
+        const size_t slice = static_cast<size_t>(C) * kD * 2;  // bytes of one chunk's tile
+        const uint4* srcq = reinterpret_cast<const uint4*>(sm + S::oQ + ci * slice);
+        const uint4* srck = reinterpret_cast<const uint4*>(sm + S::oK + ci * slice);
+        uint4* dq = reinterpret_cast<uint4*>(wb.Qt + (static_cast<size_t>(c) * a.Hk + kh) * wb.q_tile);
+        uint4* dk = reinterpret_cast<uint4*>(wb.Kt + (static_cast<size_t>(c) * a.Hk + kh) * wb.q_tile);
+        for (int i = u; i < static_cast<int>(slice / 16); i += kThreadsTc - NR - 128) {
+          dq[i] = srcq[i];
+          dk[i] = srck[i];
+        }
       }
     }
     bad = tc_sync(bad);
     if (bad) break;
 
     if (tid == 0) {
-      // U^T = V^T T'^T (cols 256..383: a dv row per lane, a token per column), A = V MN-major;
-      // W = T' K' (cols 384..511: a token per lane), B = K' MN-major
-      const uint32_t idu = tc::idesc_bf16_f32_amn(128, 128);
-      const uint32_t id = tc::idesc_bf16_f32_bmn(128, 128);
-      const uint32_t th = smem_addr(sm + S::oTh), tl = smem_addr(sm + S::oTl);
-      const uint32_t v = smem_addr(sm + S::oV);
-      const uint32_t kh_ = smem_addr(sm + S::oQ), kl = smem_addr(sm + S::oKl);
-      for (int ks = 0; ks < 8; ++ks)
-        tc::mma_bf16(tb + 256, tc::mnmajor_desc(v, 128, ks), tc::kmajor_desc(th, 128, ks), idu, ks > 0);
-      for (int ks = 0; ks < 8; ++ks)
-        tc::mma_bf16(tb + 256, tc::mnmajor_desc(v, 128, ks), tc::kmajor_desc(tl, 128, ks), idu, 1);
-      for (int ks = 0; ks < 8; ++ks)
-        tc::mma_bf16(tb + 384, tc::kmajor_desc(th, 128, ks), tc::mnmajor_desc(kh_, 128, ks), id, ks > 0);
-      for (int ks = 0; ks < 8; ++ks)
-        tc::mma_bf16(tb + 384, tc::kmajor_desc(th, 128, ks), tc::mnmajor_desc(kl, 128, ks), id, 1);
-      for (int ks = 0; ks < 8; ++ks)
-        tc::mma_bf16(tb + 384, tc::kmajor_desc(tl, 128, ks), tc::mnmajor_desc(kh_, 128, ks), id, 1);
+      // U^T = V^T T'^T (a dv row per lane, a token per column), A = V MN-major;
+      // W = T'' K (a token per lane), B = K MN-major
+      const uint32_t idu = tc::idesc_bf16_f32_amn(128, NR);
+      const uint32_t idw = tc::idesc_bf16_f32_bmn(128, kD);
+      const uint32_t t1h = smem_addr(sm + S::oT1h), t1l = smem_addr(sm + S::oT1l);
+      const uint32_t t2h = smem_addr(sm + S::oT2h), t2l = smem_addr(sm + S::oT2l);
+      const uint32_t v = smem_addr(sm + S::oV), k = smem_addr(sm + S::oK);
+      constexpr int KS = NR / 16;
+      for (int ks = 0; ks < KS; ++ks)
+        tc::mma_bf16(tb + kColU, tc::mnmajor_desc(v, kD, ks), tc::kmajor_desc(t1h, NR, ks), idu, ks > 0);
+      for (int ks = 0; ks < KS; ++ks)
+        tc::mma_bf16(tb + kColU, tc::mnmajor_desc(v, kD, ks), tc::kmajor_desc(t1l, NR, ks), idu, 1);
+      for (int ks = 0; ks < KS; ++ks)
+        tc::mma_bf16(tb + kColW, tc::kmajor_desc(t2h, NR, ks), tc::mnmajor_desc(k, kD, ks), idw, ks > 0);
+      for (int ks = 0; ks < KS; ++ks)
+        tc::mma_bf16(tb + kColW, tc::kmajor_desc(t2l, NR, ks), tc::mnmajor_desc(k, kD, ks), idw, 1);
       tc::mma_commit(bar);
     }
     if (!mbar_wait_bounded(bar, phase)) bad = true;
@@ -565,35 +599,42 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     phase ^= 1;
     tc::fence_after_sync();
     if (!bad) {
-      // U^T -> workspace (fp32 [128 x C] tile image per chunk, 16-byte pieces of a dv row);
-      // W -> hi / lo tiles [C x 128]. Every lane executes the (warp-collective) loads; only
-      // existing chunks store. Lane = dv row r of U^T and token row t of W alike
+      // U^T -> workspace (fp32 [128 x C] tile image per chunk, 16-byte pieces of a dv row):
+      // every warp, lane = dv row r, 32 token columns per warp
       const int r = 32 * (warp & 3) + lane, half = warp >> 2;
-      const int t = r;
-      const int ci = t / C, tl = t % C;
-      const int c = c_first + ci;
-      const bool store = c < nchunks;
       {
+        float uv[32];
+        tmem_load<16>(tc::taddr(tb, 32 * (warp & 3), kColU + half * 32),
+                      *reinterpret_cast<float(*)[16]>(uv));
+        tmem_load<16>(tc::taddr(tb, 32 * (warp & 3), kColU + half * 32 + 16),
+                      *reinterpret_cast<float(*)[16]>(uv + 16));
+        tc::tmem_wait_ld();
+#pragma unroll
+        for (int g = 0; g < 32; g += 8) {  // 8 tokens of one chunk: two 16-byte image pieces
+          const int T = half * 32 + g, cu = c_first + T / C, tu = T % C;
+          if (cu < nchunks) {
+            unsigned char* ub = reinterpret_cast<unsigned char*>(
+                wb.Ut + (static_cast<size_t>(cu) * a.Hv + h) * (kD * C));
+            *reinterpret_cast<float4*>(ub + u_image_offset(r, tu, C)) =
+                make_float4(uv[g], uv[g + 1], uv[g + 2], uv[g + 3]);
+            *reinterpret_cast<float4*>(ub + u_image_offset(r, tu + 4, C)) =
+                make_float4(uv[g + 4], uv[g + 5], uv[g + 6], uv[g + 7]);
+          }
+        }
+      }
+      // W -> hi / lo tiles [C x 128]: warps whose lanes hold token rows 0..63, lane = token
+      // row t, 64 columns per warp. Every lane of such a warp executes the (warp-collective)
+      // loads; only existing chunks store
+      if ((warp & 3) < 2) {
+        const int t = r, ci = t / C, tl = t % C, c = c_first + ci;
+        const bool store = c < nchunks;
         unsigned char* wt = wb.Wt + (static_cast<size_t>(store ? c : 0) * a.Hv + h) * 2 * wb.w_tile;
 #pragma unroll 1
         for (int b0 = 0; b0 < 64; b0 += 16) {
           const int col = half * 64 + b0;
-          float uv[16], wv[16];
-          tmem_load<16>(tc::taddr(tb, 32 * (warp & 3), 256 + col), uv);  // U^T[r][col ..]
-          tmem_load<16>(tc::taddr(tb, 32 * (warp & 3), 384 + col), wv);  // W[t][col ..]
+          float wv[16];
+          tmem_load<16>(tc::taddr(tb, 32 * (warp & 3), kColW + col), wv);  // W[t][col ..]
           tc::tmem_wait_ld();
-#pragma unroll
-          for (int g = 0; g < 16; g += 8) {  // 8 tokens of one chunk: two 16-byte image pieces
-            const int T = col + g, cu = c_first + T / C, tu = T % C;
-            if (cu < nchunks) {
-              unsigned char* ub = reinterpret_cast<unsigned char*>(
-                  wb.Ut + (static_cast<size_t>(cu) * a.Hv + h) * (kD * C));
-              *reinterpret_cast<float4*>(ub + u_image_offset(r, tu, C)) =
-                  make_float4(uv[g], uv[g + 1], uv[g + 2], uv[g + 3]);
-              *reinterpret_cast<float4*>(ub + u_image_offset(r, tu + 4, C)) =
-                  make_float4(uv[g + 4], uv[g + 5], uv[g + 6], uv[g + 7]);
-            }
-          }
           if (!store) continue;
 #pragma unroll
           for (int e8 = 0; e8 < 16; e8 += 8) {
@@ -613,7 +654,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   }
   if (bad && tid == 0 && a.err) atomicOr(a.err, GDN_DEVERR_TIMEOUT);
   tc_sync(false);
-  if (warp == 0) tc::tmem_dealloc(tb, kTmemCols);
+  if (warp == 0) tc::tmem_dealloc(tb, kIntraTmemCols);
 }
 
 // ============================================================== pass kernel
@@ -1056,9 +1097,13 @@ cudaError_t launch_tc_c(const LayerArgs& a, const PrefillExtra& p, const TcLayou
   wb.p_tile = L.p_tile;
   cudaError_t e;
   if (L.max_chunks > 0) {
-    constexpr int CPC = 128 / C;
+    constexpr int CPC = IntraSmem<C>::CPC;
     auto k1 = intra_tc_kernel<C>;
     e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, IntraSmem<C>::kBytes);
+    if (e != cudaSuccess) return e;
+    // the whole carveout as shared memory, so that two CTAs fit on an SM
+    e = cudaFuncSetAttribute(k1, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
     k1<<<dim3((L.max_chunks + CPC - 1) / CPC, a.Hk), kThreadsTc, IntraSmem<C>::kBytes, s>>>(
         a, p, y, meta, chunk_off, chunk_seq, wb);

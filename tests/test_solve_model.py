@@ -1,15 +1,18 @@
-"""A CPU model of the intra kernel's triangular solve (csrc/gdn_prefill_tc.cu): the same
-per-thread index arithmetic over the fp32 A / T rows of stride C + 4 (four padding floats per
-row), every shared-memory access checked for bounds, 16-byte alignment of the vector accesses
+"""A CPU model of the intra kernel's triangular solve (csrc/gdn_prefill_tc.cu; a CTA holds 64
+token rows, 64 / C chunks, solved by 64 threads): the same per-thread index arithmetic over the
+fp32 A / T rows of stride C + 4 (four padding floats per row), every shared-memory access checked for bounds, 16-byte alignment of the vector accesses
 and reads of initialised data only, with the kernel's barriers at the same points. The result
 T must equal (I + A)^-1 per chunk. The model is host logic only; the GPU parity tests check the
 kernel itself against the oracle."""
 import numpy as np
 import pytest
 
+NROW = 64        # token rows per intra CTA
+NSOLVE = 64      # solver threads (warps 0-1)
+
+
 def run_model(C, seed=0):
     SA = C + 4
-    NROW = 128
     sA = np.full(NROW * SA, np.nan, dtype=np.float64)   # NaN = never written
     def rd(i):
         assert 0 <= i < NROW * SA, ("read oob", i); v = sA[i]; assert not np.isnan(v), ("read unwritten", i); return v
@@ -18,7 +21,7 @@ def run_model(C, seed=0):
     def rd4(i):
         assert i % 4 == 0, ("float4 misaligned", i); return [rd(i + k) for k in range(4)]
     rng = np.random.default_rng(seed)
-    CPC = 128 // C
+    CPC = NROW // C
     A = np.zeros((CPC, C, C))
     for ci in range(CPC):
         M = rng.standard_normal((C, C)) * 0.3
@@ -37,7 +40,7 @@ def run_model(C, seed=0):
     # step 1: diagonal blocks of B1 rows, thread = (block, column c)
     B1 = min(C, 32)
     X1 = {}
-    for tid in range(128):
+    for tid in range(NSOLVE):
         row0 = (tid // B1) * B1; c = tid % B1; o = row0 % C
         base = row0 * SA + o
         x = [0.0] * B1
@@ -55,12 +58,12 @@ def run_model(C, seed=0):
         for r in range(B1):
             wr(base + r * SA + c, x[r])
     if C == 64:
-        # step 2a: X = A21 T11, 64 threads per chunk, 4x4 outputs per thread
+        # step 2a: X = A21 T11, 64 threads, 4x4 outputs per thread
         res = {}
-        for tid in range(128):
-            ci = tid >> 6; k = tid & 63
+        for tid in range(NSOLVE):
+            k = tid
             r0 = 4 * (k >> 3); c0 = 4 * (k & 7)
-            cb = ci * C * SA
+            cb = 0
             acc = np.zeros((4, 4))
             for l in range(0, 32, 4):
                 a = [rd4(cb + (32 + r0 + i) * SA + l) for i in range(4)]
@@ -76,10 +79,10 @@ def run_model(C, seed=0):
                     wr(cb + (32 + r0 + i) * SA + c0 + jj, acc[i][jj])
         # step 2b: T21 = -(T22 X), l < r0 + 4 (T22 rows r0..r0+3 are zero beyond)
         res = {}
-        for tid in range(128):
-            ci = tid >> 6; k = tid & 63
+        for tid in range(NSOLVE):
+            k = tid
             r0 = 4 * (k >> 3); c0 = 4 * (k & 7)
-            cb = ci * C * SA
+            cb = 0
             acc = np.zeros((4, 4))
             for l in range(0, r0 + 4, 4):
                 a = [rd4(cb + (32 + r0 + i) * SA + 32 + l) for i in range(4)]
