@@ -25,7 +25,8 @@ GDN_NOALLOC_SCRATCH_BYTES = 64 << 20
 GDN_BF16, GDN_F32 = 0, 1
 GDN_CONV_DIM_FIRST, GDN_CONV_TAP_FIRST = 0, 1
 GDN_GATE_FUSED, GDN_GATE_DIRECT = 0, 1
-GDN_DEVERR_SLOT_RANGE, GDN_DEVERR_SEQLENS = 1, 2
+GDN_DEVERR_SLOT_RANGE, GDN_DEVERR_SEQLENS, GDN_DEVERR_TIMEOUT = 1, 2, 4
+GDN_TEST_FAULT_NONE, GDN_TEST_FAULT_DECODE_CONSUMER, GDN_TEST_FAULT_PREFILL_PASS = 0, 1, 2
 GDN_ACT_SILU, GDN_ACT_SIGMOID = 0, 1
 
 
@@ -133,6 +134,8 @@ def lib():
         L.gdn_validate_slots.argtypes = [P, I32, I32]
         L.gdn_status_string.restype = ctypes.c_char_p
         L.gdn_status_string.argtypes = [I32]
+        L.gdn_testing_set_fault.restype = I32
+        L.gdn_testing_set_fault.argtypes = [I32]
         _lib = L
     return _lib
 
@@ -310,6 +313,11 @@ class DecodeGraph:
             self.close()
         except Exception:
             pass
+
+
+def gdn_testing_set_fault(mode: int) -> None:
+    """Test hook (include/gdn_testing.h): make one bounded wait of the kernels run out."""
+    _check(lib().gdn_testing_set_fault(int(mode)))
 
 
 def gdn_validate_slots(host_slot, num_slots) -> int:

@@ -5,6 +5,7 @@
 #include <vector>
 
 #include "gdn_internal.h"
+#include "gdn_testing.h"
 
 namespace {
 
@@ -257,6 +258,17 @@ int32_t gdn_validate_slots(const int32_t* host_slot, int32_t n, int32_t num_slot
   for (size_t i = 1; i < active.size(); ++i)
     if (active[i] == active[i - 1]) return 2;
   return 0;
+}
+
+gdn_status gdn_testing_set_fault(int32_t mode) {
+  if (mode != GDN_TEST_FAULT_NONE && mode != GDN_TEST_FAULT_DECODE_CONSUMER &&
+      mode != GDN_TEST_FAULT_PREFILL_PASS)
+    return GDN_ERR_INVALID_ARG;
+  const int d = mode == GDN_TEST_FAULT_DECODE_CONSUMER ? 1 : 0;
+  const int p = mode == GDN_TEST_FAULT_PREFILL_PASS ? 2 : 0;
+  if (gdn::set_decode_test_fault(d) != cudaSuccess) return GDN_ERR_CUDA;
+  if (gdn::set_prefill_test_fault(p) != cudaSuccess) return GDN_ERR_CUDA;
+  return GDN_OK;
 }
 
 const char* gdn_status_string(gdn_status status) {

@@ -49,6 +49,12 @@ namespace gdn {
 namespace {
 
 constexpr int kConsumerWarps = 8;
+
+// Test hook (gdn_testing_set_fault, mode 1): the first consumer warp of CTA 0 waits, with a
+// 10 ms bound, on a barrier nothing arrives on, and leaves as a consumer whose wait ran out
+// does, so that the kernel's bounded waits and error reporting run on the GPU. 0 in use.
+__device__ int g_test_fault = 0;
+constexpr uint64_t kTestWaitNs = 10000000ull;
 constexpr int kRingBytes = 192 * 1024;
 
 template <int N> struct VecF;
@@ -246,7 +252,7 @@ struct DecodeCfg {
   // (gated calls), then the mbarriers
   static constexpr int kOBufOffset = kRingBytes + kSetupBufs * kSetupStride * 4;
   static constexpr int kBarOffset = kOBufOffset + 2 * kUnitRows * 4;
-  static constexpr int kNumBars = 2 * kNumStages + 2 * kSetupBufs + 4;
+  static constexpr int kNumBars = 2 * kNumStages + 2 * kSetupBufs + 5;  // + the test hook's
   static constexpr int kSmemBytes = kBarOffset + kNumBars * 8;
   static_assert(kSmemBytes <= 227 * 1024, "decode shared memory exceeds the per-CTA limit");
 };
@@ -394,6 +400,7 @@ __global__ void __launch_bounds__(DecodeCfg<DK, R, kBf16State>::kThreads, 1)
   const uint32_t sfull0 = smem_addr(bars + 2 * NS), sempty0 = smem_addr(bars + 2 * NS + NB);
   const uint32_t ofull0 = smem_addr(bars + 2 * NS + 2 * NB);
   const uint32_t oempty0 = smem_addr(bars + 2 * NS + 2 * NB + 2);
+  const uint32_t dead = smem_addr(bars + 2 * NS + 2 * NB + 4);  // never arrived on
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (tid == 0) {
@@ -409,6 +416,7 @@ __global__ void __launch_bounds__(DecodeCfg<DK, R, kBf16State>::kThreads, 1)
       mbar_init(ofull0 + 8 * i, kConsumerWarps);
       mbar_init(oempty0 + 8 * i, 1);
     }
+    mbar_init(dead, 1);
     fence_mbar_init();
   }
   __syncthreads();
@@ -666,6 +674,11 @@ __global__ void __launch_bounds__(DecodeCfg<DK, R, kBf16State>::kThreads, 1)
 
   // -------------------------------------------------------------- consumers
   const int cw = warp - 1 - SW;
+  if (g_test_fault == 1 && blockIdx.x == 0 && cw == 0 &&
+      !__all_sync(0xffffffffu, mbar_wait_bounded(dead, 0, kTestWaitNs))) {
+    if (lane == 0 && a.err) atomicOr(a.err, GDN_DEVERR_TIMEOUT);
+    return;
+  }
   constexpr int RPW = Cfg::kRowsPerWarp;
   uint32_t g = 0, n = 0;
   UnitSlots slots;
@@ -976,6 +989,10 @@ int sm_count() {
     count[dev] = c;
   }
   return count[dev];
+}
+
+cudaError_t set_decode_test_fault(int mode) {
+  return cudaMemcpyToSymbol(g_test_fault, &mode, sizeof(int));
 }
 
 cudaError_t launch_decode(const LayerArgs& a, int B, cudaStream_t s) {

@@ -110,6 +110,11 @@ cudaError_t launch_prefill_prep(const LayerArgs& a, const PrefillExtra& p, int32
 size_t prefill_tc_workspace_bytes(int total_tokens, int num_seqs, int Hk, int Hv, int chunk);
 cudaError_t launch_prefill_tc(const LayerArgs& a, const PrefillExtra& p, cudaStream_t s);
 
+// test hooks (gdn_testing_set_fault): the device flag of the decode and of the tensor-core
+// prefill translation units
+cudaError_t set_decode_test_fault(int mode);
+cudaError_t set_prefill_test_fault(int mode);
+
 // prefill helpers implemented in gdn_conv.cu: the conv output y of every token of an active
 // sequence (over the chunk table of launch_prefill_prep), then each active sequence's final
 // conv window

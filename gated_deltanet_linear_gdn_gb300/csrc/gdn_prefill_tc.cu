@@ -53,6 +53,13 @@ constexpr int kThreadsTc = 256;  // 8 warps: warp w reads tensor-memory lanes 32
 constexpr int kPassThreads = kThreadsTc + 64;
 constexpr int kSyncThreads = kThreadsTc + 32;
 constexpr uint32_t kTmemCols = 512;
+
+// Test hook (gdn_testing_set_fault, mode 2): compute warp 0 of the state pass's first CTA
+// waits, with a 10 ms bound, on a barrier nothing arrives on in place of its first group-2
+// wait, and reports it as a wait that ran out, so the pass's failure path runs on the GPU:
+// the other warps leave the chunk loop while the next chunk's tiles may still be in flight.
+__device__ int g_test_fault = 0;
+constexpr uint64_t kTestWaitNs = 10000000ull;
 constexpr int kVecFloats = 256;  // per (chunk, head): f[C], dd[C], g_last
 
 struct TcLayout {
@@ -684,7 +691,7 @@ __global__ void __launch_bounds__(kPassThreads, 1)
   using S = PassSmem<C>;
   extern __shared__ __align__(1024) unsigned char sm[];
   __shared__ uint32_t s_tmem;
-  __shared__ __align__(8) uint64_t s_bar[6];  // fullA, fullB, mma1, mma2, fullU, oDone
+  __shared__ __align__(8) uint64_t s_bar[7];  // fullA, fullB, mma1, mma2, fullU, oDone, dead
 
   // CTAs in launch order take the sequences longest first, all value heads of one together
   const int i = seq_order[blockIdx.x / a.Hv], h = blockIdx.x % a.Hv;
@@ -714,6 +721,8 @@ __global__ void __launch_bounds__(kPassThreads, 1)
   // copy warp's own arrival for a phase comes only after it has seen the one before, so
   // no warp's arrivals can run into the next phase
   const uint32_t oDone = smem_addr(&s_bar[5]);
+  const uint32_t dead = smem_addr(&s_bar[6]);  // never arrived on (test hook)
+  const int test_fault = g_test_fault;
   const size_t wtile = wb.w_tile, ptile = wb.p_tile;
 
   // W hi/lo, q tile, vec of chunk c0 + it on one fullA phase (group 1's operands, and vec)
@@ -748,6 +757,7 @@ __global__ void __launch_bounds__(kPassThreads, 1)
   if (warp == 0) tc::tmem_alloc(&s_tmem, kTmemCols);
   if (copy_warp && lane == 0) {
     for (int k = 0; k < 5; ++k) mbar_init(smem_addr(&s_bar[k]), 1);
+    mbar_init(dead, 1);
     mbar_init(oDone, kThreadsTc / 32 + 1);
     fence_mbar_init();
     if (nch > 0) { issue_A(0); issue_B(0); issue_U(0); }
@@ -848,11 +858,11 @@ __global__ void __launch_bounds__(kPassThreads, 1)
     // output (vec[it & 1]). Each barrier of a chunk is armed only after this warp has seen
     // the phase it waits on for the chunk before, so no parity wait can alias a later phase
     bool ok = !bad;
-    if (lane == 0 && ok && nch > 0) {
+    if (lane == 0 && nch > 0) {
       int nA = 1, nBU = 1;  // phases issued (chunk 0's at set-up)
       if (nch > 1) prefetch_chunk(1);
       mbar_arrive(oDone);  // this warp's share of phase 0
-      if (nch > 1) {
+      if (ok && nch > 1) {
         if (mbar_wait_bounded(mma1, 0)) {
           tc::fence_after_sync();
           issue_A(1);
@@ -878,14 +888,14 @@ __global__ void __launch_bounds__(kPassThreads, 1)
           nA = it + 3;
         }
       }
-      if (!ok) {
-        if (a.err) atomicOr(a.err, GDN_DEVERR_TIMEOUT);
-        // copies may still be in flight: wait (bounded) for the last issued phase of each
-        // barrier -- one already completed (and consumed) returns at once
-        mbar_wait_bounded(fullA, (nA - 1) & 1);
-        mbar_wait_bounded(fullB, (nBU - 1) & 1);
-        mbar_wait_bounded(fullU, (nBU - 1) & 1);
-      }
+      if (!ok && a.err) atomicOr(a.err, GDN_DEVERR_TIMEOUT);
+      // copies may still be in flight -- after this warp's own failure, and after another
+      // warp's, which leaves the chunk loop without waiting for the tiles already issued for
+      // the next chunk: wait (bounded) for the last issued phase of each barrier before the
+      // CTA may exit; one already completed (and consumed) returns at once
+      mbar_wait_bounded(fullA, (nA - 1) & 1);
+      mbar_wait_bounded(fullB, (nBU - 1) & 1);
+      mbar_wait_bounded(fullU, (nBU - 1) & 1);
     }
   }
 
@@ -967,7 +977,9 @@ __global__ void __launch_bounds__(kPassThreads, 1)
         }
       }
     } else {  // compute warps
-      if (!mbar_wait_bounded(mma2, par)) mine = true;
+      const bool test_fail = test_fault == 2 && blockIdx.x == 0 && warp == 0 && it == 0;
+      if (test_fail ? !mbar_wait_bounded(dead, 0, kTestWaitNs) : !mbar_wait_bounded(mma2, par))
+        mine = true;
       mine = __any_sync(0xffffffffu, mine);  // warp-uniform before the aligned loads
       tc::fence_after_sync();
       if (!mine) {
@@ -1120,6 +1132,10 @@ cudaError_t launch_tc_c(const LayerArgs& a, const PrefillExtra& p, const TcLayou
 }
 
 }  // namespace
+
+cudaError_t set_prefill_test_fault(int mode) {
+  return cudaMemcpyToSymbol(g_test_fault, &mode, sizeof(int));
+}
 
 size_t prefill_tc_workspace_bytes(int total_tokens, int num_seqs, int Hk, int Hv, int chunk) {
   return tc_layout(total_tokens, num_seqs, Hk, Hv, chunk, 2 * Hk * kD + Hv * kD).total;

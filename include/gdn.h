@@ -120,8 +120,11 @@ typedef struct {
  * bits in it, with atomicOr, and never clear one). */
 #define GDN_DEVERR_SLOT_RANGE 1 /* an active slot >= num_slots */
 #define GDN_DEVERR_SEQLENS 2    /* cu_seqlens not non-decreasing or not ending at total_tokens */
-#define GDN_DEVERR_TIMEOUT 4    /* a bounded wait for an asynchronous copy gave up (the
-                                   affected rows are left unprocessed) */
+#define GDN_DEVERR_TIMEOUT 4    /* a bounded wait (about a second) for an asynchronous copy or
+                                   a tensor-core group gave up: the call's outputs and the
+                                   states of its active slots are not to be trusted; slots the
+                                   call does not address are untouched, and the context stays
+                                   usable (include/gdn_testing.h makes one wait run out) */
 
 /*
  * gdn_conv_update -- one decode step of the causal depthwise conv1d ([P1]

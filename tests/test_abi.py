@@ -1,4 +1,5 @@
-"""The C-ABI library loads and exports every symbol include/gdn.h declares, and its
+"""The C-ABI library loads and exports every symbol include/gdn.h and include/gdn_testing.h
+declare, and its
 host-side logic (argument checks, workspace sizing, slot validation, status strings)
 behaves as documented. No call here reaches a kernel launch: every argument error
 returns before any CUDA call, so these run without a GPU."""
@@ -21,8 +22,8 @@ def L():
     return gdn.lib()
 
 
-def declared_functions():
-    src = open(os.path.join(ROOT, "include", "gdn.h")).read()
+def declared_functions(header="gdn.h"):
+    src = open(os.path.join(ROOT, "include", header)).read()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
     return sorted(set(re.findall(r"\b(gdn_[a-z_0-9]+)\s*\(", src)))
 
@@ -34,6 +35,15 @@ def test_exports_every_declared_symbol(L):
             "gdn_status_string"} <= set(names)
     for n in names:
         assert hasattr(L, n), n
+    testing = declared_functions("gdn_testing.h")
+    assert testing == ["gdn_testing_set_fault"]
+    assert hasattr(L, testing[0])
+
+
+def test_testing_fault_rejects_unknown_modes(L):
+    """An unknown mode is refused before any CUDA call (so this runs without a GPU)."""
+    assert L.gdn_testing_set_fault(3) == gdn.GDN_ERR_INVALID_ARG
+    assert L.gdn_testing_set_fault(-1) == gdn.GDN_ERR_INVALID_ARG
 
 
 def test_status_strings(L):
