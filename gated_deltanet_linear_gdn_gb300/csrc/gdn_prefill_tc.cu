@@ -112,11 +112,11 @@ __device__ __forceinline__ uint32_t out_tile_offset(int t, int col) {
   return static_cast<uint32_t>(t * 256 + (((col >> 3) ^ (t & 7)) << 4) + (col & 7) * 2);
 }
 
-// Byte offset of U^T(r, t) (state row r, token t of the chunk) in a U tile. The tile is
-// the byte image of the pass kernel's two bf16 [128 x C] D' operand tiles (hi, then lo):
-// tokens t..t+3 of an 8-token group sit where the hi tile holds (r, group), t+4..t+7
-// where the lo tile does. A bulk copy drops U onto those tiles, and the thread that owns
-// row r and the group reads its 32 bytes before writing its D' operands over them.
+// Byte offset of U^T(r, t) (state row r, token t of the chunk) in a U tile: the byte
+// image of two bf16 [128 x C] K-major tiles, tokens t..t+3 of an 8-token group where the
+// first tile holds (r, group), t+4..t+7 where the second does. The pass kernel's thread that
+// owns row r reads a group as two 16-byte pieces, eight rows of a warp per 128 bytes, so
+// its reads are free of bank conflicts.
 __host__ __device__ __forceinline__ uint32_t u_image_offset(int r, int t, int C) {
   return static_cast<uint32_t>(((t >> 2) & 1) * (128 * C * 2)) + tc::kmajor_offset(r, t & ~7, C) +
          static_cast<uint32_t>((t & 3) * 4);
@@ -667,16 +667,14 @@ __global__ void __launch_bounds__(kThreadsTc, 2)
 // ============================================================== pass kernel
 template <int C>
 struct PassSmem {
-  static constexpr int kS = 128 * 128 * 2;      // S hi / lo  [128 x 128] bf16
-  static constexpr int kD_ = 128 * C * 2;       // D^T tiles  [128 x C]   bf16
+  static constexpr int kUh = 128 * C * 2;       // one half of the U^T image (u_image_offset)
   static constexpr int kW = C * 128 * 2;        // W, Q tiles [C x 128]   bf16
   static constexpr int kP = C * C * 2;          // P tiles    [C x C]     bf16
-  static constexpr int oSh = 0, oSl = kS;
-  static constexpr int oDh = 2 * kS, oDl = oDh + kD_, oEh = oDl + kD_, oEl = oEh + kD_;
+  static constexpr int oU = 0;                  // U^T image, fp32 [128 x C]: 2 kUh bytes
   // the q tile follows the W hi tile: together they are one [2C x 128] MMA operand
-  static constexpr int oWh = oEl + kD_, oQ = oWh + kW, oWl = oQ + kW;
+  static constexpr int oWh = oU + 2 * kUh, oQ = oWh + kW, oWl = oQ + kW;
   static constexpr int oPh = oWl + kW, oPl = oPh + kP, oKtile = oPl + kP;  // k tile [C x 128]
-  static constexpr int oVec = oKtile + kD_;     // two vec buffers of kVecFloats
+  static constexpr int oVec = oKtile + kW;      // two vec buffers of kVecFloats
   static constexpr int oO = oVec + 2 * kVecFloats * 4;  // bf16 output tile [C x 128], swizzled
   static constexpr int kBytes = oO + C * 128 * 2;
   // the kernel's static variables (tensor-memory base, mbarriers) are padded to 1 KB ahead of
@@ -691,7 +689,8 @@ __global__ void __launch_bounds__(kPassThreads, 1)
   using S = PassSmem<C>;
   extern __shared__ __align__(1024) unsigned char sm[];
   __shared__ uint32_t s_tmem;
-  __shared__ __align__(8) uint64_t s_bar[7];  // fullA, fullB, mma1, mma2, fullU, oDone, dead
+  // fullA, fullB, mma1, mma2, fullU, oDone, dead, upd
+  __shared__ __align__(8) uint64_t s_bar[8];
 
   // CTAs in launch order take the sequences longest first, all value heads of one together
   const int i = seq_order[blockIdx.x / a.Hv], h = blockIdx.x % a.Hv;
@@ -714,6 +713,13 @@ __global__ void __launch_bounds__(kPassThreads, 1)
   const bool compute = warp < kThreadsTc / 32;
   const int q = warp & 3, half = warp >> 2;  // compute warps
   const int r = 32 * q + lane;  // state row (dv index) = tensor-memory lane
+  // Tensor-memory columns. X0 = [0, 128) and X1 = [256, 384) alternate by chunk parity p:
+  // chunk it's raw D^T (then its O2^T) at [X_p, X_p + C) and O1^T at [X_p + C, X_p + 2C), its
+  // state update at [X_(1-p), X_(1-p) + 128) -- free by then, the chunk before's output has
+  // been read. The A operands of the MMAs (bf16 pairs of K per column): the state's hi / lo
+  // parts at [kColS, kColS + 64) / [kColS + 64, kColS + 128), D^T hi / lo and D'^T hi / lo at
+  // kColDE + {0, C / 2, C, 3C / 2}, C / 2 columns each.
+  constexpr int kColS = 128, kColDE = 384;
   const uint32_t fullA = smem_addr(&s_bar[0]), fullB = smem_addr(&s_bar[1]);
   const uint32_t mma1 = smem_addr(&s_bar[2]), mma2 = smem_addr(&s_bar[3]);
   const uint32_t fullU = smem_addr(&s_bar[4]);
@@ -722,6 +728,10 @@ __global__ void __launch_bounds__(kPassThreads, 1)
   // no warp's arrivals can run into the next phase
   const uint32_t oDone = smem_addr(&s_bar[5]);
   const uint32_t dead = smem_addr(&s_bar[6]);  // never arrived on (test hook)
+  // group 2 is committed in two parts: upd once the state update D'^T K is done (all the
+  // state chain waits for), mma2 once O2^T = D^T P^T is done too (the output, and the reuse of
+  // the P, k and U buffers, wait for that)
+  const uint32_t upd = smem_addr(&s_bar[7]);
   const int test_fault = g_test_fault;
   const size_t wtile = wb.w_tile, ptile = wb.p_tile;
 
@@ -748,21 +758,22 @@ __global__ void __launch_bounds__(kPassThreads, 1)
     bulk_g2s(smem_addr(sm + S::oPl), pp + ptile, static_cast<uint32_t>(ptile), fullB);
     bulk_g2s(smem_addr(sm + S::oKtile), kt, static_cast<uint32_t>(wb.q_tile), fullB);
   };
-  auto issue_U = [&](int it) {  // U^T of chunk c0 + it onto the D' tiles (free once group 2 is done)
+  auto issue_U = [&](int it) {  // U^T of chunk c0 + it (its buffer is free once group 2 is done)
     const float* ut = wb.Ut + (static_cast<size_t>(c0 + it) * a.Hv + h) * (kD * C);
     mbar_arrive_expect_tx(fullU, static_cast<uint32_t>(kD * C * 4));
-    bulk_g2s(smem_addr(sm + S::oEh), ut, static_cast<uint32_t>(kD * C * 4), fullU);
+    bulk_g2s(smem_addr(sm + S::oU), ut, static_cast<uint32_t>(kD * C * 4), fullU);
   };
 
   if (warp == 0) tc::tmem_alloc(&s_tmem, kTmemCols);
   if (copy_warp && lane == 0) {
     for (int k = 0; k < 5; ++k) mbar_init(smem_addr(&s_bar[k]), 1);
     mbar_init(dead, 1);
+    mbar_init(upd, 1);
     mbar_init(oDone, kThreadsTc / 32 + 1);
     fence_mbar_init();
     if (nch > 0) { issue_A(0); issue_B(0); issue_U(0); }
   }
-  // state (half a row per compute thread) -> registers and the split operand tiles
+  // state (half a row per compute thread) -> registers; its split parts -> tensor memory below
   const int64_t soff = (static_cast<int64_t>(slot) * a.Hv + h) * (kD * kD) + r * kD + half * 64;
   float* Sg = a.ssm + soff;                                          // fp32 state
   uint16_t* Sb = reinterpret_cast<uint16_t*>(a.ssm) + soff;          // bf16 state
@@ -784,7 +795,11 @@ __global__ void __launch_bounds__(kPassThreads, 1)
       }
     }
   }
-  auto store_S_tiles = [&]() {
+  tc_sync(false);  // the tensor-memory allocation is visible
+  const uint32_t tb = s_tmem;
+  // the state's bf16 hi / lo parts, the A operand of group 1, in tensor memory: this thread's
+  // half row r, 32 columns of k pairs each
+  auto store_S_tmem = [&]() {
 #pragma unroll
     for (int e8 = 0; e8 < 64; e8 += 8) {
       float x[8];
@@ -792,29 +807,20 @@ __global__ void __launch_bounds__(kPassThreads, 1)
       for (int e = 0; e < 8; ++e) x[e] = Sr[e8 + e];
       uint4 hi, lo;
       split8(x, hi, lo);
-      const uint32_t o = tc::kmajor_offset(r, half * 64 + e8, 128);
-      *reinterpret_cast<uint4*>(sm + S::oSh + o) = hi;
-      *reinterpret_cast<uint4*>(sm + S::oSl + o) = lo;
+      const int col = half * 32 + e8 / 2;
+      tc::tmem_st4(tc::taddr(tb, 32 * q, kColS + col), hi);
+      tc::tmem_st4(tc::taddr(tb, 32 * q, kColS + 64 + col), lo);
     }
+    tc::tmem_wait_st();
   };
-  if (compute) store_S_tiles();
+  if (compute) store_S_tmem();
   bool bad = tc_sync(false);
   bool mine = false;  // this thread's wait failure, reported at the next CTA barrier
-  const uint32_t tb = s_tmem;
-  // tensor-memory columns: D^T raw and O1^T at [base, base + C) and [base + C, base + 2C),
-  // base = 0 for even chunks and 384 for odd ones (chunk it's O1 is read while group 1 of
-  // chunk it + 1 runs); O2^T [128, 128 + C); state update [256, 384)
   constexpr int NH = C / 2;
   constexpr int KS = C / 16;
   // operand descriptors are fixed per CTA; a K step adds 256 bytes (16 units) to the start
-  const uint64_t dSh = tc::kmajor_desc(smem_addr(sm + S::oSh), 128, 0);
-  const uint64_t dSl = tc::kmajor_desc(smem_addr(sm + S::oSl), 128, 0);
   const uint64_t dWh = tc::kmajor_desc(smem_addr(sm + S::oWh), 128, 0);
   const uint64_t dWl = tc::kmajor_desc(smem_addr(sm + S::oWl), 128, 0);
-  const uint64_t dDh = tc::kmajor_desc(smem_addr(sm + S::oDh), C, 0);
-  const uint64_t dDl = tc::kmajor_desc(smem_addr(sm + S::oDl), C, 0);
-  const uint64_t dEh = tc::kmajor_desc(smem_addr(sm + S::oEh), C, 0);
-  const uint64_t dEl = tc::kmajor_desc(smem_addr(sm + S::oEl), C, 0);
   const uint64_t dPh = tc::kmajor_desc(smem_addr(sm + S::oPh), C, 0);
   const uint64_t dPl = tc::kmajor_desc(smem_addr(sm + S::oPl), C, 0);
   const uint64_t dKtile = tc::mnmajor_desc(smem_addr(sm + S::oKtile), 128, 0);  // k tile, MN-major
@@ -825,13 +831,14 @@ __global__ void __launch_bounds__(kPassThreads, 1)
   // the D^T columns and S Q^T (= O1^T, both S parts) into the next C; S_hi W_lo^T completes D
   auto issue_mma1 = [&](int it) -> bool {
     if (!mbar_wait_bounded(fullA, it & 1)) return false;
-    const uint32_t t1 = tb + ((it & 1) ? 384 : 0);
+    const uint32_t t1 = tb + ((it & 1) ? 256 : 0);
+    const uint32_t aSh = tb + kColS, aSl = tb + kColS + 64;  // a K step: 8 columns
 #pragma unroll
-    for (int ks = 0; ks < 8; ++ks) tc::mma_bf16(t1, dSh + 16 * ks, dWh + 16 * ks, id2C, ks > 0);
+    for (int ks = 0; ks < 8; ++ks) tc::mma_bf16_ts(t1, aSh + 8 * ks, dWh + 16 * ks, id2C, ks > 0);
 #pragma unroll
-    for (int ks = 0; ks < 8; ++ks) tc::mma_bf16(t1, dSl + 16 * ks, dWh + 16 * ks, id2C, 1);
+    for (int ks = 0; ks < 8; ++ks) tc::mma_bf16_ts(t1, aSl + 8 * ks, dWh + 16 * ks, id2C, 1);
 #pragma unroll
-    for (int ks = 0; ks < 8; ++ks) tc::mma_bf16(t1, dSh + 16 * ks, dWl + 16 * ks, idC, 1);
+    for (int ks = 0; ks < 8; ++ks) tc::mma_bf16_ts(t1, aSh + 8 * ks, dWl + 16 * ks, idC, 1);
     tc::mma_commit(mma1);
     return true;
   };
@@ -852,8 +859,8 @@ __global__ void __launch_bounds__(kPassThreads, 1)
     bulk_prefetch_l2(wb.Kt + ck * wb.q_tile, static_cast<uint32_t>(wb.q_tile));
   };
   if (copy_warp) {
-    // each chunk's tiles as soon as their buffers are free: P, k and U (onto the D'
-    // tiles) of chunk it + 1 once group 2 of chunk it is done; W, q and vec of chunk it + 2
+    // each chunk's tiles as soon as their buffers are free: P, k and U of chunk it + 1 once
+    // group 2 of chunk it is done (and so the D phase that read U); W, q and vec of chunk it + 2
     // once group 1 of chunk it + 1 is done and every compute warp has finished chunk it's
     // output (vec[it & 1]). Each barrier of a chunk is armed only after this warp has seen
     // the phase it waits on for the chunk before, so no parity wait can alias a later phase
@@ -905,7 +912,7 @@ __global__ void __launch_bounds__(kPassThreads, 1)
     const int L = min(C, eos - t0);
     const uint32_t par = it & 1;
     const float* vec = reinterpret_cast<const float*>(sm + S::oVec + par * kVecFloats * 4);
-    const int base = par ? 384 : 0;  // chunk it's D^T / O1^T columns
+    const int base = par ? 256 : 0, other = par ? 0 : 256;  // X_p, X_(1-p)
     if (compute) {
       if (!mbar_wait_bounded(mma1, par)) mine = true;
       if (!mbar_wait_bounded(fullU, par)) mine = true;
@@ -932,9 +939,9 @@ __global__ void __launch_bounds__(kPassThreads, 1)
 #pragma unroll
         for (int e8 = 0; e8 < NH; e8 += 8) {
           const uint32_t o = tc::kmajor_offset(r, half * NH + e8, C);
-          // this thread's U^T values of the 8 tokens, read before its D' pieces overwrite them
-          const float4 u0 = *reinterpret_cast<const float4*>(sm + S::oEh + o);
-          const float4 u1 = *reinterpret_cast<const float4*>(sm + S::oEl + o);
+          // this thread's U^T values of the 8 tokens (two 16-byte pieces of the image)
+          const float4 u0 = *reinterpret_cast<const float4*>(sm + S::oU + o);
+          const float4 u1 = *reinterpret_cast<const float4*>(sm + S::oU + S::kUh + o);
           const float u[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
           float d[8], dd[8];
 #pragma unroll
@@ -943,13 +950,15 @@ __global__ void __launch_bounds__(kPassThreads, 1)
             dd[e] = d[e] * vec[64 + half * NH + e8 + e];
           }
           uint4 hi, lo;
+          const int col = kColDE + (half * NH + e8) / 2;  // token pairs of row r
           split8(d, hi, lo);
-          *reinterpret_cast<uint4*>(sm + S::oDh + o) = hi;
-          *reinterpret_cast<uint4*>(sm + S::oDl + o) = lo;
+          tc::tmem_st4(tc::taddr(tb, 32 * q, col), hi);
+          tc::tmem_st4(tc::taddr(tb, 32 * q, col + C / 2), lo);
           split8(dd, hi, lo);
-          *reinterpret_cast<uint4*>(sm + S::oEh + o) = hi;
-          *reinterpret_cast<uint4*>(sm + S::oEl + o) = lo;
+          tc::tmem_st4(tc::taddr(tb, 32 * q, col + C), hi);
+          tc::tmem_st4(tc::taddr(tb, 32 * q, col + 3 * C / 2), lo);
         }
+        tc::tmem_wait_st();
       }
     }
     bad = pass_sync(mine);
@@ -958,18 +967,24 @@ __global__ void __launch_bounds__(kPassThreads, 1)
       // ---- MMA group 2: O2^T = D^T P^T (3 products), update = D'^T K (2 products)
       if (lane == 0) {
         if (mbar_wait_bounded(fullB, par)) {
-#pragma unroll
-          for (int ks = 0; ks < KS; ++ks)
-            tc::mma_bf16(tb + 128, dDh + 16 * ks, dPh + 16 * ks, idC, ks > 0);
-#pragma unroll
-          for (int ks = 0; ks < KS; ++ks) tc::mma_bf16(tb + 128, dDh + 16 * ks, dPl + 16 * ks, idC, 1);
-#pragma unroll
-          for (int ks = 0; ks < KS; ++ks) tc::mma_bf16(tb + 128, dDl + 16 * ks, dPh + 16 * ks, idC, 1);
+          // the update into X_(1-p) first (the state chain waits for it alone), then O2^T over
+          // the raw D^T columns (read by now); A operands from tensor memory, a K step of 8
+          // columns
+          const uint32_t aDh = tb + kColDE, aDl = aDh + C / 2, aEh = aDh + C, aEl = aDh + 3 * C / 2;
 #pragma unroll
           for (int ks = 0; ks < KS; ++ks)  // a K step of the MN-major k tile: 4096 bytes (256 units)
-            tc::mma_bf16(tb + 256, dEh + 16 * ks, dKtile + 256 * ks, id128m, ks > 0);
+            tc::mma_bf16_ts(tb + other, aEh + 8 * ks, dKtile + 256 * ks, id128m, ks > 0);
 #pragma unroll
-          for (int ks = 0; ks < KS; ++ks) tc::mma_bf16(tb + 256, dEl + 16 * ks, dKtile + 256 * ks, id128m, 1);
+          for (int ks = 0; ks < KS; ++ks)
+            tc::mma_bf16_ts(tb + other, aEl + 8 * ks, dKtile + 256 * ks, id128m, 1);
+          tc::mma_commit(upd);
+#pragma unroll
+          for (int ks = 0; ks < KS; ++ks)
+            tc::mma_bf16_ts(tb + base, aDh + 8 * ks, dPh + 16 * ks, idC, ks > 0);
+#pragma unroll
+          for (int ks = 0; ks < KS; ++ks) tc::mma_bf16_ts(tb + base, aDh + 8 * ks, dPl + 16 * ks, idC, 1);
+#pragma unroll
+          for (int ks = 0; ks < KS; ++ks) tc::mma_bf16_ts(tb + base, aDl + 8 * ks, dPh + 16 * ks, idC, 1);
           tc::mma_commit(mma2);
           n2 = it + 1;
         } else {
@@ -978,7 +993,7 @@ __global__ void __launch_bounds__(kPassThreads, 1)
       }
     } else {  // compute warps
       const bool test_fail = test_fault == 2 && blockIdx.x == 0 && warp == 0 && it == 0;
-      if (test_fail ? !mbar_wait_bounded(dead, 0, kTestWaitNs) : !mbar_wait_bounded(mma2, par))
+      if (test_fail ? !mbar_wait_bounded(dead, 0, kTestWaitNs) : !mbar_wait_bounded(upd, par))
         mine = true;
       mine = __any_sync(0xffffffffu, mine);  // warp-uniform before the aligned loads
       tc::fence_after_sync();
@@ -988,8 +1003,8 @@ __global__ void __launch_bounds__(kPassThreads, 1)
 #pragma unroll
         for (int b0 = 0; b0 < 64; b0 += 32) {  // two loads in flight per wait
           float tv0[16], tv1[16];
-          tmem_load<16>(tc::taddr(tb, 32 * q, 256 + half * 64 + b0), tv0);
-          tmem_load<16>(tc::taddr(tb, 32 * q, 256 + half * 64 + b0 + 16), tv1);
+          tmem_load<16>(tc::taddr(tb, 32 * q, other + half * 64 + b0), tv0);
+          tmem_load<16>(tc::taddr(tb, 32 * q, other + half * 64 + b0 + 16), tv1);
           tc::tmem_wait_ld();
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
@@ -997,7 +1012,7 @@ __global__ void __launch_bounds__(kPassThreads, 1)
             Sr[b0 + 16 + e] = fmaf(gl, Sr[b0 + 16 + e], tv1[e]);
           }
         }
-        store_S_tiles();
+        store_S_tmem();
       }
     }
     bad = pass_sync(mine);
@@ -1009,51 +1024,57 @@ __global__ void __launch_bounds__(kPassThreads, 1)
       }
     } else {
       // chunk it's output O = f_t O1 + O2, while group 1 of chunk it + 1 runs
-      float o1[NH], o2[NH];
-      if constexpr (NH >= 16) {
+      // (O2 is there once the whole of group 2 is done; a failed wait skips the output)
+      if (!mbar_wait_bounded(mma2, par)) mine = true;
+      mine = __any_sync(0xffffffffu, mine);  // warp-uniform before the aligned loads
+      tc::fence_after_sync();
+      if (!mine) {
+        float o1[NH], o2[NH];
+        if constexpr (NH >= 16) {
 #pragma unroll
-        for (int b0 = 0; b0 < NH; b0 += 16) {
-          float ta[16], tbv[16];
-          tmem_load<16>(tc::taddr(tb, 32 * q, base + C + half * NH + b0), ta);
-          tmem_load<16>(tc::taddr(tb, 32 * q, 128 + half * NH + b0), tbv);
+          for (int b0 = 0; b0 < NH; b0 += 16) {
+            float ta[16], tbv[16];
+            tmem_load<16>(tc::taddr(tb, 32 * q, base + C + half * NH + b0), ta);
+            tmem_load<16>(tc::taddr(tb, 32 * q, base + half * NH + b0), tbv);
 #pragma unroll
-          for (int e = 0; e < 16; ++e) { o1[b0 + e] = ta[e]; o2[b0 + e] = tbv[e]; }
+            for (int e = 0; e < 16; ++e) { o1[b0 + e] = ta[e]; o2[b0 + e] = tbv[e]; }
+          }
+        } else {
+          float ta[8], tbv[8];
+          tmem_load<8>(tc::taddr(tb, 32 * q, base + C + half * NH), ta);
+          tmem_load<8>(tc::taddr(tb, 32 * q, base + half * NH), tbv);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) { o1[e] = ta[e]; o2[e] = tbv[e]; }
         }
-      } else {
-        float ta[8], tbv[8];
-        tmem_load<8>(tc::taddr(tb, 32 * q, base + C + half * NH), ta);
-        tmem_load<8>(tc::taddr(tb, 32 * q, 128 + half * NH), tbv);
+        tc::tmem_wait_ld();
+        if (a.out_f32) {
 #pragma unroll
-        for (int e = 0; e < 8; ++e) { o1[e] = ta[e]; o2[e] = tbv[e]; }
-      }
-      tc::tmem_wait_ld();
-      if (a.out_f32) {
+          for (int e = 0; e < NH; ++e) {
+            const int tt = half * NH + e;
+            if (tt < L)
+              static_cast<float*>(a.out)[(static_cast<int64_t>(t0 + tt) * a.Hv + h) * kD + r] =
+                  fmaf(vec[tt], o1[e], o2[e]);
+          }
+        } else {
+          // stage the warp's [NH tokens x 32 dv] block in the bf16 tile, then copy it out in
+          // 16-byte pieces; the tile's 16-byte pieces are XOR-swizzled by token so both the
+          // 2-byte writes and the 16-byte reads are free of bank conflicts
+          unsigned char* ot = sm + S::oO;
 #pragma unroll
-        for (int e = 0; e < NH; ++e) {
-          const int tt = half * NH + e;
-          if (tt < L)
-            static_cast<float*>(a.out)[(static_cast<int64_t>(t0 + tt) * a.Hv + h) * kD + r] =
-                fmaf(vec[tt], o1[e], o2[e]);
-        }
-      } else {
-        // stage the warp's [NH tokens x 32 dv] block in the bf16 tile, then copy it out in
-        // 16-byte pieces; the tile's 16-byte pieces are XOR-swizzled by token so both the
-        // 2-byte writes and the 16-byte reads are free of bank conflicts
-        unsigned char* ot = sm + S::oO;
+          for (int e = 0; e < NH; ++e) {
+            const int tt = half * NH + e;
+            *reinterpret_cast<uint16_t*>(ot + out_tile_offset(tt, r)) = f2bf(fmaf(vec[tt], o1[e], o2[e]));
+          }
+          __syncwarp();
 #pragma unroll
-        for (int e = 0; e < NH; ++e) {
-          const int tt = half * NH + e;
-          *reinterpret_cast<uint16_t*>(ot + out_tile_offset(tt, r)) = f2bf(fmaf(vec[tt], o1[e], o2[e]));
-        }
-        __syncwarp();
-#pragma unroll
-        for (int k = 0; k < NH / 8; ++k) {
-          const int pc = lane + 32 * k;
-          const int tt = half * NH + pc / 4, col = 32 * q + (pc % 4) * 8;
-          if (tt < L)
-            *reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.out) +
-                                      (static_cast<int64_t>(t0 + tt) * a.Hv + h) * kD + col) =
-                *reinterpret_cast<const uint4*>(ot + out_tile_offset(tt, col));
+          for (int k = 0; k < NH / 8; ++k) {
+            const int pc = lane + 32 * k;
+            const int tt = half * NH + pc / 4, col = 32 * q + (pc % 4) * 8;
+            if (tt < L)
+              *reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.out) +
+                                        (static_cast<int64_t>(t0 + tt) * a.Hv + h) * kD + col) =
+                  *reinterpret_cast<const uint4*>(ot + out_tile_offset(tt, col));
+          }
         }
       }
       __syncwarp();

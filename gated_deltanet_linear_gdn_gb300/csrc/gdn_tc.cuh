@@ -14,7 +14,8 @@
 //
 // Accumulators (M = 128, cta_group::1): row i of D lives in tensor-memory lane
 // i, column j in column (base + j); warp w of the CTA may access lanes
-// 32 * (w % 4) .. 32 * (w % 4) + 31.
+// 32 * (w % 4) .. 32 * (w % 4) + 31. An A operand may live in tensor memory too
+// (mma_bf16_ts), row m in lane m, two bf16 of K per column.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -101,6 +102,19 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint6
       : "memory");
 }
 
+// The same with the A operand in tensor memory (M = 128: row m in lane m; K = 16 per MMA as 8
+// columns, each holding the bf16 pair (k, k + 1) with element k in the low half; checked
+// against exact integer products before use).
+__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Arrive (once) on an mbarrier when every MMA this thread issued so far is done.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
@@ -145,6 +159,16 @@ __device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&v)[8]) {
 }
 __device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// --- registers -> tensor memory: 32 lanes x 4 columns of 32 bits per warp (lane = thread) ---
+__device__ __forceinline__ void tmem_st4(uint32_t taddr, const uint4& v) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr),
+               "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
 // tensor-memory address of (lane, column)

@@ -16,18 +16,19 @@ blocked) -- what a time bound does. The roles then follow the kernel's failure h
 Checked over many schedules, chunk counts and failure points: every warp finishes (the
 unbounded named and CTA barriers stay matched), and when tensor memory is freed no bulk copy
 is in flight and no MMA group is queued or running. The buffer-version checks of the
-success-path model keep holding. Planted mistakes (the copy warp's drain left out, or done
-only after its own failure) each fail some schedule. The MMA warp's drain is never needed here:
-every committed MMA group is waited for by the compute warps before any warp can leave the
-loop (a wait that gives up skips one warp's wait, the others still wait), so it stays as a
-guard only. Host logic only.
+success-path model keep holding. Planted mistakes each fail some schedule:
+the copy warp's drain left out, or done only after its own failure; the MMA warp's drain left
+out -- a failure reported at the barrier after the state update leaves the warps to exit while
+the second part of group 2 (O2, which only the output waits for) may still run. Host logic
+only.
 """
 import random
 
 import pytest
 
 import test_pass_protocol_model as base
-from test_pass_protocol_model import N_COMPUTE, par, tm_d
+from test_pass_protocol_model import (N_COMPUTE, g1_reads, g1_writes, o2_reads, o2_writes, par,
+                                      u_bufs, upd_reads, upd_writes, xp)
 
 
 class FailSim(base.Sim):
@@ -96,7 +97,7 @@ def copy_warp(s, me):
     if nch > 0:
         s.copy("fullA", ["W", "Q", ("vec", 0)], 0)
         s.copy("fullB", ["P", "Kt"], 0)
-        s.copy("fullU", [("E", w) for w in range(N_COMPUTE)], ("U", 0))
+        s.copy("fullU", u_bufs(), ("U", 0))
         nA = nBU = 1
     yield from s.sync("cta", 10)
     ok = True
@@ -115,7 +116,7 @@ def copy_warp(s, me):
                 ok = False
                 break
             s.copy("fullB", ["P", "Kt"], it + 1)
-            s.copy("fullU", [("E", w) for w in range(N_COMPUTE)], ("U", it + 1))
+            s.copy("fullU", u_bufs(), ("U", it + 1))
             nBU = it + 2
             if it + 2 < nch:
                 if not (yield from s.bounded("oDone", it, me)):
@@ -146,8 +147,7 @@ def mma_warp(s, me):
         nonlocal n1
         if not (yield from s.bounded("fullA", k, me)):
             return False
-        s.mma(f"mma1({k})", [(("S", w), k) for w in range(N_COMPUTE)] + [("W", k), ("Q", k)],
-              [(tm_d(s, k), k)], "mma1", k)
+        s.mma(f"mma1({k})", g1_reads(k), g1_writes(s, k), "mma1", k)
         n1 = k + 1
         return True
 
@@ -159,9 +159,8 @@ def mma_warp(s, me):
         if bad[0]:
             break
         if (yield from s.bounded("fullB", it, me)):
-            s.mma(f"mma2({it})", [(("D", w), it) for w in range(N_COMPUTE)]
-                  + [(("E", w), ("D'", it)) for w in range(N_COMPUTE)] + [("P", it), ("Kt", it)],
-                  [("tmO2", it)], "mma2", it)
+            s.mma(f"upd({it})", upd_reads(it), upd_writes(s, it), "upd", it)
+            s.mma(f"mma2({it})", o2_reads(it), o2_writes(s, it), "mma2", it)
             n2 = it + 1
         else:
             mine = True
@@ -190,32 +189,37 @@ def compute_warp(s, w, me):
         ok2 = yield from s.bounded("fullU", it, me)
         mine = mine or not (ok1 and ok2)
         tag = f"warp{w} chunk {it}"
+        x = xp(s, it)
         if not mine:
-            s.read(tm_d(s, it), it, tag)
-            s.read(("E", w), ("U", it), tag)
+            s.read(("Xd", x), ("raw", it), tag)
+            s.read(("U", w), ("U", it), tag)
             s.read(("vec", par(it)), it, tag)
             yield lambda: True
             s.write(("D", w), it)
-            s.write(("E", w), ("D'", it))
+            s.write(("E", w), it)
         yield from s.or_sync("named", N_COMPUTE + 1, mine, bad)            # B1
         if bad[0]:
             break
-        if not (yield from s.bounded("mma2", it, me)):
+        if not (yield from s.bounded("upd", it, me)):
             mine = True
         if not mine:
-            s.read("tmO2", it, tag)
+            s.read(("Xd", 1 - x), ("dS", it), tag)
+            s.read(("Xo", 1 - x), ("dS", it), tag)
             s.read(("vec", par(it)), it, tag)
             s.write(("S", w), it + 1)
         yield from s.or_sync("named", N_COMPUTE + 1, mine, bad)            # B2
         if bad[0]:
             break
-        s.read_begin(tm_d(s, it), it, tag)
-        s.read_begin("tmO2", it, tag)
-        s.read_begin(("vec", par(it)), it, tag)
-        yield lambda: True
-        s.read_end(tm_d(s, it), it, tag)
-        s.read_end("tmO2", it, tag)
-        s.read_end(("vec", par(it)), it, tag)
+        if not (yield from s.bounded("mma2", it, me)):
+            mine = True                  # the output is skipped; reported at the next barrier
+        if not mine:
+            s.read_begin(("Xo", x), ("O1", it), tag)
+            s.read_begin(("Xd", x), ("O2", it), tag)
+            s.read_begin(("vec", par(it)), it, tag)
+            yield lambda: True
+            s.read_end(("Xo", x), ("O1", it), tag)
+            s.read_end(("Xd", x), ("O2", it), tag)
+            s.read_end(("vec", par(it)), it, tag)
         s.arrive_odone(it)
     yield from s.or_sync("named", N_COMPUTE + 1, bad[0] or mine, bad)
     yield from s.sync("cta", 10)
@@ -270,10 +274,11 @@ def test_pass_failure_path_drains_and_finishes(nch):
         assert s.failed
 
 
-@pytest.mark.parametrize("mutant", ["no copy drain", "drain only on own failure"])
+@pytest.mark.parametrize("mutant", ["no copy drain", "drain only on own failure", "no MMA drain"])
 def test_failure_model_catches_missing_drains(mutant):
     """Leaving out the copy warp's drain, or draining only after its own failure, lets the CTA
-    free tensor memory (and exit) with copies still landing in its shared memory."""
+    free tensor memory (and exit) with copies still landing in its shared memory; leaving out
+    the MMA warp's drain lets it free tensor memory under a running MMA group."""
     caught = 0
     total = waits_in_clean_run(5)
     for seed in range(80):

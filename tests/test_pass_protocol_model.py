@@ -3,9 +3,13 @@ pass_tc_kernel): a copy warp, an MMA warp and eight compute warps, in the order 
 executes its steps, over mbarriers with the hardware's parity semantics (a wait for phase k
 returns once the barrier's current phase has a different parity), transaction-counted
 barriers completed when a bulk copy lands, MMA groups that run in issue order and complete
-their commit barrier when done, a named barrier over the compute and MMA warps, and the CTA
+their commit barrier when done (group 2 in two parts: the state update, committed on its own
+barrier, then O2), a named barrier over the compute and MMA warps, and the CTA
 barriers. Copies and MMA groups take random times and the scheduler interleaves the warps at
-random. Over many schedules and chunk counts it checks that
+random. The buffers are shared-memory tiles (W, q, P, k, the U image, vec) and tensor-memory
+regions: the bf16 operand parts of the state and of D / D' (each warp its rows), and two
+accumulator regions that alternate by chunk parity -- a chunk's raw D^T, then its O2^T, and
+O1^T in one, its state update in the other. Over many schedules and chunk counts it checks that
 
 - no parity wait can alias: while a thread waits for phase k the barrier never completes
   phase k + 1 (else the wait would miss phase k and hang);
@@ -15,7 +19,8 @@ random. Over many schedules and chunk counts it checks that
 - every warp finishes.
 
 Planted mistakes (a missing wait, a buffer reused early, an early arrival, a group issued
-before its barrier, one accumulator set instead of two) each fail some schedule, so the
+before its barrier, one accumulator set instead of two, the output read before the second
+part of group 2 is done) each fail some schedule, so the
 checks have teeth. The model is host logic only; the GPU tests run the kernel itself.
 """
 import random
@@ -48,7 +53,7 @@ class Bar:
 class Sim:
     def __init__(self, nch, rng, mutant=None):
         self.nch, self.rng, self.mutant = nch, rng, mutant
-        self.bars = {n: Bar(n) for n in ("fullA", "fullB", "fullU", "mma1", "mma2")}
+        self.bars = {n: Bar(n) for n in ("fullA", "fullB", "fullU", "mma1", "upd", "mma2")}
         self.bars["oDone"] = Bar("oDone", N_COMPUTE + 1)
         self.events = []      # [countdown, callable]
         self.mma_queue = []   # MMA groups in issue order: (name, start_fn, finish_fn)
@@ -117,7 +122,7 @@ class Sim:
         if self.mma_busy is None and self.mma_queue:
             start, finish = self.mma_queue.pop(0)
             start()
-            self.mma_busy = [self.rng.randint(1, 10), finish]
+            self.mma_busy = [self.rng.randint(1, 40), finish]  # at times longer than a copy
 
     # ---- thread-side waits (generators yield predicates)
     def wait(self, bar, k):
@@ -143,9 +148,45 @@ def par(k):
     return k & 1
 
 
-def tm_d(s, k):
-    """Tensor-memory columns of chunk k's D^T and O1^T: two sets, by parity."""
-    return ("tmD", 0 if s.mutant == "one D/O1 set" else par(k))
+def xp(s, k):
+    """The accumulator region of chunk k (X0 or X1, by parity): its raw D^T, then O2^T, in the
+    "d" half and O1^T in the "o" half; the other region takes chunk k's state update."""
+    return 0 if s.mutant == "one D/O1 set" else par(k)
+
+
+def u_bufs():
+    """The U^T image in shared memory: every compute warp's rows."""
+    return [("U", w) for w in range(N_COMPUTE)]
+
+
+def g1_reads(k):
+    """Group 1 of chunk k: the state's hi / lo parts (tensor memory, each warp's rows), W, q."""
+    return [(("S", w), k) for w in range(N_COMPUTE)] + [("W", k), ("Q", k)]
+
+
+def g1_writes(s, k):
+    x = xp(s, k)
+    return [(("Xd", x), ("raw", k)), (("Xo", x), ("O1", k))]
+
+
+def upd_reads(k):
+    """Group 2 of chunk k, first part (committed on its own barrier): the state update from
+    D' hi / lo (tensor memory, each warp's rows) and the k tile."""
+    return [(("E", w), k) for w in range(N_COMPUTE)] + [("Kt", k)]
+
+
+def upd_writes(s, k):
+    x = xp(s, k)
+    return [(("Xd", 1 - x), ("dS", k)), (("Xo", 1 - x), ("dS", k))]
+
+
+def o2_reads(k):
+    """Group 2 of chunk k, second part: O2^T from D hi / lo and the P tiles."""
+    return [(("D", w), k) for w in range(N_COMPUTE)] + [("P", k)]
+
+
+def o2_writes(s, k):
+    return [(("Xd", xp(s, k)), ("O2", k))]
 
 
 def copy_warp(s):
@@ -153,7 +194,7 @@ def copy_warp(s):
     if nch > 0:
         s.copy("fullA", ["W", "Q", ("vec", 0)], 0)
         s.copy("fullB", ["P", "Kt"], 0)
-        s.copy("fullU", [("E", w) for w in range(N_COMPUTE)], ("U", 0))
+        s.copy("fullU", u_bufs(), ("U", 0))
     yield from s.sync("cta", 10)
     if nch == 0:
         yield from s.sync("cta", 10)
@@ -164,12 +205,12 @@ def copy_warp(s):
         yield from s.wait("mma1", 0)
         s.copy("fullA", ["W", "Q", ("vec", 1)], 1)
         if early_u:
-            s.copy("fullU", [("E", w) for w in range(N_COMPUTE)], ("U", 1))
+            s.copy("fullU", u_bufs(), ("U", 1))
     for it in range(nch - 1):
         yield from s.wait("mma2", it)
         s.copy("fullB", ["P", "Kt"], it + 1)
         if not early_u:
-            s.copy("fullU", [("E", w) for w in range(N_COMPUTE)], ("U", it + 1))
+            s.copy("fullU", u_bufs(), ("U", it + 1))
         if it + 2 < nch:
             if s.mutant == "arrive early":
                 s.bars["oDone"].arrive(it + 1)
@@ -180,7 +221,7 @@ def copy_warp(s):
             yield from s.wait("mma1", it + 1)
             s.copy("fullA", ["W", "Q", ("vec", par(it + 2))], it + 2)
             if early_u:
-                s.copy("fullU", [("E", w) for w in range(N_COMPUTE)], ("U", it + 2))
+                s.copy("fullU", u_bufs(), ("U", it + 2))
     yield from s.sync("cta", 10)
 
 
@@ -190,17 +231,15 @@ def mma_warp(s):
 
     def issue1(k):
         yield from s.wait("fullA", k)
-        s.mma(f"mma1({k})", [(("S", w), k) for w in range(N_COMPUTE)] + [("W", k), ("Q", k)],
-              [(tm_d(s, k), k)], "mma1", k)
+        s.mma(f"mma1({k})", g1_reads(k), g1_writes(s, k), "mma1", k)
 
     if nch > 0:
         yield from issue1(0)
     for it in range(nch):
         yield from s.sync("named", N_COMPUTE + 1)                          # B1
         yield from s.wait("fullB", it)
-        s.mma(f"mma2({it})", [(("D", w), it) for w in range(N_COMPUTE)]
-              + [(("E", w), ("D'", it)) for w in range(N_COMPUTE)] + [("P", it), ("Kt", it)],
-              [("tmO2", it)], "mma2", it)
+        s.mma(f"upd({it})", upd_reads(it), upd_writes(s, it), "upd", it)
+        s.mma(f"mma2({it})", o2_reads(it), o2_writes(s, it), "mma2", it)
         if s.mutant == "group 1 before the state barrier" and it + 1 < nch:
             yield from issue1(it + 1)
         yield from s.sync("named", N_COMPUTE + 1)                          # B2
@@ -218,24 +257,28 @@ def compute_warp(s, w):
         yield from s.wait("mma1", it)
         yield from s.wait("fullU", it)
         tag = f"warp{w} chunk {it}"
-        s.read(tm_d(s, it), it, tag)
-        s.read(("E", w), ("U", it), tag)                                   # its own U bytes
+        x = xp(s, it)
+        s.read(("Xd", x), ("raw", it), tag)
+        s.read(("U", w), ("U", it), tag)                                   # its rows of U
         s.read(("vec", par(it)), it, tag)
         yield lambda: True                                                 # other warps may run
-        s.write(("D", w), it)                                              # its D, D' pieces
-        s.write(("E", w), ("D'", it))
+        s.write(("D", w), it)                                              # its D, D' rows
+        s.write(("E", w), it)
         yield from s.sync("named", N_COMPUTE + 1)                          # B1
-        yield from s.wait("mma2", it)
-        s.read("tmO2", it, tag)
+        yield from s.wait("upd", it)
+        s.read(("Xd", 1 - x), ("dS", it), tag)                             # the state update
+        s.read(("Xo", 1 - x), ("dS", it), tag)
         s.read(("vec", par(it)), it, tag)
         s.write(("S", w), it + 1)                                          # next chunk's S rows
         yield from s.sync("named", N_COMPUTE + 1)                          # B2
-        s.read_begin(tm_d(s, it), it, tag)                                 # O1, under group 1
-        s.read_begin("tmO2", it, tag)
+        if s.mutant != "output before O2":
+            yield from s.wait("mma2", it)
+        s.read_begin(("Xo", x), ("O1", it), tag)                           # under group 1
+        s.read_begin(("Xd", x), ("O2", it), tag)
         s.read_begin(("vec", par(it)), it, tag)
         yield lambda: True
-        s.read_end(tm_d(s, it), it, tag)
-        s.read_end("tmO2", it, tag)
+        s.read_end(("Xo", x), ("O1", it), tag)
+        s.read_end(("Xd", x), ("O2", it), tag)
         s.read_end(("vec", par(it)), it, tag)
         s.bars["oDone"].arrive(it)
     yield from s.sync("named", N_COMPUTE + 1)
@@ -271,7 +314,8 @@ def test_pass_protocol_over_random_schedules(nch):
 
 
 @pytest.mark.parametrize("mutant", ["no output barrier", "U after group 1", "arrive early",
-                                    "group 1 before the state barrier", "one D/O1 set"])
+                                    "group 1 before the state barrier", "one D/O1 set",
+                                    "output before O2"])
 def test_model_catches_planted_mistakes(mutant):
     """Each mistake, planted in the model, fails some schedule."""
     caught = 0
