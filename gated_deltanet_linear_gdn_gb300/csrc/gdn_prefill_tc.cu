@@ -5,9 +5,10 @@
 // Source: vLLM PR #53864 (CuteDSL GDN prefill), "Numerical root cause and
 // fix": the prefill forms the per-chunk KK^T block and inverts the unit
 // lower-triangular matrix built from it; a bf16 Newton-Schulz inverse fails on
-// correlated keys. Here that inverse is solved EXACTLY in fp32 (forward
-// substitution, one column per thread), and every contraction runs on the
-// tensor cores with fp32 accumulation.
+// correlated keys. Here that inverse is solved EXACTLY in fp32 (a blocked
+// recursive inverse: 8 x 8 diagonal blocks by forward substitution, then blocks
+// of 16, 32 and 64 rows as T21 = -T22 (A21 T11)), and every contraction runs on
+// the tensor cores with fp32 accumulation.
 //
 // Algebra per chunk of C tokens starting from state S0 (G_t = running sum of g
 // inside the chunk, raw bf16 q, k, v, inverse norms iq_t, ik_t):
@@ -170,10 +171,11 @@ __device__ __forceinline__ bool pass_sync(bool bad) {
   return any != 0;
 }
 
-// acc[i][j] += sum_k a[i][k] b[k][j] for 4 x 4 fp32 blocks held as float4 rows
-__device__ __forceinline__ void fma4x4(float (&acc)[4][4], const float4 (&a)[4], const float4 (&b)[4]) {
+// acc[i][j] += sum_k a[i][k] b[k][j] for RB x 4 fp32 blocks held as float4 rows (k = 0..3)
+template <int RB>
+__device__ __forceinline__ void fma_rows(float (&acc)[RB][4], const float4 (&a)[RB], const float4 (&b)[4]) {
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
+  for (int i = 0; i < RB; ++i) {
     const float ai[4] = {a[i].x, a[i].y, a[i].z, a[i].w};
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk) {
@@ -185,8 +187,69 @@ __device__ __forceinline__ void fma4x4(float (&acc)[4][4], const float4 (&a)[4],
   }
 }
 
-// barrier of the intra kernel's two solver warps (warps 0-1; named barrier 1)
-__device__ __forceinline__ void solver_sync() { asm volatile("bar.sync 1, 64;" ::: "memory"); }
+// barrier of the intra kernel's four solver warps (warps 0-3; named barrier 1)
+constexpr int kSolveThreads = 128;
+__device__ __forceinline__ void solver_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+// One level of the intra kernel's blocked inverse (the solver threads): every diagonal block of
+// 2b rows of a chunk is built from its two b-row halves, already inverted in place, as
+// T21 = -T22 (A21 T11), written over A21 (rows of stride SA floats, chunk-local columns). A
+// thread takes RB rows x 4 columns of T21; the products skip the zero parts of the triangular
+// factors (T11 has none above its diagonal, T22 none right of it).
+template <int b, int C, int SA>
+__device__ __forceinline__ void solve_merge(float* sA, int tid) {
+  constexpr int RB = b == 32 ? 2 : 1;      // rows per thread
+  constexpr int COLS = b / 4;              // 4-column groups of a row
+  constexpr int PER = b * b / (4 * RB);    // threads per block
+  constexpr int NT = (64 / (2 * b)) * PER;  // threads at work
+  static_assert(NT <= kSolveThreads && NT % 32 == 0, "whole warps of the solver threads");
+  const bool on = tid < NT;
+  const int m = tid / PER, idx = tid % PER;
+  const int R0 = 2 * b * m, o = R0 % C;
+  const int j0 = 4 * (idx % COLS), i0 = RB * (idx / COLS);
+  float* A21 = sA + (R0 + b + i0) * SA + o;  // the thread's row i: A21 + i SA
+  float acc[RB][4];
+#pragma unroll
+  for (int i = 0; i < RB; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.0f;
+  if (on) {  // X = A21 T11: column block j0 needs rows l >= j0 of T11
+    for (int l = j0; l < b; l += 4) {
+      float4 av[RB], tv[4];
+#pragma unroll
+      for (int i = 0; i < RB; ++i) av[i] = *reinterpret_cast<const float4*>(A21 + i * SA + l);
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk)
+        tv[kk] = *reinterpret_cast<const float4*>(sA + (R0 + l + kk) * SA + o + j0);
+      fma_rows<RB>(acc, av, tv);
+    }
+  }
+  solver_sync();  // every A21 read: X takes its place
+  if (on) {
+#pragma unroll
+    for (int i = 0; i < RB; ++i)
+      *reinterpret_cast<float4*>(A21 + i * SA + j0) = make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+  }
+  solver_sync();
+#pragma unroll
+  for (int i = 0; i < RB; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.0f;
+  if (on) {  // T22 X: rows i0 .. i0 + RB - 1 of T22 need columns l < i0 + RB
+    for (int l = 0; l < i0 + RB; l += 4) {
+      float4 av[RB], xv[4];
+#pragma unroll
+      for (int i = 0; i < RB; ++i) av[i] = *reinterpret_cast<const float4*>(A21 + i * SA + b + l);
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk)
+        xv[kk] = *reinterpret_cast<const float4*>(sA + (R0 + b + l + kk) * SA + o + j0);
+      fma_rows<RB>(acc, av, xv);
+    }
+  }
+  solver_sync();  // every X read: T21 takes its place
+  if (on) {
+#pragma unroll
+    for (int i = 0; i < RB; ++i)
+      *reinterpret_cast<float4*>(A21 + i * SA + j0) =
+          make_float4(-acc[i][0], -acc[i][1], -acc[i][2], -acc[i][3]);
+  }
+}
 
 // ============================================================== intra kernel
 // A CTA takes 64 token rows (64 / C chunks) of one k-head, so that two CTAs fit on an SM
@@ -434,93 +497,53 @@ __global__ void __launch_bounds__(kThreadsTc, 2)
     bad = tc_sync(bad);
     if (bad) break;
 
-    if (tid < NR) {
+    if (tid < kSolveThreads) {
       // exact fp32 T = (I + A)^-1 of every chunk, written over A in place (A is strictly lower
-      // triangular, so its upper part already holds T's zeros)
-      // 1) diagonal blocks of B1 = min(C, 32) rows: forward substitution, a column per thread,
-      //    A's rows read 16 bytes at a time (the same address across the warp's block)
-      constexpr int B1 = C < 32 ? C : 32;
-      {
-        const int row0 = (tid / B1) * B1, c = tid % B1;
-        float* Ab = sA + row0 * SA + row0 % C;  // block entry (r, l): Ab[r * SA + l]
-        float x[B1];
+      // triangular, so its upper part already holds T's zeros), a blocked recursive inverse:
+      // 1) the 8 x 8 diagonal blocks by forward substitution, a column per thread (threads
+      //    0..63), A's rows read 16 bytes at a time (the same address across the block's threads)
+      float x[8];
+      const int R0 = 8 * (tid >> 3), cc = tid & 7;
+      float* Ab = sA + R0 * SA + R0 % C;  // block entry (r, l): Ab[r * SA + l]
+      if (tid < 64) {
 #pragma unroll
-        for (int r = 0; r < B1; ++r) {
+        for (int r = 0; r < 8; ++r) {
+          const float4 a0 = *reinterpret_cast<const float4*>(Ab + r * SA);
+          const float4 a1 = *reinterpret_cast<const float4*>(Ab + r * SA + 4);
+          const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
           float s0 = 0.0f, s1 = 0.0f;
 #pragma unroll
-          for (int l = 0; l < r; l += 4) {
-            const float4 a4 = *reinterpret_cast<const float4*>(Ab + r * SA + l);
-            s0 = fmaf(a4.x, x[l], s0);
-            if (l + 1 < r) s1 = fmaf(a4.y, x[l + 1], s1);
-            if (l + 2 < r) s0 = fmaf(a4.z, x[l + 2], s0);
-            if (l + 3 < r) s1 = fmaf(a4.w, x[l + 3], s1);
+          for (int l = 0; l < r; l += 2) {
+            s0 = fmaf(av[l], x[l], s0);
+            if (l + 1 < r) s1 = fmaf(av[l + 1], x[l + 1], s1);
           }
-          x[r] = (r < c) ? 0.0f : (r == c ? 1.0f : -(s0 + s1));
+          x[r] = (r < cc) ? 0.0f : (r == cc ? 1.0f : -(s0 + s1));
         }
-        solver_sync();  // every block of A read
-#pragma unroll
-        for (int r = 0; r < B1; ++r) Ab[r * SA + c] = x[r];
       }
-      if constexpr (C == 64) {
-        // 2) the off-diagonal block T21 = -T22 (A21 T11) (T11, T22 now in place of A11, A22):
-        //    64 threads, 4 x 4 outputs each from 16-byte row loads
-        const int k = tid, r0 = 4 * (k >> 3), c0 = 4 * (k & 7);
-        float* Ac = sA;
-        float acc[4][4];
+      solver_sync();  // every diagonal block read
+      if (tid < 64) {
+#pragma unroll
+        for (int r = 0; r < 8; ++r) Ab[r * SA + cc] = x[r];
+      }
+      // 2) blocks of 16, 32 and 64 rows, as far as the chunk goes, from their two halves
+      solver_sync();
+      solve_merge<8, C, SA>(sA, tid);
+      if constexpr (C >= 32) {
         solver_sync();
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-#pragma unroll
-          for (int jj = 0; jj < 4; ++jj) acc[i][jj] = 0.0f;
-#pragma unroll
-        for (int l = 0; l < 32; l += 4) {  // X = A21 T11
-          float4 av4[4], tv4[4];
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-            av4[i] = *reinterpret_cast<const float4*>(Ac + (32 + r0 + i) * SA + l);
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            tv4[kk] = *reinterpret_cast<const float4*>(Ac + (l + kk) * SA + c0);
-          fma4x4(acc, av4, tv4);
-        }
-        solver_sync();  // A21 read: X takes its place
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-          *reinterpret_cast<float4*>(Ac + (32 + r0 + i) * SA + c0) =
-              make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+        solve_merge<16, C, SA>(sA, tid);
+      }
+      if constexpr (C >= 64) {
         solver_sync();
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-#pragma unroll
-          for (int jj = 0; jj < 4; ++jj) acc[i][jj] = 0.0f;
-#pragma unroll
-        for (int l = 0; l < 32; l += 4) {  // T22 X; rows r0 .. r0+3 of T22 vanish past column r0+3
-          if (l < r0 + 4) {
-            float4 av4[4], xv4[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-              av4[i] = *reinterpret_cast<const float4*>(Ac + (32 + r0 + i) * SA + 32 + l);
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              xv4[kk] = *reinterpret_cast<const float4*>(Ac + (32 + l + kk) * SA + c0);
-            fma4x4(acc, av4, xv4);
-          }
-        }
-        solver_sync();  // X read: T21 takes its place
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-          *reinterpret_cast<float4*>(Ac + (32 + r0 + i) * SA + c0) =
-              make_float4(-acc[i][0], -acc[i][1], -acc[i][2], -acc[i][3]);
+        solve_merge<32, C, SA>(sA, tid);
       }
       solver_sync();
       // 3) T' = T diag(beta) and T'' = T diag(beta e^G ik) into the block-diagonal bf16 hi / lo
-      //    tiles: row tid, 8 columns at a time, 16-byte stores (the warp's lanes on consecutive
-      //    rows)
+      //    tiles: row tid % 64, groups of 8 columns (tid / 64) + 2k, 16-byte stores (the warp's
+      //    lanes on consecutive rows)
       {
-        const int t = tid, ci = t / C;
+        const int t = tid & 63, ci = t / C;
         const float* Tr = sA + t * SA;
-#pragma unroll
-        for (int g = 0; g < C / 8; ++g) {
+        for (int g = tid >> 6; g < C / 8; g += 2) {
           const float4 u0 = *reinterpret_cast<const float4*>(Tr + 8 * g);
           const float4 u1 = *reinterpret_cast<const float4*>(Tr + 8 * g + 4);
           const float tv[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
@@ -542,12 +565,12 @@ __global__ void __launch_bounds__(kThreadsTc, 2)
           *reinterpret_cast<uint4*>(sm + S::oT2l + o) = lo;
         }
       }
-    } else if (tid < NR + 128) {
+    } else {
       // V (raw bf16) as an MN-major operand over the 64 tokens, in the k tile's layout:
       // 16-byte pieces of 8 channels of one token. A thread takes channel group cg of tokens
       // 8i + (u & 7), i = 0..7: the 8 lanes sharing cg hold 8 consecutive tokens, so each
       // 16-byte store hits its own bank group. All 8 loads are issued before the first store
-      const int u = tid - NR;
+      const int u = tid - kSolveThreads;
       const int cg = (u >> 3) & 15, tr = u & 7;
       const uint16_t* yv = y + 2 * a.Hk * kD + h * kD + 8 * cg;
       uint4 vb[8];
@@ -561,11 +584,9 @@ __global__ void __launch_bounds__(kThreadsTc, 2)
 #pragma unroll
       for (int i = 0; i < 8; ++i)
         *reinterpret_cast<uint4*>(sm + S::oV + tc::kmajor_offset(8 * i + tr, 8 * cg, kD)) = vb[i];
-    } else if (hr == 0) {
-      // the last two warps, idle during the solve: the q and k tiles of each chunk ->
-      // workspace (a chunk's rows are one contiguous slice of either smem tile)
-      const int u = tid - (NR + 128);
-      for (int ci = 0; ci < CPC; ++ci) {
+      // then, for the first value head, the q and k tiles of each chunk -> workspace (a
+      // chunk's rows are one contiguous slice of either smem tile)
+      for (int ci = 0; ci < CPC && hr == 0; ++ci) {
         const int c = c_first + ci;
         if (c >= nchunks) break;
         const size_t slice = static_cast<size_t>(C) * kD * 2;  // bytes of one chunk's tile
@@ -573,7 +594,7 @@ __global__ void __launch_bounds__(kThreadsTc, 2)
         const uint4* srck = reinterpret_cast<const uint4*>(sm + S::oK + ci * slice);
         uint4* dq = reinterpret_cast<uint4*>(wb.Qt + (static_cast<size_t>(c) * a.Hk + kh) * wb.q_tile);
         uint4* dk = reinterpret_cast<uint4*>(wb.Kt + (static_cast<size_t>(c) * a.Hk + kh) * wb.q_tile);
-        for (int i = u; i < static_cast<int>(slice / 16); i += kThreadsTc - NR - 128) {
+        for (int i = u; i < static_cast<int>(slice / 16); i += kThreadsTc - kSolveThreads) {
           dq[i] = srcq[i];
           dk[i] = srck[i];
         }

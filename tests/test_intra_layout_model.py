@@ -11,6 +11,7 @@ import pytest
 
 NR = 64          # token rows per CTA
 THREADS = 256
+NSOLVE = 128     # threads 0..127 solve; 128..255 build the V tile and copy the q / k tiles
 KD = 128         # dk = dv
 
 
@@ -97,20 +98,22 @@ def test_intra_writes_cover_each_piece_once(C):
             (k if which else q).append(kmajor_offset(tok, 64 * hf + 8 * k8, KD))
     pieces_once(q, L["Q"][1], "q tile")
     pieces_once(k, L["K"][1], "k tile")
-    # V: threads NR .. NR + 127, channel group cg, tokens 8 i + tr
+    # V: threads NSOLVE .. 255, channel group cg, tokens 8 i + tr
     v = []
-    for tid in range(NR, NR + 128):
-        u = tid - NR
+    for tid in range(NSOLVE, THREADS):
+        u = tid - NSOLVE
         cg, tr = (u >> 3) & 15, u & 7
         for i in range(8):
             v.append(kmajor_offset(8 * i + tr, 8 * cg, KD))
     pieces_once(v, L["V"][1], "V tile")
-    # T' / T'': row t (solver thread t < 64), the 8-column pieces of its chunk's diagonal block;
-    # the rest of the tile is zeroed once per CTA when there are several chunks
+    # T' / T'': solver thread tid writes row tid % 64, 8-column groups (tid // 64) + 2k of its
+    # chunk's diagonal block; the rest of the tile is zeroed once per CTA when there are
+    # several chunks
     diag = []
-    for t in range(NR):
+    for tid in range(NSOLVE):
+        t = tid & 63
         ci = t // C
-        for g in range(C // 8):
+        for g in range(tid >> 6, C // 8, 2):
             diag.append(kmajor_offset(t, ci * C + 8 * g, NR))
     offdiag = [kmajor_offset(r, c, NR) for r in range(NR) for c in range(0, NR, 8)
                if r // C != c // C]
@@ -145,8 +148,9 @@ def test_intra_writes_cover_each_piece_once(C):
         pieces_once(U[ci], KD * C * 4, f"U image, chunk {ci}")
         pieces_once(W[ci], C * KD * 2, f"W tile, chunk {ci}")
         pieces_once(P[ci], C * C * 2, f"P tile, chunk {ci}")
-    # q / k tiles -> workspace: the last 64 threads, each chunk's contiguous slice
-    nthr = THREADS - NR - 128
+    # q / k tiles -> workspace: threads NSOLVE .. 255 after the V tile, each chunk's contiguous
+    # slice
+    nthr = THREADS - NSOLVE
     for ci in range(CPC):
         slice_pieces = C * KD * 2 // 16
         got = [16 * i for u in range(nthr) for i in range(u, slice_pieces, nthr)]

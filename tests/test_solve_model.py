@@ -1,115 +1,166 @@
 """A CPU model of the intra kernel's triangular solve (csrc/gdn_prefill_tc.cu; a CTA holds 64
-token rows, 64 / C chunks, solved by 64 threads): the same per-thread index arithmetic over the
-fp32 A / T rows of stride C + 4 (four padding floats per row), every shared-memory access checked for bounds, 16-byte alignment of the vector accesses
-and reads of initialised data only, with the kernel's barriers at the same points. The result
-T must equal (I + A)^-1 per chunk. The model is host logic only; the GPU parity tests check the
-kernel itself against the oracle."""
+token rows, 64 / C chunks, solved by 128 threads): the same per-thread index arithmetic over the
+fp32 A / T rows of stride C + 4 (four padding floats per row), every shared-memory access checked
+for bounds, 16-byte alignment of the vector accesses and reads of initialised data only, with the
+kernel's barriers at the same points (each phase reads everything first, then writes, as the
+barrier between them allows). The solve is a blocked recursive inverse: 8 x 8 diagonal blocks by
+forward substitution, then blocks of 16, 32 and 64 rows (as far as the chunk goes) from two
+halves, T21 = -T22 (A21 T11). The result T must equal (I + A)^-1 per chunk; a planted index
+mistake fails. The model is host logic only; the GPU parity tests check the kernel itself against
+the oracle."""
 import numpy as np
 import pytest
 
 NROW = 64        # token rows per intra CTA
-NSOLVE = 64      # solver threads (warps 0-1)
+NSOLVE = 128     # solver threads (warps 0-3)
 
 
-def run_model(C, seed=0):
+def merge_threads(b):
+    """(active threads, rows per thread) of the merge that builds blocks of 2b rows."""
+    rb = 2 if b == 32 else 1
+    return (NROW // (2 * b)) * b * b // (4 * rb), rb
+
+
+def run_model(C, seed=0, mutant=None):
     SA = C + 4
     sA = np.full(NROW * SA, np.nan, dtype=np.float64)   # NaN = never written
+
     def rd(i):
-        assert 0 <= i < NROW * SA, ("read oob", i); v = sA[i]; assert not np.isnan(v), ("read unwritten", i); return v
+        assert 0 <= i < NROW * SA, ("read oob", i)
+        v = sA[i]
+        assert not np.isnan(v), ("read unwritten", i)
+        return v
+
     def wr(i, v):
-        assert 0 <= i < NROW * SA, ("write oob", i); sA[i] = v
+        assert 0 <= i < NROW * SA, ("write oob", i)
+        sA[i] = v
+
     def rd4(i):
-        assert i % 4 == 0, ("float4 misaligned", i); return [rd(i + k) for k in range(4)]
+        assert i % 4 == 0, ("float4 misaligned", i)
+        return np.array([rd(i + k) for k in range(4)])
+
+    def wr4(i, v):
+        assert i % 4 == 0, ("float4 misaligned", i)
+        for k in range(4):
+            wr(i + k, v[k])
+
     rng = np.random.default_rng(seed)
     CPC = NROW // C
     A = np.zeros((CPC, C, C))
     for ci in range(CPC):
-        M = rng.standard_normal((C, C)) * 0.3
-        A[ci] = np.tril(M, -1)
-    # A/P phase: thread (row t, half) writes its NH columns as float4 (row-contiguous)
+        A[ci] = np.tril(rng.standard_normal((C, C)) * 0.3, -1)
+    # A/P phase: thread (row t, half) writes its C / 2 columns as float4 (row-contiguous)
     NH = C // 2
     for t in range(NROW):
         ci, tl = divmod(t, C)
         for half in range(2):
             for k in range(NH // 4):
                 j0 = half * NH + 4 * k
-                for e in range(4):
-                    wr(t * SA + j0 + e, A[ci][tl][j0 + e])
-        for k in range(4):
-            wr(t * SA + C + k, 0.5)   # padding (scale, beta, iq, ik), not read by the solve
-    # step 1: diagonal blocks of B1 rows, thread = (block, column c)
-    B1 = min(C, 32)
-    X1 = {}
+                wr4(t * SA + j0, A[ci][tl][j0:j0 + 4])
+        wr4(t * SA + C, [0.5] * 4)   # padding (scale, beta, iq, ik), not read by the solve
+
+    # level 0: 8 x 8 diagonal blocks, thread = (block, column c): threads 0..63
+    writes = []
     for tid in range(NSOLVE):
-        row0 = (tid // B1) * B1; c = tid % B1; o = row0 % C
-        base = row0 * SA + o
-        x = [0.0] * B1
-        for r in range(B1):
+        if tid >= 64:
+            continue
+        R0 = 8 * (tid >> 3)
+        c = tid & 7
+        o = R0 % C
+        x = [0.0] * 8
+        for r in range(8):
+            a = np.concatenate([rd4((R0 + r) * SA + o), rd4((R0 + r) * SA + o + 4)])
             s0 = s1 = 0.0
-            for l4 in range(0, r, 4):
-                a4 = rd4(base + r * SA + l4)
-                s0 += a4[0] * x[l4]
-                if l4 + 1 < r: s1 += a4[1] * x[l4 + 1]
-                if l4 + 2 < r: s0 += a4[2] * x[l4 + 2]
-                if l4 + 3 < r: s1 += a4[3] * x[l4 + 3]
+            for l in range(0, r, 2):
+                s0 += a[l] * x[l]
+                if l + 1 < r:
+                    s1 += a[l + 1] * x[l + 1]
             x[r] = 0.0 if r < c else (1.0 if r == c else -(s0 + s1))
-        X1[tid] = (base, c, x)
-    for tid, (base, c, x) in X1.items():      # after the barrier: in place
-        for r in range(B1):
-            wr(base + r * SA + c, x[r])
-    if C == 64:
-        # step 2a: X = A21 T11, 64 threads, 4x4 outputs per thread
-        res = {}
-        for tid in range(NSOLVE):
-            k = tid
-            r0 = 4 * (k >> 3); c0 = 4 * (k & 7)
-            cb = 0
-            acc = np.zeros((4, 4))
-            for l in range(0, 32, 4):
-                a = [rd4(cb + (32 + r0 + i) * SA + l) for i in range(4)]
-                tt = [rd4(cb + (l + kk) * SA + c0) for kk in range(4)]
-                for i in range(4):
+        for r in range(8):
+            writes.append(((R0 + r) * SA + o + c, x[r]))
+    for i, v in writes:                        # after the barrier: in place
+        wr(i, v)
+
+    # merges: blocks of 2b rows from two b-row halves
+    b = 8
+    while 2 * b <= C:
+        nt, rb = merge_threads(b)
+        per_merge = b * b // (4 * rb)
+        cols = b // 4
+        # X = A21 T11 (T11 is lower triangular: column block j0 needs l >= j0)
+        res = []
+        for tid in range(nt):
+            m, idx = divmod(tid, per_merge)
+            R0 = 2 * b * m
+            o = R0 % C
+            j0 = 4 * (idx % cols)
+            i0 = rb * (idx // cols)
+            if mutant == "X from l = 0 of the next half":
+                j0_l = j0 + 4 if j0 + 4 < b else j0
+            else:
+                j0_l = j0
+            acc = np.zeros((rb, 4))
+            for l in range(j0_l, b, 4):
+                av = [rd4((R0 + b + i0 + i) * SA + o + l) for i in range(rb)]
+                tv = [rd4((R0 + l + kk) * SA + o + j0) for kk in range(4)]
+                for i in range(rb):
                     for kk in range(4):
-                        for jj in range(4):
-                            acc[i][jj] += a[i][kk] * tt[kk][jj]
-            res[tid] = (cb, r0, c0, acc)
-        for tid, (cb, r0, c0, acc) in res.items():   # after the barrier: X over A21
-            for i in range(4):
-                for jj in range(4):
-                    wr(cb + (32 + r0 + i) * SA + c0 + jj, acc[i][jj])
-        # step 2b: T21 = -(T22 X), l < r0 + 4 (T22 rows r0..r0+3 are zero beyond)
-        res = {}
-        for tid in range(NSOLVE):
-            k = tid
-            r0 = 4 * (k >> 3); c0 = 4 * (k & 7)
-            cb = 0
-            acc = np.zeros((4, 4))
-            for l in range(0, r0 + 4, 4):
-                a = [rd4(cb + (32 + r0 + i) * SA + 32 + l) for i in range(4)]
-                xx = [rd4(cb + (32 + l + kk) * SA + c0) for kk in range(4)]
-                for i in range(4):
+                        acc[i] += av[i][kk] * tv[kk]
+            res.append((R0, o, i0, j0, acc))
+        for R0, o, i0, j0, acc in res:         # after the barrier: X over A21
+            for i in range(rb):
+                wr4((R0 + b + i0 + i) * SA + o + j0, acc[i])
+        # T21 = -(T22 X) (T22 is lower triangular: rows i0 .. i0 + rb - 1 need l < i0 + rb)
+        res = []
+        for tid in range(nt):
+            m, idx = divmod(tid, per_merge)
+            R0 = 2 * b * m
+            o = R0 % C
+            j0 = 4 * (idx % cols)
+            i0 = rb * (idx // cols)
+            acc = np.zeros((rb, 4))
+            for l in range(0, i0 + rb, 4):
+                av = [rd4((R0 + b + i0 + i) * SA + o + b + l) for i in range(rb)]
+                xv = [rd4((R0 + b + l + kk) * SA + o + j0) for kk in range(4)]
+                for i in range(rb):
                     for kk in range(4):
-                        for jj in range(4):
-                            acc[i][jj] += a[i][kk] * xx[kk][jj]
-            res[tid] = (cb, r0, c0, -acc)
-        for tid, (cb, r0, c0, acc) in res.items():
-            for i in range(4):
-                for jj in range(4):
-                    wr(cb + (32 + r0 + i) * SA + c0 + jj, acc[i][jj])
-    # step 3 reads rows: T[t][8g .. 8g+7]
+                        acc[i] += av[i][kk] * xv[kk]
+            res.append((R0, o, i0, j0, -acc))
+        for R0, o, i0, j0, acc in res:         # after the barrier: T21 over X
+            for i in range(rb):
+                wr4((R0 + b + i0 + i) * SA + o + j0, acc[i])
+        b *= 2
+
+    # the T' / T'' step reads rows: T[t][8g .. 8g+7], thread t % 64, groups (t >> 6) + 2k
+    for tid in range(NSOLVE):
+        t = tid & 63
+        for g in range(tid >> 6, C // 8, 2):
+            rd4(t * SA + 8 * g)
+            rd4(t * SA + 8 * g + 4)
     ok = True
     for ci in range(CPC):
         T = np.zeros((C, C))
         for r in range(C):
             for g in range(C // 8):
-                v = rd4(ci * C * SA + r * SA + 8 * g) + rd4(ci * C * SA + r * SA + 8 * g + 4)
-                T[r, 8 * g:8 * g + 8] = v
+                T[r, 8 * g:8 * g + 8] = np.concatenate(
+                    [rd4((ci * C + r) * SA + 8 * g), rd4((ci * C + r) * SA + 8 * g + 4)])
         ref = np.linalg.inv(np.eye(C) + A[ci])
-        err = np.abs(T - ref).max() / np.abs(ref).max()
-        ok &= err < 1e-12
+        ok &= np.abs(T - ref).max() / np.abs(ref).max() < 1e-12
     return ok
 
 
 @pytest.mark.parametrize("C", [64, 32, 16])
 def test_solve_model_inverse_and_accesses(C):
     assert run_model(C, seed=C)
+
+
+def test_solve_model_threads_fit():
+    for b in (8, 16, 32):
+        nt, rb = merge_threads(b)
+        assert nt <= NSOLVE and nt % 32 == 0
+        assert nt * 4 * rb == (NROW // (2 * b)) * b * b   # every output exactly once
+
+
+def test_solve_model_catches_a_planted_mistake():
+    """Skipping the first column block of T11 in X = A21 T11 gives a wrong T."""
+    assert not run_model(64, seed=1, mutant="X from l = 0 of the next half")
