@@ -303,8 +303,12 @@ __global__ void __launch_bounds__(kThreadsTc, 2)
   constexpr int SA = S::kSA;
   float* s_G = reinterpret_cast<float*>(sm + S::oG);
   float* s_part = reinterpret_cast<float*>(sm + S::oPart);
+  // after phase 1 the partial norms are consumed: the head loop keeps each token's beta and
+  // beta e^G ik there, 16-byte rows for the T' / T'' scaling
+  float* s_beta = s_part;
+  float* s_bsc = s_part + NR;
   // per-token values in A's row padding
-  constexpr int kSc = 0, kBeta = 1, kIq = 2, kIk = 3;
+  constexpr int kBeta = 1, kIq = 2, kIk = 3;
   auto pad = [&](int t, int k) -> float& { return sA[t * SA + C + k]; };
   int* s_t0 = reinterpret_cast<int*>(sm + S::oT0);
   int* s_L = s_t0 + CPC;
@@ -388,21 +392,27 @@ __global__ void __launch_bounds__(kThreadsTc, 2)
   const int R = a.Hv / a.Hk;
   for (int hr = 0; hr < R && !bad; ++hr) {
     const int h = kh * R + hr;
-    // gates of the 64 token rows, then the running sums per chunk
+    // gates of the 64 token rows (warps 0 and 1, a row per thread), then the running sums per
+    // chunk: an inclusive scan over the lanes of a chunk (C <= 32: inside a warp; C = 64: each
+    // warp, then the second adds the first's total)
     if (tid < NR) {
       const int ci = tid / C, tl = tid % C;
       float g = 0.0f, be = 0.0f;
       if (tl < s_L[ci])
         gate_log(a.a, a.b, a.gate_mode, a.A_log, a.dt_bias,
                  static_cast<int64_t>(s_t0[ci] + tl) * a.Hv + h, h, g, be);
-      s_G[tid] = g;
       pad(tid, kBeta) = be;
+      s_beta[tid] = be;
+      constexpr int kSeg = C < 32 ? C : 32;
+#pragma unroll
+      for (int d = 1; d < kSeg; d <<= 1) {
+        const float n = __shfl_up_sync(0xffffffffu, g, d);
+        if ((lane & (kSeg - 1)) >= d) g += n;
+      }
+      s_G[tid] = g;
     }
     __syncthreads();
-    if (tid < CPC) {
-      float run = 0.0f;
-      for (int t = 0; t < C; ++t) { run += s_G[tid * C + t]; s_G[tid * C + t] = run; }
-    }
+    if (C == 64 && tid >= 32 && tid < 64) s_G[tid] += s_G[31];  // read by all after the barrier below
     if (hr == 0) {  // the G | QK product (issued once)
       if (!mbar_wait_bounded(bar, phase)) bad = true;
       bad = __any_sync(0xffffffffu, bad);
@@ -453,7 +463,7 @@ __global__ void __launch_bounds__(kThreadsTc, 2)
         for (int e = 0; e < NH; ++e) {
           const int j = half * NH + e;
           const int tj = ci * C + j;
-          const float dec = (live && j < tl) ? expf(Gt - s_G[tj]) : 0.0f;
+          const float dec = (live && j < tl) ? __expf(Gt - s_G[tj]) : 0.0f;
           av[e] = (j < tl) ? bt * dec * ikt * pad(tj, kIk) * xv[e] : 0.0f;
         }
 #pragma unroll
@@ -461,7 +471,7 @@ __global__ void __launch_bounds__(kThreadsTc, 2)
           *reinterpret_cast<float4*>(sA + t * SA + half * NH + e) =
               make_float4(av[e], av[e + 1], av[e + 2], av[e + 3]);
         // the token's W scale e^{G_t} ik_t (the solve reads columns 0 .. C-1 only)
-        if (half == 0) pad(t, kSc) = live ? expf(Gt) * ikt : 0.0f;
+        if (half == 0) s_bsc[t] = bt * (live ? expf(Gt) * ikt : 0.0f);
       } else if (c < nchunks) {
         const float iqt = pad(t, kIq) * a.scale;
         float pv[NH];
@@ -469,7 +479,7 @@ __global__ void __launch_bounds__(kThreadsTc, 2)
         for (int e = 0; e < NH; ++e) {
           const int j = half * NH + e;
           const int tj = ci * C + j;
-          const float dec = (live && j <= tl) ? expf(Gt - s_G[tj]) : 0.0f;
+          const float dec = (live && j <= tl) ? __expf(Gt - s_G[tj]) : 0.0f;
           pv[e] = dec * iqt * pad(tj, kIk) * xv[e];
         }
         unsigned char* ph = wb.Pt + (static_cast<size_t>(c) * a.Hv + h) * 2 * wb.p_tile;
@@ -548,12 +558,17 @@ __global__ void __launch_bounds__(kThreadsTc, 2)
           const float4 u1 = *reinterpret_cast<const float4*>(Tr + 8 * g + 4);
           const float tv[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
           const int jb = ci * C + 8 * g;
+          const float4 b0 = *reinterpret_cast<const float4*>(s_beta + jb);
+          const float4 b1 = *reinterpret_cast<const float4*>(s_beta + jb + 4);
+          const float4 c0 = *reinterpret_cast<const float4*>(s_bsc + jb);
+          const float4 c1 = *reinterpret_cast<const float4*>(s_bsc + jb + 4);
+          const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+          const float cv[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
           float x1[8], x2[8];
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
-            const float be = pad(jb + e, kBeta);
-            x1[e] = tv[e] * be;
-            x2[e] = tv[e] * (be * pad(jb + e, kSc));
+            x1[e] = tv[e] * bv[e];
+            x2[e] = tv[e] * cv[e];
           }
           uint4 hi, lo;
           const uint32_t o = tc::kmajor_offset(t, jb, NR);
