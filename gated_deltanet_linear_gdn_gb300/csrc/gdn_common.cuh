@@ -293,6 +293,20 @@ __device__ __forceinline__ void gate_from_raw(const GateRaw& r, int gate_mode, f
   }
 }
 
+// log-space variant used by the chunked prefill (it needs g itself), from loaded inputs.
+__device__ __forceinline__ void gate_log_raw(const GateRaw& r, int gate_mode, float& g,
+                                             float& beta) {
+  if (gate_mode == GDN_GATE_DIRECT) {
+    g = r.a;
+    beta = r.b;
+  } else {
+    const float x = __fadd_rn(r.a, r.dt_bias);
+    const float sp = x > 20.0f ? x : log1pf(expf(x));
+    g = __fmul_rn(-expf(r.A_log), sp);
+    beta = __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-r.b)));
+  }
+}
+
 // log-space variant used by the chunked prefill (it needs g itself).
 __device__ __forceinline__ void gate_log(const void* a, const void* b, int gate_mode,
                                          const float* A_log, const float* dt_bias, int64_t idx,

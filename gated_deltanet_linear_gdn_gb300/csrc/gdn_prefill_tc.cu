@@ -332,6 +332,15 @@ __global__ void __launch_bounds__(kThreadsTc, 2)
     s_L[tid] = L;
   }
   __syncthreads();
+  // the first value head's gate inputs of this thread's token row, loaded before phase 1 so
+  // that their latency overlaps it
+  GateRaw gr0{};
+  if (tid < NR) {
+    const int ci = tid / C, tl = tid % C, h0 = kh * (a.Hv / a.Hk);
+    if (tl < s_L[ci])
+      gr0 = gate_load(a.a, a.b, a.gate_mode, a.A_log, a.dt_bias,
+                      static_cast<int64_t>(s_t0[ci] + tl) * a.Hv + h0, h0);
+  }
 
   // ---- phase 1: raw q, k rows -> tensor-core tiles; norms. Thread: token row tok, q or k,
   // half of the 128 channels ----
@@ -398,9 +407,13 @@ __global__ void __launch_bounds__(kThreadsTc, 2)
     if (tid < NR) {
       const int ci = tid / C, tl = tid % C;
       float g = 0.0f, be = 0.0f;
-      if (tl < s_L[ci])
-        gate_log(a.a, a.b, a.gate_mode, a.A_log, a.dt_bias,
-                 static_cast<int64_t>(s_t0[ci] + tl) * a.Hv + h, h, g, be);
+      if (tl < s_L[ci]) {
+        if (hr == 0)
+          gate_log_raw(gr0, a.gate_mode, g, be);
+        else
+          gate_log(a.a, a.b, a.gate_mode, a.A_log, a.dt_bias,
+                   static_cast<int64_t>(s_t0[ci] + tl) * a.Hv + h, h, g, be);
+      }
       pad(tid, kBeta) = be;
       s_beta[tid] = be;
       constexpr int kSeg = C < 32 ? C : 32;
@@ -725,8 +738,8 @@ __global__ void __launch_bounds__(kPassThreads, 1)
   using S = PassSmem<C>;
   extern __shared__ __align__(1024) unsigned char sm[];
   __shared__ uint32_t s_tmem;
-  // fullA, fullB, mma1, mma2, fullU, oDone, dead, upd
-  __shared__ __align__(8) uint64_t s_bar[8];
+  // fullA, fullB, mma1, mma2, fullU, oDone, dead, upd, scaled
+  __shared__ __align__(8) uint64_t s_bar[9];
 
   // CTAs in launch order take the sequences longest first, all value heads of one together
   const int i = seq_order[blockIdx.x / a.Hv], h = blockIdx.x % a.Hv;
@@ -768,6 +781,9 @@ __global__ void __launch_bounds__(kPassThreads, 1)
   // state chain waits for), mma2 once O2^T = D^T P^T is done too (the output, and the reuse of
   // the P, k and U buffers, wait for that)
   const uint32_t upd = smem_addr(&s_bar[7]);
+  // scaled: every compute warp has replaced its O1 columns by f_t O1 (one arrival per warp),
+  // on which the O2 products then accumulate
+  const uint32_t scaled = smem_addr(&s_bar[8]);
   const int test_fault = g_test_fault;
   const size_t wtile = wb.w_tile, ptile = wb.p_tile;
 
@@ -805,6 +821,7 @@ __global__ void __launch_bounds__(kPassThreads, 1)
     for (int k = 0; k < 5; ++k) mbar_init(smem_addr(&s_bar[k]), 1);
     mbar_init(dead, 1);
     mbar_init(upd, 1);
+    mbar_init(scaled, kThreadsTc / 32);
     mbar_init(oDone, kThreadsTc / 32 + 1);
     fence_mbar_init();
     if (nch > 0) { issue_A(0); issue_B(0); issue_U(0); }
@@ -1014,13 +1031,21 @@ __global__ void __launch_bounds__(kPassThreads, 1)
           for (int ks = 0; ks < KS; ++ks)
             tc::mma_bf16_ts(tb + other, aEl + 8 * ks, dKtile + 256 * ks, id128m, 1);
           tc::mma_commit(upd);
+          // O = f_t O1 + O2: the O2 products accumulate onto the O1 columns once every compute
+          // warp has scaled them (committed whatever happened, so that what was issued can be
+          // waited for)
+          if (mbar_wait_bounded(scaled, par)) {
+            tc::fence_after_sync();
+            const uint32_t tO = tb + base + C;
 #pragma unroll
-          for (int ks = 0; ks < KS; ++ks)
-            tc::mma_bf16_ts(tb + base, aDh + 8 * ks, dPh + 16 * ks, idC, ks > 0);
+            for (int ks = 0; ks < KS; ++ks) tc::mma_bf16_ts(tO, aDh + 8 * ks, dPh + 16 * ks, idC, 1);
 #pragma unroll
-          for (int ks = 0; ks < KS; ++ks) tc::mma_bf16_ts(tb + base, aDh + 8 * ks, dPl + 16 * ks, idC, 1);
+            for (int ks = 0; ks < KS; ++ks) tc::mma_bf16_ts(tO, aDh + 8 * ks, dPl + 16 * ks, idC, 1);
 #pragma unroll
-          for (int ks = 0; ks < KS; ++ks) tc::mma_bf16_ts(tb + base, aDl + 8 * ks, dPh + 16 * ks, idC, 1);
+            for (int ks = 0; ks < KS; ++ks) tc::mma_bf16_ts(tO, aDl + 8 * ks, dPh + 16 * ks, idC, 1);
+          } else {
+            mine = true;
+          }
           tc::mma_commit(mma2);
           n2 = it + 1;
         } else {
@@ -1028,6 +1053,45 @@ __global__ void __launch_bounds__(kPassThreads, 1)
         }
       }
     } else {  // compute warps
+      {
+        // f_t O1 in place over this thread's O1 columns, while the state update runs; the O2
+        // products then accumulate onto it. (No wait failed before the barrier, or the loop
+        // would have ended.)
+        float o1[NH];
+        if constexpr (NH >= 16) {
+#pragma unroll
+          for (int b0 = 0; b0 < NH; b0 += 16) {
+            float tv[16];
+            tmem_load<16>(tc::taddr(tb, 32 * q, base + C + half * NH + b0), tv);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) o1[b0 + e] = tv[e];
+          }
+        } else {
+          float tv[8];
+          tmem_load<8>(tc::taddr(tb, 32 * q, base + C + half * NH), tv);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) o1[e] = tv[e];
+        }
+        tc::tmem_wait_ld();
+        if constexpr (NH >= 16) {
+#pragma unroll
+          for (int b0 = 0; b0 < NH; b0 += 16) {
+            float tv[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) tv[e] = vec[half * NH + b0 + e] * o1[b0 + e];
+            tc::tmem_st16(tc::taddr(tb, 32 * q, base + C + half * NH + b0), tv);
+          }
+        } else {
+          float tv[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) tv[e] = vec[half * NH + e] * o1[e];
+          tc::tmem_st8(tc::taddr(tb, 32 * q, base + C + half * NH), tv);
+        }
+        tc::tmem_wait_st();
+        tc::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(scaled);
+      }
       const bool test_fail = test_fault == 2 && blockIdx.x == 0 && warp == 0 && it == 0;
       if (test_fail ? !mbar_wait_bounded(dead, 0, kTestWaitNs) : !mbar_wait_bounded(upd, par))
         mine = true;
@@ -1059,28 +1123,27 @@ __global__ void __launch_bounds__(kPassThreads, 1)
         if (!mine) n1 = it + 2;
       }
     } else {
-      // chunk it's output O = f_t O1 + O2, while group 1 of chunk it + 1 runs
-      // (O2 is there once the whole of group 2 is done; a failed wait skips the output)
+      // chunk it's output O = f_t O1 + O2 (formed by group 2 in the O1 columns), while group 1
+      // of chunk it + 1 runs (O is there once the whole of group 2 is done; a failed wait
+      // skips the output)
       if (!mbar_wait_bounded(mma2, par)) mine = true;
       mine = __any_sync(0xffffffffu, mine);  // warp-uniform before the aligned loads
       tc::fence_after_sync();
       if (!mine) {
-        float o1[NH], o2[NH];
+        float ov[NH];
         if constexpr (NH >= 16) {
 #pragma unroll
           for (int b0 = 0; b0 < NH; b0 += 16) {
-            float ta[16], tbv[16];
+            float ta[16];
             tmem_load<16>(tc::taddr(tb, 32 * q, base + C + half * NH + b0), ta);
-            tmem_load<16>(tc::taddr(tb, 32 * q, base + half * NH + b0), tbv);
 #pragma unroll
-            for (int e = 0; e < 16; ++e) { o1[b0 + e] = ta[e]; o2[b0 + e] = tbv[e]; }
+            for (int e = 0; e < 16; ++e) ov[b0 + e] = ta[e];
           }
         } else {
-          float ta[8], tbv[8];
+          float ta[8];
           tmem_load<8>(tc::taddr(tb, 32 * q, base + C + half * NH), ta);
-          tmem_load<8>(tc::taddr(tb, 32 * q, base + half * NH), tbv);
 #pragma unroll
-          for (int e = 0; e < 8; ++e) { o1[e] = ta[e]; o2[e] = tbv[e]; }
+          for (int e = 0; e < 8; ++e) ov[e] = ta[e];
         }
         tc::tmem_wait_ld();
         if (a.out_f32) {
@@ -1088,8 +1151,7 @@ __global__ void __launch_bounds__(kPassThreads, 1)
           for (int e = 0; e < NH; ++e) {
             const int tt = half * NH + e;
             if (tt < L)
-              static_cast<float*>(a.out)[(static_cast<int64_t>(t0 + tt) * a.Hv + h) * kD + r] =
-                  fmaf(vec[tt], o1[e], o2[e]);
+              static_cast<float*>(a.out)[(static_cast<int64_t>(t0 + tt) * a.Hv + h) * kD + r] = ov[e];
           }
         } else {
           // stage the warp's [NH tokens x 32 dv] block in the bf16 tile, then copy it out in
@@ -1099,7 +1161,7 @@ __global__ void __launch_bounds__(kPassThreads, 1)
 #pragma unroll
           for (int e = 0; e < NH; ++e) {
             const int tt = half * NH + e;
-            *reinterpret_cast<uint16_t*>(ot + out_tile_offset(tt, r)) = f2bf(fmaf(vec[tt], o1[e], o2[e]));
+            *reinterpret_cast<uint16_t*>(ot + out_tile_offset(tt, r)) = f2bf(ov[e]);
           }
           __syncwarp();
 #pragma unroll

@@ -27,7 +27,7 @@ import random
 import pytest
 
 import test_pass_protocol_model as base
-from test_pass_protocol_model import (N_COMPUTE, g1_reads, g1_writes, o2_reads, o2_writes, par,
+from test_pass_protocol_model import (N_COMPUTE, g1_reads, g1_writes, o2_reads, o2_rmw, par,
                                       u_bufs, upd_reads, upd_writes, xp)
 
 
@@ -160,7 +160,11 @@ def mma_warp(s, me):
             break
         if (yield from s.bounded("fullB", it, me)):
             s.mma(f"upd({it})", upd_reads(it), upd_writes(s, it), "upd", it)
-            s.mma(f"mma2({it})", o2_reads(it), o2_writes(s, it), "mma2", it)
+            if (yield from s.bounded("scaled", it, me)):
+                s.mma(f"mma2({it})", o2_reads(it), [], "mma2", it, o2_rmw(s, it))
+            else:
+                mine = True
+                s.mma(f"commit mma2({it})", [], [], "mma2", it)
             n2 = it + 1
         else:
             mine = True
@@ -200,11 +204,15 @@ def compute_warp(s, w, me):
         yield from s.or_sync("named", N_COMPUTE + 1, mine, bad)            # B1
         if bad[0]:
             break
+        s.read(("Xo", x, w), ("O1", it), tag)       # f_t O1 in place (no wait failed before B1)
+        yield lambda: True
+        s.write(("Xo", x, w), ("fO1", it))
+        s.bars["scaled"].arrive(it)
         if not (yield from s.bounded("upd", it, me)):
             mine = True
         if not mine:
             s.read(("Xd", 1 - x), ("dS", it), tag)
-            s.read(("Xo", 1 - x), ("dS", it), tag)
+            s.read(("Xo", 1 - x, w), ("dS", it), tag)
             s.read(("vec", par(it)), it, tag)
             s.write(("S", w), it + 1)
         yield from s.or_sync("named", N_COMPUTE + 1, mine, bad)            # B2
@@ -213,12 +221,10 @@ def compute_warp(s, w, me):
         if not (yield from s.bounded("mma2", it, me)):
             mine = True                  # the output is skipped; reported at the next barrier
         if not mine:
-            s.read_begin(("Xo", x), ("O1", it), tag)
-            s.read_begin(("Xd", x), ("O2", it), tag)
+            s.read_begin(("Xo", x, w), ("O", it), tag)
             s.read_begin(("vec", par(it)), it, tag)
             yield lambda: True
-            s.read_end(("Xo", x), ("O1", it), tag)
-            s.read_end(("Xd", x), ("O2", it), tag)
+            s.read_end(("Xo", x, w), ("O", it), tag)
             s.read_end(("vec", par(it)), it, tag)
         s.arrive_odone(it)
     yield from s.or_sync("named", N_COMPUTE + 1, bad[0] or mine, bad)

@@ -8,8 +8,9 @@ barrier, then O2), a named barrier over the compute and MMA warps, and the CTA
 barriers. Copies and MMA groups take random times and the scheduler interleaves the warps at
 random. The buffers are shared-memory tiles (W, q, P, k, the U image, vec) and tensor-memory
 regions: the bf16 operand parts of the state and of D / D' (each warp its rows), and two
-accumulator regions that alternate by chunk parity -- a chunk's raw D^T, then its O2^T, and
-O1^T in one, its state update in the other. Over many schedules and chunk counts it checks that
+accumulator regions that alternate by chunk parity -- a chunk's raw D^T and O1^T in one (the
+compute warps scale O1^T by f_t in place, and O2^T is then added onto it, giving the output),
+its state update in the other. Over many schedules and chunk counts it checks that
 
 - no parity wait can alias: while a thread waits for phase k the barrier never completes
   phase k + 1 (else the wait would miss phase k and hang);
@@ -20,7 +21,8 @@ O1^T in one, its state update in the other. Over many schedules and chunk counts
 
 Planted mistakes (a missing wait, a buffer reused early, an early arrival, a group issued
 before its barrier, one accumulator set instead of two, the output read before the second
-part of group 2 is done) each fail some schedule, so the
+part of group 2 is done, O2 added before the compute warps have scaled O1) each fail some
+schedule, so the
 checks have teeth. The model is host logic only; the GPU tests run the kernel itself.
 """
 import random
@@ -55,6 +57,7 @@ class Sim:
         self.nch, self.rng, self.mutant = nch, rng, mutant
         self.bars = {n: Bar(n) for n in ("fullA", "fullB", "fullU", "mma1", "upd", "mma2")}
         self.bars["oDone"] = Bar("oDone", N_COMPUTE + 1)
+        self.bars["scaled"] = Bar("scaled", N_COMPUTE)
         self.events = []      # [countdown, callable]
         self.mma_queue = []   # MMA groups in issue order: (name, start_fn, finish_fn)
         self.mma_busy = None  # [countdown, finish_fn]
@@ -93,15 +96,22 @@ class Sim:
             self.bars[bar].complete()
         self.later(land)
 
-    def mma(self, name, reads, writes, bar, k):
+    def mma(self, name, reads, writes, bar, k, rmw=()):
+        """An MMA group: it reads `reads`, writes `writes`, and reads then rewrites each
+        (buffer, version in, version out) of `rmw` (an accumulator it adds onto)."""
         def start():
             for b, v in reads:
                 self.read_begin(b, v, name)
+            for b, vin, vout in rmw:
+                assert self.buf.get(b) == vin, f"{b} holds {self.buf.get(b)}, {name} adds onto {vin}"
+                self.write(b, ("mma", name))
             for b, v in writes:
                 self.write(b, ("mma", name))
         def finish():
             for b, v in reads:
                 self.read_end(b, v, name)
+            for b, vin, vout in rmw:
+                self.write(b, vout)
             for b, v in writes:
                 self.write(b, v)
             self.bars[bar].complete()
@@ -165,8 +175,9 @@ def g1_reads(k):
 
 
 def g1_writes(s, k):
+    """The raw D^T half, and the O1^T half in pieces: each compute warp's rows and columns."""
     x = xp(s, k)
-    return [(("Xd", x), ("raw", k)), (("Xo", x), ("O1", k))]
+    return [(("Xd", x), ("raw", k))] + [(("Xo", x, w), ("O1", k)) for w in range(N_COMPUTE)]
 
 
 def upd_reads(k):
@@ -177,16 +188,17 @@ def upd_reads(k):
 
 def upd_writes(s, k):
     x = xp(s, k)
-    return [(("Xd", 1 - x), ("dS", k)), (("Xo", 1 - x), ("dS", k))]
+    return [(("Xd", 1 - x), ("dS", k))] + [(("Xo", 1 - x, w), ("dS", k)) for w in range(N_COMPUTE)]
 
 
 def o2_reads(k):
-    """Group 2 of chunk k, second part: O2^T from D hi / lo and the P tiles."""
+    """Group 2 of chunk k, second part: O2^T from D hi / lo and the P tiles..."""
     return [(("D", w), k) for w in range(N_COMPUTE)] + [("P", k)]
 
 
-def o2_writes(s, k):
-    return [(("Xd", xp(s, k)), ("O2", k))]
+def o2_rmw(s, k):
+    """... added onto f_t O1^T, which the compute warps left in the O1 columns."""
+    return [(("Xo", xp(s, k), w), ("fO1", k), ("O", k)) for w in range(N_COMPUTE)]
 
 
 def copy_warp(s):
@@ -239,7 +251,9 @@ def mma_warp(s):
         yield from s.sync("named", N_COMPUTE + 1)                          # B1
         yield from s.wait("fullB", it)
         s.mma(f"upd({it})", upd_reads(it), upd_writes(s, it), "upd", it)
-        s.mma(f"mma2({it})", o2_reads(it), o2_writes(s, it), "mma2", it)
+        if s.mutant != "O2 before the scaling":
+            yield from s.wait("scaled", it)
+        s.mma(f"mma2({it})", o2_reads(it), [], "mma2", it, o2_rmw(s, it))
         if s.mutant == "group 1 before the state barrier" and it + 1 < nch:
             yield from issue1(it + 1)
         yield from s.sync("named", N_COMPUTE + 1)                          # B2
@@ -265,20 +279,22 @@ def compute_warp(s, w):
         s.write(("D", w), it)                                              # its D, D' rows
         s.write(("E", w), it)
         yield from s.sync("named", N_COMPUTE + 1)                          # B1
+        s.read(("Xo", x, w), ("O1", it), tag)                              # f_t O1 in place
+        yield lambda: True
+        s.write(("Xo", x, w), ("fO1", it))
+        s.bars["scaled"].arrive(it)
         yield from s.wait("upd", it)
         s.read(("Xd", 1 - x), ("dS", it), tag)                             # the state update
-        s.read(("Xo", 1 - x), ("dS", it), tag)
+        s.read(("Xo", 1 - x, w), ("dS", it), tag)
         s.read(("vec", par(it)), it, tag)
         s.write(("S", w), it + 1)                                          # next chunk's S rows
         yield from s.sync("named", N_COMPUTE + 1)                          # B2
         if s.mutant != "output before O2":
             yield from s.wait("mma2", it)
-        s.read_begin(("Xo", x), ("O1", it), tag)                           # under group 1
-        s.read_begin(("Xd", x), ("O2", it), tag)
+        s.read_begin(("Xo", x, w), ("O", it), tag)                         # under group 1
         s.read_begin(("vec", par(it)), it, tag)
         yield lambda: True
-        s.read_end(("Xo", x), ("O1", it), tag)
-        s.read_end(("Xd", x), ("O2", it), tag)
+        s.read_end(("Xo", x, w), ("O", it), tag)
         s.read_end(("vec", par(it)), it, tag)
         s.bars["oDone"].arrive(it)
     yield from s.sync("named", N_COMPUTE + 1)
@@ -315,7 +331,7 @@ def test_pass_protocol_over_random_schedules(nch):
 
 @pytest.mark.parametrize("mutant", ["no output barrier", "U after group 1", "arrive early",
                                     "group 1 before the state barrier", "one D/O1 set",
-                                    "output before O2"])
+                                    "output before O2", "O2 before the scaling"])
 def test_model_catches_planted_mistakes(mutant):
     """Each mistake, planted in the model, fails some schedule."""
     caught = 0
