@@ -83,7 +83,9 @@ __device__ __forceinline__ void window8(const LayerArgs& a, const PrefillExtra& 
 // (from x or, before the sequence start, the initial conv state) and then rolled in
 // registers, and the input rows come kConvBatch at a time with the next batch in flight
 // (the loads, 4 bytes each, need that depth to keep the memory system busy). The
-// per-channel arithmetic is conv_tap_sum and silu_f, as in the decode conv.
+// per-channel taps are conv_tap_sum's, as in the decode conv; the SiLU is silu_fast (the
+// kernel is bound by instruction issue, and its bf16 output feeds the prefill, whose bound is
+// far looser than the unit of bf16 it can move; the decode conv keeps the IEEE silu_f).
 constexpr int kConvRun = 32;
 constexpr int kConvBatch = 8;
 constexpr int kConvRunThreads = 256;
@@ -173,7 +175,7 @@ __global__ void __launch_bounds__(kConvRunThreads)
       if (kb + k >= n) break;
       win[kConvW - 1] = make_float2(__uint_as_float(xc[k] << 16), __uint_as_float(xc[k] & 0xFFFF0000u));
       float2 acc = conv_tap_sum2<kF32Cache>(win, w, bias);
-      if (silu) acc = make_float2(silu_f(acc.x), silu_f(acc.y));
+      if (silu) acc = make_float2(silu_fast(acc.x), silu_fast(acc.y));
 #pragma unroll
       for (int j = 0; j < kConvW - 1; ++j) win[j] = win[j + 1];
       *reinterpret_cast<uint32_t*>(yo + static_cast<int64_t>(kb + k) * a.D) = pack_bf2(acc.x, acc.y);
