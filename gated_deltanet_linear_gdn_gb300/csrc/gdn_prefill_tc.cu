@@ -37,6 +37,8 @@
 //       forms D^T P^T and the state update D'^T K; M = dv = 128 throughout.
 // Every wait is bounded (GDN_DEVERR_TIMEOUT on expiry, the CTA stops cleanly
 // and frees its tensor memory).
+#include <climits>
+
 #include "gdn_common.cuh"
 #include "gdn_internal.h"
 #include "gdn_ptx.cuh"
@@ -47,6 +49,15 @@ namespace gdn {
 namespace {
 
 constexpr int kD = 128;          // dk = dv
+
+// Programmatic dependent launch. grid_dep_launch: once every CTA of this grid has executed it
+// (or exited), the next kernel of the stream, if launched as a programmatic dependent, may
+// start. grid_dep_wait: waits until the grid this one was launched as a dependent of has
+// completed and its memory is visible.
+__device__ __forceinline__ void grid_dep_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 constexpr int kThreadsTc = 256;  // 8 warps: warp w reads tensor-memory lanes 32 (w % 4) ..
 // the pass kernel adds two warps: warp 8 (lane 0) issues the MMA groups, warp 9 (lane 0) the
 // bulk copies. The copy warp paces itself on mbarriers alone; the other nine warps meet at
@@ -63,8 +74,13 @@ __device__ int g_test_fault = 0;
 constexpr uint64_t kTestWaitNs = 10000000ull;
 constexpr int kVecFloats = 256;  // per (chunk, head): f[C], dd[C], g_last
 
+// A prefill of at most kPieceSeqHeads (sequence, value head) pairs leaves most SMs free during
+// its state pass; its chunks then run in pieces (launch_tc_c), the pass of one piece beside the
+// intra kernel of the next, and a sequence's fp32 state crosses a piece boundary in `sx`.
+constexpr int kPieceSeqHeads = 64;
+
 struct TcLayout {
-  size_t meta, seq_ok, chunk_off, chunk_seq, seq_order, ybuf, Qt, Kt, Wt, Pt, Ut, vec, total;
+  size_t meta, seq_ok, chunk_off, chunk_seq, seq_order, ybuf, Qt, Kt, Wt, Pt, Ut, vec, sx, total;
   int max_chunks;
   // per-tile byte sizes
   size_t q_tile, w_tile, p_tile, u_tile;
@@ -93,6 +109,9 @@ TcLayout tc_layout(int T, int N, int Hk, int Hv, int C, int D) {
   L.Pt = off; off = align256(off + static_cast<size_t>(mc) * Hv * 2 * L.p_tile);
   L.Ut = off; off = align256(off + static_cast<size_t>(mc) * Hv * L.u_tile);
   L.vec = off; off = align256(off + static_cast<size_t>(mc) * Hv * kVecFloats * 4);
+  L.sx = off;
+  if (static_cast<int64_t>(N) * Hv <= kPieceSeqHeads)
+    off = align256(off + static_cast<size_t>(N) * Hv * kD * kD * 4);
   L.total = off;
   return L;
 }
@@ -295,7 +314,12 @@ template <int C>
 __global__ void __launch_bounds__(kThreadsTc, 2)
     intra_tc_kernel(LayerArgs a, PrefillExtra p, const uint16_t* __restrict__ y,
                     const int32_t* meta, const int32_t* chunk_off, const int32_t* chunk_seq,
-                    TcBufs wb) {
+                    TcBufs wb, int cta0, int chain) {
+  // cta0: the first CTA of this launch (a piece of the chunks). Every CTA, its work done, lets
+  // the pass over the piece (a programmatic dependent of this grid) start its set-up. chain:
+  // launched as a programmatic dependent of the pass over the piece before; CTA 0 then waits
+  // for that pass before it exits, so that this grid -- which the pass over the piece waits
+  // for -- completes only after it (the other CTAs leave at once and free their SM)
   using S = IntraSmem<C>;
   constexpr int CPC = S::CPC, NR = S::kRows;
   extern __shared__ __align__(1024) unsigned char sm[];
@@ -318,8 +342,13 @@ __global__ void __launch_bounds__(kThreadsTc, 2)
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int kh = blockIdx.y;
   const int nchunks = meta[0];
-  const int c_first = blockIdx.x * CPC;
-  if (c_first >= nchunks) return;  // no chunk of this CTA exists
+  const int c_first = (cta0 + blockIdx.x) * CPC;
+  const bool waits = chain && blockIdx.x == 0 && blockIdx.y == 0;
+  if (c_first >= nchunks) {  // no chunk of this CTA exists
+    grid_dep_launch();
+    if (waits) grid_dep_wait();
+    return;
+  }
   if (tid < CPC) {
     const int c = c_first + tid;
     int t0 = 0, L = 0;
@@ -711,6 +740,8 @@ __global__ void __launch_bounds__(kThreadsTc, 2)
   if (bad && tid == 0 && a.err) atomicOr(a.err, GDN_DEVERR_TIMEOUT);
   tc_sync(false);
   if (warp == 0) tc::tmem_dealloc(tb, kIntraTmemCols);
+  grid_dep_launch();
+  if (waits) grid_dep_wait();
 }
 
 // ============================================================== pass kernel
@@ -734,8 +765,14 @@ struct PassSmem {
 template <int C>
 __global__ void __launch_bounds__(kPassThreads, 1)
     pass_tc_kernel(LayerArgs a, PrefillExtra p, const int32_t* seq_ok, const int32_t* chunk_off,
-                   const int32_t* seq_order, TcBufs wb) {
+                   const int32_t* seq_order, TcBufs wb, int g_lo, int g_hi, float* sx, int pdl) {
+  // [g_lo, g_hi): the chunks of this launch (a piece of the call's chunks, or all of them); a
+  // sequence's state enters from its slot at its first chunk, else from sx, and leaves to its
+  // slot after its last chunk, else to sx. pdl: launched as a programmatic dependent of the
+  // piece's intra kernel (which follows the pass over the piece before)
   using S = PassSmem<C>;
+  // the next piece's intra kernel may start once every CTA of this pass is resident
+  if (pdl) grid_dep_launch();
   extern __shared__ __align__(1024) unsigned char sm[];
   __shared__ uint32_t s_tmem;
   // fullA, fullB, mma1, mma2, fullU, oDone, dead, upd, scaled
@@ -745,7 +782,8 @@ __global__ void __launch_bounds__(kPassThreads, 1)
   const int i = seq_order[blockIdx.x / a.Hv], h = blockIdx.x % a.Hv;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int bos = p.cu_seqlens[i], eos = p.cu_seqlens[i + 1];
-  if (!seq_ok[i]) {  // inactive / invalid sequence (or bad cu_seqlens): zero outputs
+  if (!seq_ok[i]) {  // inactive / invalid sequence (or bad cu_seqlens): zero outputs, once
+    if (g_lo != 0) return;
     int64_t n = static_cast<int64_t>(max(eos - bos, 0));
     if (bos < 0 || eos > p.total_tokens) n = 0;
     for (int64_t idx = tid; idx < n * kD; idx += kPassThreads) {
@@ -755,7 +793,18 @@ __global__ void __launch_bounds__(kPassThreads, 1)
     }
     return;
   }
-  const int c0 = chunk_off[i], nch = chunk_off[i + 1] - c0;
+  const int cs = chunk_off[i], ce = chunk_off[i + 1];  // the sequence's chunks
+  int c0 = cs, c1 = ce;  // this launch's share of them: [c0, c1)
+  if (cs == ce) {        // no token: the first piece stores the initial (or zero) state
+    if (g_lo != 0) return;
+  } else {
+    c0 = max(cs, g_lo);
+    c1 = min(ce, g_hi);
+    if (c1 <= c0) return;
+  }
+  const int nch = c1 - c0;
+  const bool from_slot = c0 == cs, to_slot = c1 == ce;
+  if (pdl) grid_dep_wait();  // the piece's intra tiles, and the state the piece before left in sx
   const int32_t slot = a.slot[i];
   const bool init = (p.has_init == nullptr) || (p.has_init[i] != 0);
   const bool mma_warp = warp == kThreadsTc / 32, copy_warp = warp == kThreadsTc / 32 + 1;
@@ -830,8 +879,15 @@ __global__ void __launch_bounds__(kPassThreads, 1)
   const int64_t soff = (static_cast<int64_t>(slot) * a.Hv + h) * (kD * kD) + r * kD + half * 64;
   float* Sg = a.ssm + soff;                                          // fp32 state
   uint16_t* Sb = reinterpret_cast<uint16_t*>(a.ssm) + soff;          // bf16 state
+  float* Sx = sx ? sx + ((static_cast<int64_t>(i) * a.Hv + h) * kD + r) * kD + half * 64 : nullptr;
   float Sr[64];
-  if (compute) {
+  if (compute && !from_slot) {
+#pragma unroll
+    for (int e = 0; e < 64; e += 4) {
+      const float4 v = *reinterpret_cast<const float4*>(Sx + e);
+      Sr[e] = v.x; Sr[e + 1] = v.y; Sr[e + 2] = v.z; Sr[e + 3] = v.w;
+    }
+  } else if (compute) {
     if (a.ssm_bf16) {
 #pragma unroll
       for (int e = 0; e < 64; e += 8) {
@@ -961,7 +1017,7 @@ __global__ void __launch_bounds__(kPassThreads, 1)
 
   int n1 = (mma_warp && nch > 0 && !mine) ? 1 : 0, n2 = 0;  // MMA groups committed
   for (int it = 0; it < nch && !bad && !copy_warp; ++it) {
-    const int t0 = bos + it * C;
+    const int t0 = bos + (c0 - cs + it) * C;
     const int L = min(C, eos - t0);
     const uint32_t par = it & 1;
     const float* vec = reinterpret_cast<const float*>(sm + S::oVec + par * kVecFloats * 4);
@@ -1186,7 +1242,11 @@ __global__ void __launch_bounds__(kPassThreads, 1)
     if (n2 > 0) mbar_wait_bounded(mma2, (n2 - 1) & 1);
   }
   if (!bad) {
-    if (compute) {
+    if (compute && !to_slot) {  // the next piece takes the state from here, unrounded
+#pragma unroll
+      for (int e = 0; e < 64; e += 4)
+        *reinterpret_cast<float4*>(Sx + e) = make_float4(Sr[e], Sr[e + 1], Sr[e + 2], Sr[e + 3]);
+    } else if (compute) {
       if (a.ssm_bf16) {  // rounded to bf16 only here, at the write-back
 #pragma unroll
         for (int e = 0; e < 64; e += 8) {
@@ -1208,6 +1268,23 @@ __global__ void __launch_bounds__(kPassThreads, 1)
   if (warp == 0) tc::tmem_dealloc(tb, kTmemCols);
 }
 
+// A kernel launch, as a programmatic dependent of the stream's previous kernel when `pdl`.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k(void (*kern)(KArgs...), dim3 grid, int threads, size_t smem, cudaStream_t s,
+                     bool pdl, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(threads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 template <int C>
 cudaError_t launch_tc_c(const LayerArgs& a, const PrefillExtra& p, const TcLayout& L, char* ws,
                         const uint16_t* y, cudaStream_t s) {
@@ -1226,28 +1303,60 @@ cudaError_t launch_tc_c(const LayerArgs& a, const PrefillExtra& p, const TcLayou
   wb.q_tile = L.q_tile;
   wb.w_tile = L.w_tile;
   wb.p_tile = L.p_tile;
-  cudaError_t e;
-  if (L.max_chunks > 0) {
-    constexpr int CPC = IntraSmem<C>::CPC;
-    auto k1 = intra_tc_kernel<C>;
-    e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, IntraSmem<C>::kBytes);
-    if (e != cudaSuccess) return e;
-    // the whole carveout as shared memory, so that two CTAs fit on an SM
-    e = cudaFuncSetAttribute(k1, cudaFuncAttributePreferredSharedMemoryCarveout,
-                             cudaSharedmemCarveoutMaxShared);
-    if (e != cudaSuccess) return e;
-    k1<<<dim3((L.max_chunks + CPC - 1) / CPC, a.Hk), kThreadsTc, IntraSmem<C>::kBytes, s>>>(
-        a, p, y, meta, chunk_off, chunk_seq, wb);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-  }
+  constexpr int CPC = IntraSmem<C>::CPC;
+  const int M = L.max_chunks;  // an upper bound of the call's chunks
+  auto k1 = intra_tc_kernel<C>;
   auto k2 = pass_tc_kernel<C>;
+  cudaError_t e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       IntraSmem<C>::kBytes);
+  if (e != cudaSuccess) return e;
+  // the whole carveout as shared memory, so that two CTAs fit on an SM
+  e = cudaFuncSetAttribute(k1, cudaFuncAttributePreferredSharedMemoryCarveout,
+                           cudaSharedmemCarveoutMaxShared);
+  if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, PassSmem<C>::kBytes);
   if (e != cudaSuccess) return e;
-  if (p.before_pass && (e = cudaEventRecord(p.before_pass, s)) != cudaSuccess) return e;
-  k2<<<static_cast<unsigned>(p.num_seqs) * a.Hv, kPassThreads, PassSmem<C>::kBytes, s>>>(
-      a, p, seq_ok, chunk_off, seq_order, wb);
-  return cudaGetLastError();
+  const unsigned pass_ctas = static_cast<unsigned>(p.num_seqs) * a.Hv;
+
+  // Pieces. With few (sequence, value head) pairs the state pass holds few SMs for its whole
+  // chain, so the chunks run in pieces, in one stream: intra(0), pass(0), intra(1), pass(1), ...
+  // Each later kernel is a programmatic dependent of the one before: intra(k + 1) starts once
+  // every CTA of pass(k) is resident (a pass CTA needs an SM of its own: its shared and tensor
+  // memory exclude an intra CTA) and runs on the other SMs beside it; its CTA 0 then waits for
+  // pass(k) before it exits, so pass(k + 1), which waits for intra(k + 1), finds the state
+  // pass(k) left. The first piece is short, so that the first pass starts early, and each next
+  // one half as long again: its intra kernel, on the SMs the pass leaves, keeps ahead of the
+  // pass before it. Not for the mixed step, which puts its decode rows beside the pass.
+  int bounds[16] = {0, M}, pieces = 1;
+  if (static_cast<int64_t>(p.num_seqs) * a.Hv <= kPieceSeqHeads && !p.before_pass && M >= 16) {
+    int n = (max(4, M / 8) + CPC - 1) / CPC * CPC, g = 0;
+    pieces = 0;
+    while (g < M && pieces < 15) {
+      const int left = M - g;
+      const int take = (pieces == 14 || left < n + n / 2) ? left : n;  // a short tail joins
+      bounds[pieces] = g;
+      g += take;
+      ++pieces;
+      n = (n * 3 / 2 + CPC - 1) / CPC * CPC;
+    }
+    bounds[pieces] = M;
+  }
+  float* sx = pieces > 1 ? reinterpret_cast<float*>(ws + L.sx) : nullptr;
+  for (int k = 0; k < pieces; ++k) {
+    const int g_lo = bounds[k], g_hi = k + 1 < pieces ? bounds[k + 1] : INT_MAX;
+    const int n_chunks = bounds[k + 1] - g_lo;
+    if (n_chunks > 0) {
+      e = launch_k(k1, dim3((n_chunks + CPC - 1) / CPC, a.Hk), kThreadsTc, IntraSmem<C>::kBytes, s,
+                   k > 0, a, p, y, meta, chunk_off, chunk_seq, wb, g_lo / CPC, k > 0 ? 1 : 0);
+      if (e != cudaSuccess) return e;
+    }
+    if (pieces == 1 && p.before_pass && (e = cudaEventRecord(p.before_pass, s)) != cudaSuccess)
+      return e;
+    e = launch_k(k2, dim3(pass_ctas), kPassThreads, PassSmem<C>::kBytes, s, pieces > 1, a, p,
+                 seq_ok, chunk_off, seq_order, wb, g_lo, g_hi, sx, pieces > 1 ? 1 : 0);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 }  // namespace

@@ -196,6 +196,36 @@ def test_prefill_packing_invariance(geo, chunk, lens):
         assert torch.equal(ds.conv_state.cpu()[inv[sl]], d.conv_state.cpu()[sl])
 
 
+@pytest.mark.parametrize("chunk,state_bf16", [(64, False), (32, False), (64, True)])
+def test_prefill_pieces_bitwise(chunk, state_bf16):
+    """A long sequence alone runs its chunks in pieces (its intra kernel beside its state pass,
+    the fp32 state handed from piece to piece); packed with 44 other sequences it runs in one
+    piece. Its outputs, final state and conv window are bitwise the same either way (with a
+    bf16 state too: the state crosses piece boundaries unrounded)."""
+    geo = gi.QWEN3_NEXT
+    lens = [4096, 37, 150, 9, 200] + [5] * 40
+    inp = gi.make_inputs(geo, lens, 64, seed=12, state_bf16=state_bf16)
+    d = Device(inp)
+    full = gpu_prefill(d, chunk=chunk, out_f32=False)
+    torch.cuda.synchronize()
+    assert int(d.err.item()) == 0
+    full_bits = torch_to_bits(full)
+    sub = gi.LayerInputs(**{**inp.__dict__})
+    n0 = lens[0]
+    sub.mixed, sub.a, sub.b = inp.mixed[:n0], inp.a[:n0], inp.b[:n0]
+    sub.slot = inp.slot[:1].copy()
+    sub.cu_seqlens = np.array([0, n0], np.int32)
+    sub.has_init = None if inp.has_init is None else inp.has_init[:1].copy()
+    ds = Device(sub)
+    o = gpu_prefill(ds, chunk=chunk, out_f32=False)
+    torch.cuda.synchronize()
+    assert int(ds.err.item()) == 0
+    assert np.array_equal(torch_to_bits(o), full_bits[:n0])
+    s0 = int(inp.slot[0])
+    assert torch.equal(ds.ssm.cpu()[s0], d.ssm.cpu()[s0])
+    assert torch.equal(ds.conv_state.cpu()[s0], d.conv_state.cpu()[s0])
+
+
 def test_prefill_then_decode_continues_the_state():
     """A prefill followed by decode steps equals the oracle run over the whole stream."""
     import oracle
