@@ -117,6 +117,23 @@ def ncu_traffic(state="f32", batch=None, num_slots=None):
     return e
 
 
+def prefill_launches(T, N, Hv, C, conv):
+    """Kernels one tensor-core prefill call launches: prep (+ the conv and its final-window
+    kernel), then an intra and a pass kernel per piece of the chunks. The piece rule is the
+    library's (a call with at most 64 (sequence, value head) pairs and at least 16 chunks runs
+    in pieces that grow by half, the first max(4, chunks / 8) long), restated here to count."""
+    M = (T + N * (C - 1)) // C
+    pieces = 1
+    if N * Hv <= 64 and M >= 16:
+        n, g, pieces = max(4, M // 8), 0, 0
+        while g < M and pieces < 15:
+            left = M - g
+            g += left if (pieces == 14 or left < n + n // 2) else n
+            pieces += 1
+            n = n * 3 // 2
+    return 1 + (2 if conv else 0) + 2 * pieces
+
+
 def aggregate_ranks(mean_ms: float, bytes_per_rank: int, world: int, device=None):
     """Whole-job throughput over `world` ranks, each running its own copy of the workload:
     the step time is the max over ranks, the bytes are the sum. Returns (max_ms, GB/s).
@@ -324,13 +341,14 @@ def run_ours(args, rank, world):
                                         tt["slot"], tt["hi"], tt["out"], ws, dims, chunk=64,
                                         stream=stream)
             ms = central(timed(pcall, 5, 2))
+            launches = prefill_launches(T, N, geo.Hv, 64, inp.conv_w is not None)
             fl = prefill_flops_per_token(geo) * T
             tpk, tkind = load_bf16_peak()
             prefill[name] = {"tokens": T, "seqs": N, "ms": round(ms, 3),
                              "tokens_per_s": round(T / ms * 1e3, 1),
                              "TFLOPs": round(fl / ms / 1e9, 2),
                              "frac_of_bf16_tensor_peak": round(fl / ms / 1e9 / tpk, 4),
-                             "peak_kind": tkind, "gpu_launches_per_call": 3 if inp.conv_w is None else 5,
+                             "peak_kind": tkind, "gpu_launches_per_call": launches,
                              "GBps": round(prefill_bytes(T, N, geo, conv=inp.conv_w is not None) / ms / 1e6, 1)}
             if name.startswith("single"):  # the same call with the output gate (+1 launch)
                 og = gdn.OutputGate(torch.randn(T, geo.Hv, geo.dv, device=dev).to(torch.bfloat16),

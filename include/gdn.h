@@ -228,6 +228,13 @@ size_t gdn_chunked_prefill_workspace_size(int32_t total_tokens, int32_t num_seqs
  *               16-byte aligned; its contents on entry do not matter
  * Other arguments as in gdn_decode_step.
  * Supported: dk == dv in {32, 64, 128}, W == 4, Hv % Hk == 0, D % 8 == 0.
+ *
+ * With dk = dv = 128 and at most 64 (sequence, value head) pairs, the call runs its chunks in
+ * pieces: several kernel launches on `stream`, the later ones programmatic dependents of the
+ * ones before, so that each piece's state pass runs beside the next piece's intra-chunk
+ * kernel. For the caller nothing changes: all of the call's work is ordered on `stream` as
+ * before, and the results are bitwise those of one piece (the state crosses piece boundaries
+ * in fp32, in the workspace).
  */
 gdn_status gdn_chunked_prefill(const void* mixed_qkv, const void* a, const void* b,
                                gdn_gate_mode gate_mode, const float* A_log,
