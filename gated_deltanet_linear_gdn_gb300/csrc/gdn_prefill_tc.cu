@@ -206,6 +206,19 @@ __device__ __forceinline__ void fma_rows(float (&acc)[RB][4], const float4 (&a)[
   }
 }
 
+// Inclusive sum of v over the lanes of a chunk of C tokens within a warp (the whole warp for
+// C >= 32; a C = 64 chunk's second warp then adds the first's total)
+template <int C>
+__device__ __forceinline__ float chunk_scan(float v, int lane) {
+  constexpr int kSeg = C < 32 ? C : 32;
+#pragma unroll
+  for (int d = 1; d < kSeg; d <<= 1) {
+    const float n = __shfl_up_sync(0xffffffffu, v, d);
+    if ((lane & (kSeg - 1)) >= d) v += n;
+  }
+  return v;
+}
+
 // barrier of the intra kernel's four solver warps (warps 0-3; named barrier 1)
 constexpr int kSolveThreads = 128;
 __device__ __forceinline__ void solver_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
@@ -302,7 +315,10 @@ struct IntraSmem {
   static constexpr int oA = oT1l + kTT;
   static constexpr int oG = oA + kRows * kSA * 4;    // cumulative log-gates G: 64 floats
   static constexpr int oPart = oG + kRows * 4;       // partial squared norms [2][2][64]
-  static constexpr int oBar = oPart + 4 * kRows * 4, oTmem = oBar + 8, oT0 = oTmem + 8;
+  // per token: k's norm factor, the second value head's running gate sums (scanned within each
+  // warp) and beta, computed during the first head's solve
+  static constexpr int oTok = oPart + 4 * kRows * 4;
+  static constexpr int oBar = oTok + 3 * kRows * 4, oTmem = oBar + 8, oT0 = oTmem + 8;
   static constexpr int kBytes = oT0 + 2 * CPC * 4;
   static_assert(oT1h - oT2h >= kTT && oT1l - oT2l >= kTT, "M = 128 reads stay in the block");
   static_assert(kBytes <= 113 * 1024, "two intra CTAs must fit on an SM");
@@ -331,6 +347,9 @@ __global__ void __launch_bounds__(kThreadsTc, 2)
   // beta e^G ik there, 16-byte rows for the T' / T'' scaling
   float* s_beta = s_part;
   float* s_bsc = s_part + NR;
+  float* s_ik = reinterpret_cast<float*>(sm + S::oTok);
+  float* s_G1 = s_ik + NR;
+  float* s_beta1 = s_ik + 2 * NR;
   // per-token values in A's row padding
   constexpr int kBeta = 1, kIq = 2, kIk = 3;
   auto pad = [&](int t, int k) -> float& { return sA[t * SA + C + k]; };
@@ -422,7 +441,9 @@ __global__ void __launch_bounds__(kThreadsTc, 2)
   if (tid < 2 * NR) {  // the two halves' sums, in a fixed order
     const int tok = tid & 63, which = tid >> 6;
     const float ss = s_part[which * NR + tok] + s_part[(2 + which) * NR + tok];
-    pad(tok, which ? kIk : kIq) = a.qk_l2norm ? 1.0f / sqrtf(ss + 1e-6f) : 1.0f;
+    const float inv = a.qk_l2norm ? 1.0f / sqrtf(ss + 1e-6f) : 1.0f;
+    pad(tok, which ? kIk : kIq) = inv;
+    if (which) s_ik[tok] = inv;
   }
   uint32_t phase = 0;
   bool bad = false;
@@ -436,21 +457,21 @@ __global__ void __launch_bounds__(kThreadsTc, 2)
     if (tid < NR) {
       const int ci = tid / C, tl = tid % C;
       float g = 0.0f, be = 0.0f;
-      if (tl < s_L[ci]) {
-        if (hr == 0)
-          gate_log_raw(gr0, a.gate_mode, g, be);
-        else
-          gate_log(a.a, a.b, a.gate_mode, a.A_log, a.dt_bias,
-                   static_cast<int64_t>(s_t0[ci] + tl) * a.Hv + h, h, g, be);
+      if (hr == 1) {  // computed during the first head's solve, already scanned
+        g = s_G1[tid];
+        be = s_beta1[tid];
+      } else {
+        if (tl < s_L[ci]) {
+          if (hr == 0)
+            gate_log_raw(gr0, a.gate_mode, g, be);
+          else
+            gate_log(a.a, a.b, a.gate_mode, a.A_log, a.dt_bias,
+                     static_cast<int64_t>(s_t0[ci] + tl) * a.Hv + h, h, g, be);
+        }
+        g = chunk_scan<C>(g, lane);
       }
       pad(tid, kBeta) = be;
       s_beta[tid] = be;
-      constexpr int kSeg = C < 32 ? C : 32;
-#pragma unroll
-      for (int d = 1; d < kSeg; d <<= 1) {
-        const float n = __shfl_up_sync(0xffffffffu, g, d);
-        if ((lane & (kSeg - 1)) >= d) g += n;
-      }
       s_G[tid] = g;
     }
     __syncthreads();
@@ -502,11 +523,17 @@ __global__ void __launch_bounds__(kThreadsTc, 2)
         const float bt = pad(t, kBeta), ikt = pad(t, kIk);
         float av[NH];
 #pragma unroll
-        for (int e = 0; e < NH; ++e) {
-          const int j = half * NH + e;
-          const int tj = ci * C + j;
-          const float dec = (live && j < tl) ? __expf(Gt - s_G[tj]) : 0.0f;
-          av[e] = (j < tl) ? bt * dec * ikt * pad(tj, kIk) * xv[e] : 0.0f;
+        for (int e4 = 0; e4 < NH; e4 += 4) {
+          const int j0 = half * NH + e4, tj0 = ci * C + j0;
+          const float4 G4 = *reinterpret_cast<const float4*>(s_G + tj0);
+          const float4 K4 = *reinterpret_cast<const float4*>(s_ik + tj0);
+          const float Gj[4] = {G4.x, G4.y, G4.z, G4.w}, ikj[4] = {K4.x, K4.y, K4.z, K4.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int j = j0 + e;
+            const float dec = (live && j < tl) ? __expf(Gt - Gj[e]) : 0.0f;
+            av[e4 + e] = (j < tl) ? bt * dec * ikt * ikj[e] * xv[e4 + e] : 0.0f;
+          }
         }
 #pragma unroll
         for (int e = 0; e < NH; e += 4)  // the thread's half row of A, 16 bytes at a time
@@ -518,11 +545,17 @@ __global__ void __launch_bounds__(kThreadsTc, 2)
         const float iqt = pad(t, kIq) * a.scale;
         float pv[NH];
 #pragma unroll
-        for (int e = 0; e < NH; ++e) {
-          const int j = half * NH + e;
-          const int tj = ci * C + j;
-          const float dec = (live && j <= tl) ? __expf(Gt - s_G[tj]) : 0.0f;
-          pv[e] = dec * iqt * pad(tj, kIk) * xv[e];
+        for (int e4 = 0; e4 < NH; e4 += 4) {
+          const int j0 = half * NH + e4, tj0 = ci * C + j0;
+          const float4 G4 = *reinterpret_cast<const float4*>(s_G + tj0);
+          const float4 K4 = *reinterpret_cast<const float4*>(s_ik + tj0);
+          const float Gj[4] = {G4.x, G4.y, G4.z, G4.w}, ikj[4] = {K4.x, K4.y, K4.z, K4.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int j = j0 + e;
+            const float dec = (live && j <= tl) ? __expf(Gt - Gj[e]) : 0.0f;
+            pv[e4 + e] = dec * iqt * ikj[e] * xv[e4 + e];
+          }
         }
         unsigned char* ph = wb.Pt + (static_cast<size_t>(c) * a.Hv + h) * 2 * wb.p_tile;
 #pragma unroll
@@ -655,6 +688,17 @@ __global__ void __launch_bounds__(kThreadsTc, 2)
           dq[i] = srcq[i];
           dk[i] = srck[i];
         }
+      }
+      // then, during the first head's solve, the second head's gates (warps 4 and 5, token row
+      // u), scanned within the warp as that head's gate phase would
+      if (hr == 0 && R > 1 && u < NR) {
+        const int ci = u / C, tl = u % C, h1 = kh * R + 1;
+        float g = 0.0f, be = 0.0f;
+        if (tl < s_L[ci])
+          gate_log(a.a, a.b, a.gate_mode, a.A_log, a.dt_bias,
+                   static_cast<int64_t>(s_t0[ci] + tl) * a.Hv + h1, h1, g, be);
+        s_G1[u] = chunk_scan<C>(g, lane);
+        s_beta1[u] = be;
       }
     }
     bad = tc_sync(bad);

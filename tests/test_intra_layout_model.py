@@ -35,6 +35,7 @@ def layout(C):
     L["A"] = (o, NR * sa * 4); o += NR * sa * 4
     L["G"] = (o, NR * 4); o += NR * 4
     L["part"] = (o, 4 * NR * 4); o += 4 * NR * 4
+    L["tok"] = (o, 3 * NR * 4); o += 3 * NR * 4   # ik, the second head's G and beta
     L["bar"] = (o, 8); o += 8
     L["tmem"] = (o, 8); o += 8
     L["t0"] = (o, 2 * (NR // C) * 4); o += 2 * (NR // C) * 4
