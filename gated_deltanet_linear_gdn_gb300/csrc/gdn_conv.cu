@@ -77,51 +77,64 @@ __device__ __forceinline__ void window8(const LayerArgs& a, const PrefillExtra& 
 
 // y[t, :] = conv output of token t (bf16) for every token of an active sequence (the
 // tokens of inactive ones are never read). A CTA covers a run of min(kConvRun, C) tokens
-// inside one chunk (so within one sequence, found in the chunk table) and 2 kConvRunThreads
-// channels; a thread keeps one channel pair for the run, so a warp reads 128 contiguous
-// bytes of each input row: the conv parameters are loaded once, the window is built once
-// (from x or, before the sequence start, the initial conv state) and then rolled in
-// registers, and the input rows come kConvBatch at a time with the next batch in flight
-// (the loads, 4 bytes each, need that depth to keep the memory system busy). The
-// per-channel taps are conv_tap_sum's, as in the decode conv; the SiLU is silu_fast (the
-// kernel is bound by instruction issue, and its bf16 output feeds the prefill, whose bound is
-// far looser than the unit of bf16 it can move; the decode conv keeps the IEEE silu_f).
+// inside one chunk (so within one sequence, found in the chunk table) and 8 kConvRunThreads
+// channels; a thread keeps 8 consecutive channels for the run, so each of its input and
+// output rows is one 16-byte access and a warp moves 512 contiguous bytes of a row. The conv
+// parameters are loaded once, the window is built once (from x or, before the sequence start,
+// the initial conv state) and then rolled in registers, and the input rows come kBatch at a
+// time with the next batch in flight.
+// Per channel the taps are conv_tap_sum's (fp32 accumulator from the bias, taps in order).
+// With a bf16 cache every operand is a bf16 value, so each tap product rounded to bf16 is one
+// packed bf16 multiply of the raw input words (the exact product, rounded once to nearest
+// even, as the fp32 product -- exact for two bf16 factors -- rounded to bf16 is); with an fp32
+// cache the products are fp32 (the initial window's values need not be bf16). The SiLU is
+// silu_fast (the kernel is bound by instruction issue and memory, and its bf16 output feeds
+// the prefill, whose bound is far looser than the unit of bf16 it can move; the decode conv
+// keeps the IEEE silu_f).
 constexpr int kConvRun = 32;
-constexpr int kConvBatch = 8;
 constexpr int kConvRunThreads = 256;
+constexpr int kConvBatch = 8;
 
-// The W-1 taps before token t0 of channels c0, c0 + 1 (t0 in sequence i starting at bos):
-// positions before bos come from the initial conv state, or are zero without one.
+// two bf16 values (lo, hi) times two bf16 values, each product rounded to bf16
+__device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+__device__ __forceinline__ float2 bf16x2_to_float2(uint32_t v) {
+  return make_float2(__uint_as_float(v << 16), __uint_as_float(v & 0xFFFF0000u));
+}
+
+// The W-1 taps before token t0 of channels [c0, c0 + 8) (t0 in sequence i starting at bos, a
+// run start: bos itself or at least 16 tokens later): at the sequence start they are the
+// initial conv state (zero without one), otherwise the W-1 input rows before t0.
 template <bool kF32Cache>
-__device__ __forceinline__ void window2(const LayerArgs& a, const PrefillExtra& p, int i, int bos,
-                                        int t0, int c0, float (&win)[2][kConvW - 1]) {
+__device__ __forceinline__ void window_before8(const LayerArgs& a, const PrefillExtra& p, int i,
+                                               int bos, int t0, int c0,
+                                               float (&win)[8][kConvW - 1]) {
+  if (t0 == bos) {
+    const bool init = (p.has_init == nullptr) || (p.has_init[i] != 0);
+    if (init) {
+      load_conv8<kF32Cache>(a.conv_state, a.conv_layout, a.slot[i], a.D, c0, win);
+    } else {
+#pragma unroll
+      for (int ch = 0; ch < 8; ++ch)
+#pragma unroll
+        for (int j = 0; j < kConvW - 1; ++j) win[ch][j] = 0.0f;
+    }
+    return;
+  }
   const uint16_t* x = static_cast<const uint16_t*>(a.mixed);
-  const bool init = (p.has_init == nullptr) || (p.has_init[i] != 0);
-  const int64_t s = a.slot[i];
 #pragma unroll
   for (int j = 0; j < kConvW - 1; ++j) {
-    const int pos = t0 - (kConvW - 1) + j;
-    if (pos >= bos) {
-      const uint32_t v = *reinterpret_cast<const uint32_t*>(x + static_cast<int64_t>(pos) * a.D + c0);
-      win[0][j] = __uint_as_float(v << 16);
-      win[1][j] = __uint_as_float(v & 0xFFFF0000u);
-    } else if (!init) {
-      win[0][j] = win[1][j] = 0.0f;
-    } else {
-      const int jj = (kConvW - 1) + (pos - bos);  // tap of the initial window
+    float v[8];
+    unpack8(__ldg(reinterpret_cast<const uint4*>(x + static_cast<int64_t>(t0 - (kConvW - 1) + j) * a.D + c0)), v);
 #pragma unroll
-      for (int ch = 0; ch < 2; ++ch) {
-        const int64_t idx = a.conv_layout == GDN_CONV_DIM_FIRST
-                                ? (s * a.D + c0 + ch) * (kConvW - 1) + jj
-                                : (s * (kConvW - 1) + jj) * a.D + c0 + ch;
-        win[ch][j] = kF32Cache ? static_cast<const float*>(a.conv_state)[idx]
-                               : bf2f(static_cast<const uint16_t*>(a.conv_state)[idx]);
-      }
-    }
+    for (int ch = 0; ch < 8; ++ch) win[ch][j] = v[ch];
   }
 }
 
-template <bool kF32Cache>
+template <bool kF32Cache, int kBatch>
 __global__ void __launch_bounds__(kConvRunThreads)
     prefill_conv_kernel(LayerArgs a, PrefillExtra p, const int32_t* meta,
                         const int32_t* chunk_off, const int32_t* chunk_seq, uint16_t* y) {
@@ -132,53 +145,102 @@ __global__ void __launch_bounds__(kConvRunThreads)
   const int bos = p.cu_seqlens[i], eos = p.cu_seqlens[i + 1];
   const int t0 = bos + (c - chunk_off[i]) * p.chunk + (blockIdx.x % runs) * run;
   const int n = min(run, eos - t0);
-  const int c0 = (blockIdx.y * kConvRunThreads + threadIdx.x) * 2;
+  const int c0 = (blockIdx.y * kConvRunThreads + threadIdx.x) * 8;
   if (n <= 0 || c0 >= a.D) return;
   const uint16_t* x = static_cast<const uint16_t*>(a.mixed) + c0;
-  float2 w[kConvW], bias;  // (channel c0, channel c0 + 1) pairs
+  // parameters: tap j of the channel pair (c0 + 2q, c0 + 2q + 1)
+  uint32_t wq[kConvW][4];  // as bf16 pairs (lo = channel c0 + 2q)
+  float2 bias[4];
   {
-    const uint16_t* wp = static_cast<const uint16_t*>(a.conv_w) + static_cast<int64_t>(c0) * kConvW;
-    const uint4 wv = __ldg(reinterpret_cast<const uint4*>(wp));  // [2 channels][4 taps]
-    float wf[8];
-    unpack8(wv, wf);
+    const uint4* wp = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.conv_w) +
+                                                     static_cast<int64_t>(c0) * kConvW);
+    uint32_t wa[16];  // [8 channels][4 taps] bf16, two per word
 #pragma unroll
-    for (int j = 0; j < kConvW; ++j) w[j] = make_float2(wf[j], wf[kConvW + j]);
+    for (int k = 0; k < 4; ++k) {
+      const uint4 v = __ldg(wp + k);
+      wa[4 * k] = v.x; wa[4 * k + 1] = v.y; wa[4 * k + 2] = v.z; wa[4 * k + 3] = v.w;
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+#pragma unroll
+      for (int j = 0; j < kConvW; ++j)
+        wq[j][q] = __byte_perm(wa[4 * q + (j >> 1)], wa[4 * q + 2 + (j >> 1)],
+                               (j & 1) ? 0x7632 : 0x5410);
     const uint16_t* bp = static_cast<const uint16_t*>(a.conv_b);
-    bias = bp ? make_float2(bf2f(bp[c0]), bf2f(bp[c0 + 1])) : make_float2(0.0f, 0.0f);
+    if (bp) {
+      const uint4 bv = __ldg(reinterpret_cast<const uint4*>(bp + c0));
+      bias[0] = bf16x2_to_float2(bv.x); bias[1] = bf16x2_to_float2(bv.y);
+      bias[2] = bf16x2_to_float2(bv.z); bias[3] = bf16x2_to_float2(bv.w);
+    } else {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) bias[q] = make_float2(0.0f, 0.0f);
+    }
   }
   auto load_x = [&](int k) {  // input row t0 + k (zeros past the run)
-    return k < n ? __ldg(reinterpret_cast<const unsigned int*>(x + static_cast<int64_t>(t0 + k) * a.D))
-                 : 0u;
+    return k < n ? __ldg(reinterpret_cast<const uint4*>(x + static_cast<int64_t>(t0 + k) * a.D))
+                 : make_uint4(0u, 0u, 0u, 0u);
   };
-  uint32_t xn[kConvBatch];
+  uint4 xn[kBatch];
 #pragma unroll
-  for (int k = 0; k < kConvBatch; ++k) xn[k] = load_x(k);
-  float2 win[kConvW];  // taps 0 .. W-2 of the current token, then its input
+  for (int k = 0; k < kBatch; ++k) xn[k] = load_x(k);
+  // taps 0 .. W-2 of the current token: bf16 pairs (bf16 cache) or floats (fp32 cache)
+  uint32_t wb[kConvW - 1][4];
+  float2 wf[kConvW - 1][4];
   {
-    float w2[2][kConvW - 1];
-    window2<kF32Cache>(a, p, i, bos, t0, c0, w2);
+    float w8[8][kConvW - 1];
+    window_before8<kF32Cache>(a, p, i, bos, t0, c0, w8);
 #pragma unroll
-    for (int j = 0; j < kConvW - 1; ++j) win[j] = make_float2(w2[0][j], w2[1][j]);
+    for (int j = 0; j < kConvW - 1; ++j)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        wf[j][q] = make_float2(w8[2 * q][j], w8[2 * q + 1][j]);
+        wb[j][q] = pack_bf2(w8[2 * q][j], w8[2 * q + 1][j]);  // exact: bf16 values
+      }
   }
   uint16_t* yo = y + static_cast<int64_t>(t0) * a.D + c0;
   const bool silu = a.silu != 0;
 #pragma unroll 1
-  for (int kb = 0; kb < n; kb += kConvBatch) {
-    uint32_t xc[kConvBatch];
+  for (int kb = 0; kb < n; kb += kBatch) {
+    uint4 xc[kBatch];
 #pragma unroll
-    for (int k = 0; k < kConvBatch; ++k) {
+    for (int k = 0; k < kBatch; ++k) {
       xc[k] = xn[k];
-      xn[k] = load_x(kb + kConvBatch + k);
+      xn[k] = load_x(kb + kBatch + k);
     }
 #pragma unroll
-    for (int k = 0; k < kConvBatch; ++k) {
+    for (int k = 0; k < kBatch; ++k) {
       if (kb + k >= n) break;
-      win[kConvW - 1] = make_float2(__uint_as_float(xc[k] << 16), __uint_as_float(xc[k] & 0xFFFF0000u));
-      float2 acc = conv_tap_sum2<kF32Cache>(win, w, bias);
-      if (silu) acc = make_float2(silu_fast(acc.x), silu_fast(acc.y));
+      const uint32_t xw[4] = {xc[k].x, xc[k].y, xc[k].z, xc[k].w};
+      uint32_t o[4];
 #pragma unroll
-      for (int j = 0; j < kConvW - 1; ++j) win[j] = win[j + 1];
-      *reinterpret_cast<uint32_t*>(yo + static_cast<int64_t>(kb + k) * a.D) = pack_bf2(acc.x, acc.y);
+      for (int q = 0; q < 4; ++q) {
+        float2 acc = bias[q];
+        if (!kF32Cache) {
+#pragma unroll
+          for (int j = 0; j < kConvW; ++j)
+            acc = __fadd2_rn(acc, bf16x2_to_float2(mul_bf16x2(wq[j][q], j < kConvW - 1 ? wb[j][q] : xw[q])));
+        } else {
+          const float2 xf = bf16x2_to_float2(xw[q]);
+#pragma unroll
+          for (int j = 0; j < kConvW; ++j)
+            acc = __fadd2_rn(acc, __fmul2_rn(bf16x2_to_float2(wq[j][q]), j < kConvW - 1 ? wf[j][q] : xf));
+        }
+        if (silu) acc = make_float2(silu_fast(acc.x), silu_fast(acc.y));
+        o[q] = pack_bf2(acc.x, acc.y);
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        if (!kF32Cache) {
+#pragma unroll
+          for (int j = 0; j < kConvW - 2; ++j) wb[j][q] = wb[j + 1][q];
+          wb[kConvW - 2][q] = xw[q];
+        } else {
+#pragma unroll
+          for (int j = 0; j < kConvW - 2; ++j) wf[j][q] = wf[j + 1][q];
+          wf[kConvW - 2][q] = bf16x2_to_float2(xw[q]);
+        }
+      }
+      *reinterpret_cast<uint4*>(yo + static_cast<int64_t>(kb + k) * a.D) = make_uint4(o[0], o[1], o[2], o[3]);
     }
   }
 }
@@ -235,11 +297,13 @@ cudaError_t launch_prefill_conv(const LayerArgs& a, const PrefillExtra& p, const
   const int gy = (groups + kConvThreads - 1) / kConvThreads;
   if (max_chunks > 0) {
     dim3 grid(static_cast<unsigned>(max_chunks) * (p.chunk / min(kConvRun, p.chunk)),
-              (a.D / 2 + kConvRunThreads - 1) / kConvRunThreads);
+              (a.D / 8 + kConvRunThreads - 1) / kConvRunThreads);
     if (a.conv_f32)
-      prefill_conv_kernel<true><<<grid, kConvRunThreads, 0, s>>>(a, p, meta, chunk_off, chunk_seq, y);
+      prefill_conv_kernel<true, kConvBatch><<<grid, kConvRunThreads, 0, s>>>(a, p, meta, chunk_off,
+                                                                             chunk_seq, y);
     else
-      prefill_conv_kernel<false><<<grid, kConvRunThreads, 0, s>>>(a, p, meta, chunk_off, chunk_seq, y);
+      prefill_conv_kernel<false, kConvBatch><<<grid, kConvRunThreads, 0, s>>>(a, p, meta, chunk_off,
+                                                                              chunk_seq, y);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
