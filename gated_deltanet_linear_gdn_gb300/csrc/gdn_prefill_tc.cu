@@ -330,12 +330,14 @@ template <int C>
 __global__ void __launch_bounds__(kThreadsTc, 2)
     intra_tc_kernel(LayerArgs a, PrefillExtra p, const uint16_t* __restrict__ y,
                     const int32_t* meta, const int32_t* chunk_off, const int32_t* chunk_seq,
-                    TcBufs wb, int cta0, int chain) {
+                    TcBufs wb, int cta0, int chain, int hsplit) {
   // cta0: the first CTA of this launch (a piece of the chunks). Every CTA, its work done, lets
   // the pass over the piece (a programmatic dependent of this grid) start its set-up. chain:
   // launched as a programmatic dependent of the pass over the piece before; CTA 0 then waits
   // for that pass before it exits, so that this grid -- which the pass over the piece waits
-  // for -- completes only after it (the other CTAs leave at once and free their SM)
+  // for -- completes only after it (the other CTAs leave at once and free their SM).
+  // hsplit: the CTA takes the one value head blockIdx.z of its k-head (a launch that fits one
+  // wave finishes in about half the time, each CTA repeating phase 1); otherwise all of them.
   using S = IntraSmem<C>;
   constexpr int CPC = S::CPC, NR = S::kRows;
   extern __shared__ __align__(1024) unsigned char sm[];
@@ -362,7 +364,9 @@ __global__ void __launch_bounds__(kThreadsTc, 2)
   const int kh = blockIdx.y;
   const int nchunks = meta[0];
   const int c_first = (cta0 + blockIdx.x) * CPC;
-  const bool waits = chain && blockIdx.x == 0 && blockIdx.y == 0;
+  const bool waits = chain && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0;
+  const int R = a.Hv / a.Hk;
+  const int hr0 = hsplit ? static_cast<int>(blockIdx.z) : 0, hr1 = hsplit ? hr0 + 1 : R;
   if (c_first >= nchunks) {  // no chunk of this CTA exists
     grid_dep_launch();
     if (waits) grid_dep_wait();
@@ -384,7 +388,7 @@ __global__ void __launch_bounds__(kThreadsTc, 2)
   // that their latency overlaps it
   GateRaw gr0{};
   if (tid < NR) {
-    const int ci = tid / C, tl = tid % C, h0 = kh * (a.Hv / a.Hk);
+    const int ci = tid / C, tl = tid % C, h0 = kh * R + hr0;
     if (tl < s_L[ci])
       gr0 = gate_load(a.a, a.b, a.gate_mode, a.A_log, a.dt_bias,
                       static_cast<int64_t>(s_t0[ci] + tl) * a.Hv + h0, h0);
@@ -448,8 +452,7 @@ __global__ void __launch_bounds__(kThreadsTc, 2)
   uint32_t phase = 0;
   bool bad = false;
 
-  const int R = a.Hv / a.Hk;
-  for (int hr = 0; hr < R && !bad; ++hr) {
+  for (int hr = hr0; hr < hr1 && !bad; ++hr) {
     const int h = kh * R + hr;
     // gates of the 64 token rows (warps 0 and 1, a row per thread), then the running sums per
     // chunk: an inclusive scan over the lanes of a chunk (C <= 32: inside a warp; C = 64: each
@@ -457,12 +460,12 @@ __global__ void __launch_bounds__(kThreadsTc, 2)
     if (tid < NR) {
       const int ci = tid / C, tl = tid % C;
       float g = 0.0f, be = 0.0f;
-      if (hr == 1) {  // computed during the first head's solve, already scanned
+      if (hr == 1 && hr0 == 0) {  // computed during the first head's solve, already scanned
         g = s_G1[tid];
         be = s_beta1[tid];
       } else {
         if (tl < s_L[ci]) {
-          if (hr == 0)
+          if (hr == hr0)
             gate_log_raw(gr0, a.gate_mode, g, be);
           else
             gate_log(a.a, a.b, a.gate_mode, a.A_log, a.dt_bias,
@@ -476,7 +479,7 @@ __global__ void __launch_bounds__(kThreadsTc, 2)
     }
     __syncthreads();
     if (C == 64 && tid >= 32 && tid < 64) s_G[tid] += s_G[31];  // read by all after the barrier below
-    if (hr == 0) {  // the G | QK product (issued once)
+    if (hr == hr0) {  // the G | QK product (issued once)
       if (!mbar_wait_bounded(bar, phase)) bad = true;
       bad = __any_sync(0xffffffffu, bad);
       phase ^= 1;
@@ -691,7 +694,7 @@ __global__ void __launch_bounds__(kThreadsTc, 2)
       }
       // then, during the first head's solve, the second head's gates (warps 4 and 5, token row
       // u), scanned within the warp as that head's gate phase would
-      if (hr == 0 && R > 1 && u < NR) {
+      if (hr == 0 && hr1 > 1 && u < NR) {
         const int ci = u / C, tl = u % C, h1 = kh * R + 1;
         float g = 0.0f, be = 0.0f;
         if (tl < s_L[ci])
@@ -1390,8 +1393,15 @@ cudaError_t launch_tc_c(const LayerArgs& a, const PrefillExtra& p, const TcLayou
     const int g_lo = bounds[k], g_hi = k + 1 < pieces ? bounds[k + 1] : INT_MAX;
     const int n_chunks = bounds[k + 1] - g_lo;
     if (n_chunks > 0) {
-      e = launch_k(k1, dim3((n_chunks + CPC - 1) / CPC, a.Hk), kThreadsTc, IntraSmem<C>::kBytes, s,
-                   k > 0, a, p, y, meta, chunk_off, chunk_seq, wb, g_lo / CPC, k > 0 ? 1 : 0);
+      // the first intra kernel of several pieces holds up the first pass: when its CTAs split
+      // by value head still fit one wave (two per SM), each takes one head
+      const unsigned nx = static_cast<unsigned>((n_chunks + CPC - 1) / CPC);
+      const int R = a.Hv / a.Hk;
+      const int hsplit = (k == 0 && pieces > 1 && R > 1 &&
+                          static_cast<int64_t>(nx) * a.Hk * R <= 2 * static_cast<int64_t>(sm_count()))
+                             ? 1 : 0;
+      e = launch_k(k1, dim3(nx, a.Hk, hsplit ? R : 1), kThreadsTc, IntraSmem<C>::kBytes, s, k > 0, a,
+                   p, y, meta, chunk_off, chunk_seq, wb, g_lo / CPC, k > 0 ? 1 : 0, hsplit);
       if (e != cudaSuccess) return e;
     }
     if (pieces == 1 && p.before_pass && (e = cudaEventRecord(p.before_pass, s)) != cudaSuccess)
