@@ -67,52 +67,109 @@ WsLayout ws_layout(int T, int N, int Hv, int dk, int dv, int C, int conv, int D)
 
 // ---------------------------------------------------------------- prep
 constexpr int kOrderMaxSeqs = 1024;  // sequences ranked by length; identity order beyond
+constexpr int kPrepThreads = 1024;
 
-__global__ void prep_kernel(LayerArgs a, PrefillExtra p, int32_t* meta, int32_t* seq_ok,
-                            int32_t* chunk_off, int32_t* chunk_seq, int32_t* seq_order) {
-  __shared__ int s_valid;
-  __shared__ int s_cnt[kOrderMaxSeqs];
-  const int N = p.num_seqs, C = p.chunk;
-  if (threadIdx.x == 0) {
-    int valid = p.cu_seqlens[0] == 0 && p.cu_seqlens[N] == p.total_tokens;
-    for (int i = 0; i < N && valid; ++i) valid = p.cu_seqlens[i + 1] >= p.cu_seqlens[i];
-    if (!valid && a.err) atomicOr(a.err, GDN_DEVERR_SEQLENS);
-    s_valid = valid;
+// Inclusive sum of v over the block (kPrepThreads threads), in a fixed order.
+__device__ __forceinline__ int block_scan_incl(int v, int* s_warp) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int u = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += u;
   }
+  if (lane == 31) s_warp[warp] = v;
   __syncthreads();
-  const int valid = s_valid;
-  for (int i = threadIdx.x; i < N; i += blockDim.x) {
-    const int32_t s = a.slot[i];
-    if (s >= a.num_slots && a.err) atomicOr(a.err, GDN_DEVERR_SLOT_RANGE);
-    seq_ok[i] = valid && s > 0 && s < a.num_slots;
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    int acc = 0;
-    chunk_off[0] = 0;
-    for (int i = 0; i < N; ++i) {
-      const int len = valid ? p.cu_seqlens[i + 1] - p.cu_seqlens[i] : 0;
-      acc += seq_ok[i] ? (len + C - 1) / C : 0;
-      chunk_off[i + 1] = acc;
+  if (warp == 0) {
+    int w = s_warp[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int u = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += u;
     }
-    meta[0] = acc;
+    s_warp[lane] = w;
   }
   __syncthreads();
-  for (int i = threadIdx.x; i < N; i += blockDim.x)
-    for (int c = chunk_off[i]; c < chunk_off[i + 1]; ++c) chunk_seq[c] = i;
+  const int r = v + (warp > 0 ? s_warp[warp - 1] : 0);
+  __syncthreads();  // s_warp free for the next call
+  return r;
+}
+
+// The chunk table of a prefill call, one CTA. Every step is parallel over sequences or chunks
+// and works in shared memory: the call's first kernels wait for it.
+__global__ void __launch_bounds__(kPrepThreads)
+    prep_kernel(LayerArgs a, PrefillExtra p, int32_t* meta, int32_t* seq_ok, int32_t* chunk_off,
+                int32_t* chunk_seq, int32_t* seq_order) {
+  __shared__ int s_bad;
+  __shared__ int s_warp[32];
+  __shared__ int s_off[kOrderMaxSeqs + 1];  // chunk_off, when N <= kOrderMaxSeqs
+  const int N = p.num_seqs, C = p.chunk, tid = threadIdx.x;
+  // a kernel launched as a programmatic dependent of this one may start now; it waits for this
+  // grid's completion before it reads the tables
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (tid == 0) s_bad = 0;
+  __syncthreads();
+  // cu_seqlens: starts at 0, ends at total_tokens, never decreases
+  for (int i = tid; i <= N; i += kPrepThreads) {
+    const int v = p.cu_seqlens[i];
+    const bool bad = (i == 0 && v != 0) || (i == N && v != p.total_tokens) ||
+                     (i < N && p.cu_seqlens[i + 1] < v);
+    if (bad) s_bad = 1;
+  }
+  __syncthreads();
+  const bool valid = s_bad == 0;
+  if (tid == 0 && !valid && a.err) atomicOr(a.err, GDN_DEVERR_SEQLENS);
+  const bool small = N <= kOrderMaxSeqs;
+  // per sequence: active or not, its chunk count; chunk_off by a running block scan
+  int carry = 0;
+  if (tid == 0) chunk_off[0] = 0;
+  if (small && tid == 0) s_off[0] = 0;
+  for (int b = 0; b < N; b += kPrepThreads) {
+    const int i = b + tid;
+    int cnt = 0;
+    if (i < N) {
+      const int32_t sl = a.slot[i];
+      if (sl >= a.num_slots && a.err) atomicOr(a.err, GDN_DEVERR_SLOT_RANGE);
+      const bool ok = valid && sl > 0 && sl < a.num_slots;
+      seq_ok[i] = ok;
+      if (ok) cnt = (p.cu_seqlens[i + 1] - p.cu_seqlens[i] + C - 1) / C;
+    }
+    const int incl = carry + block_scan_incl(cnt, s_warp);
+    if (i < N) {
+      chunk_off[i + 1] = incl;
+      if (small) s_off[i + 1] = incl;
+    }
+    if (tid == kPrepThreads - 1) s_warp[0] = incl;  // the tile's last prefix: the next carry
+    __syncthreads();
+    carry = s_warp[0];
+    __syncthreads();
+  }
+  if (tid == 0) meta[0] = carry;
+  __syncthreads();  // chunk_off (global) and s_off visible to the block
+  // chunk_seq[c]: the last sequence whose first chunk is at or before c
+  const int32_t* off = small ? s_off : chunk_off;
+  for (int c = tid; c < carry; c += kPrepThreads) {
+    int lo = 0, hi = N - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (off[mid] <= c) lo = mid;
+      else hi = mid - 1;
+    }
+    chunk_seq[c] = lo;
+  }
   if (seq_order == nullptr) return;
   // seq_order[r] = the sequence of rank r by descending chunk count (ties by index): a state
   // pass launched in this order starts its longest chains first
-  if (N > kOrderMaxSeqs) {
-    for (int i = threadIdx.x; i < N; i += blockDim.x) seq_order[i] = i;
+  if (!small) {
+    for (int i = tid; i < N; i += kPrepThreads) seq_order[i] = i;
     return;
   }
-  for (int i = threadIdx.x; i < N; i += blockDim.x) s_cnt[i] = chunk_off[i + 1] - chunk_off[i];
-  __syncthreads();
-  for (int i = threadIdx.x; i < N; i += blockDim.x) {
-    const int ci = s_cnt[i];
+  for (int i = tid; i < N; i += kPrepThreads) {
+    const int ci = s_off[i + 1] - s_off[i];
     int r = 0;
-    for (int j = 0; j < N; ++j) r += (s_cnt[j] > ci) || (s_cnt[j] == ci && j < i);
+    for (int j = 0; j < N; ++j) {
+      const int cj = s_off[j + 1] - s_off[j];
+      r += (cj > ci) || (cj == ci && j < i);
+    }
     seq_order[r] = i;
   }
 }
@@ -450,7 +507,7 @@ cudaError_t launch_prefill_dk(const LayerArgs& a, const PrefillExtra& p, cudaStr
   float* Pb = reinterpret_cast<float*>(ws + L.P);
   float* Gb = reinterpret_cast<float*>(ws + L.G);
 
-  prep_kernel<<<1, 256, 0, s>>>(a, p, meta, seq_ok, chunk_off, chunk_seq, nullptr);
+  prep_kernel<<<1, kPrepThreads, 0, s>>>(a, p, meta, seq_ok, chunk_off, chunk_seq, nullptr);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const uint16_t* y = static_cast<const uint16_t*>(a.mixed);
@@ -482,7 +539,7 @@ cudaError_t launch_prefill_dk(const LayerArgs& a, const PrefillExtra& p, cudaStr
 cudaError_t launch_prefill_prep(const LayerArgs& a, const PrefillExtra& p, int32_t* meta,
                                 int32_t* seq_ok, int32_t* chunk_off, int32_t* chunk_seq,
                                 int32_t* seq_order, cudaStream_t s) {
-  prep_kernel<<<1, 256, 0, s>>>(a, p, meta, seq_ok, chunk_off, chunk_seq, seq_order);
+  prep_kernel<<<1, kPrepThreads, 0, s>>>(a, p, meta, seq_ok, chunk_off, chunk_seq, seq_order);
   return cudaGetLastError();
 }
 

@@ -330,7 +330,7 @@ template <int C>
 __global__ void __launch_bounds__(kThreadsTc, 2)
     intra_tc_kernel(LayerArgs a, PrefillExtra p, const uint16_t* __restrict__ y,
                     const int32_t* meta, const int32_t* chunk_off, const int32_t* chunk_seq,
-                    TcBufs wb, int cta0, int chain, int hsplit) {
+                    TcBufs wb, int cta0, int chain, int hsplit, int pre_wait) {
   // cta0: the first CTA of this launch (a piece of the chunks). Every CTA, its work done, lets
   // the pass over the piece (a programmatic dependent of this grid) start its set-up. chain:
   // launched as a programmatic dependent of the pass over the piece before; CTA 0 then waits
@@ -338,6 +338,9 @@ __global__ void __launch_bounds__(kThreadsTc, 2)
   // for -- completes only after it (the other CTAs leave at once and free their SM).
   // hsplit: the CTA takes the one value head blockIdx.z of its k-head (a launch that fits one
   // wave finishes in about half the time, each CTA repeating phase 1); otherwise all of them.
+  // pre_wait: launched as a programmatic dependent of the kernel before it (the chunk table's,
+  // or the conv's), whose results it waits for before reading anything.
+  if (pre_wait) grid_dep_wait();
   using S = IntraSmem<C>;
   constexpr int CPC = S::CPC, NR = S::kRows;
   extern __shared__ __align__(1024) unsigned char sm[];
@@ -1374,6 +1377,8 @@ cudaError_t launch_tc_c(const LayerArgs& a, const PrefillExtra& p, const TcLayou
   // pass(k) left. The first piece is short, so that the first pass starts early, and each next
   // one half as long again: its intra kernel, on the SMs the pass leaves, keeps ahead of the
   // pass before it. Not for the mixed step, which puts its decode rows beside the pass.
+  // intra(0) is a programmatic dependent too, of the kernel before it (the chunk table's, or the
+  // conv's), and waits for it at entry: its launch overlaps that kernel.
   int bounds[16] = {0, M}, pieces = 1;
   if (static_cast<int64_t>(p.num_seqs) * a.Hv <= kPieceSeqHeads && !p.before_pass && M >= 16) {
     int n = (max(4, M / 8) + CPC - 1) / CPC * CPC, g = 0;
@@ -1400,8 +1405,9 @@ cudaError_t launch_tc_c(const LayerArgs& a, const PrefillExtra& p, const TcLayou
       const int hsplit = (k == 0 && pieces > 1 && R > 1 &&
                           static_cast<int64_t>(nx) * a.Hk * R <= 2 * static_cast<int64_t>(sm_count()))
                              ? 1 : 0;
-      e = launch_k(k1, dim3(nx, a.Hk, hsplit ? R : 1), kThreadsTc, IntraSmem<C>::kBytes, s, k > 0, a,
-                   p, y, meta, chunk_off, chunk_seq, wb, g_lo / CPC, k > 0 ? 1 : 0, hsplit);
+      e = launch_k(k1, dim3(nx, a.Hk, hsplit ? R : 1), kThreadsTc, IntraSmem<C>::kBytes, s, true, a,
+                   p, y, meta, chunk_off, chunk_seq, wb, g_lo / CPC, k > 0 ? 1 : 0, hsplit,
+                   k == 0 ? 1 : 0);
       if (e != cudaSuccess) return e;
     }
     if (pieces == 1 && p.before_pass && (e = cudaEventRecord(p.before_pass, s)) != cudaSuccess)

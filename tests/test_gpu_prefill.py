@@ -112,6 +112,23 @@ def test_prefill_slot_contract_and_empty_sequences():
     assert np.all(d.conv_state_host()[5] == 0)
 
 
+@pytest.mark.parametrize("geo", [gi.TINY, gi.Geometry(1, 2, 128, 128)], ids=["tiny", "head128"])
+def test_prefill_more_sequences_than_ranked(geo):
+    """1,100 sequences, more than the chunk-table kernel ranks by length (1,024): mostly 0..4
+    tokens, a few longer ones, some inactive slots and some without an initial state."""
+    rng = np.random.default_rng(1100)
+    n = 1100
+    lens = rng.integers(0, 5, n)
+    lens[rng.choice(n, 6, replace=False)] = [40, 70, 129, 150, 64, 200]
+    slots = rng.permutation(np.arange(1, 1201))[:n]
+    slots[rng.choice(n, 20, replace=False)] = 0
+    slots[rng.choice(n, 5, replace=False)] = -1
+    inp = gi.make_inputs(geo, [int(x) for x in lens], 1201, seed=1101, slots=list(slots),
+                         has_init=list(rng.integers(0, 2, n)))
+    for chunk in (16, 64):
+        check_prefill(inp, chunk=chunk, bf16_too=False)
+
+
 def test_prefill_bad_cu_seqlens_sets_error():
     inp = gi.make_inputs(gi.TINY, [5, 6], 4, seed=6)
     d = Device(inp)
