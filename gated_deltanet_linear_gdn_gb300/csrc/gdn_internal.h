@@ -67,7 +67,7 @@ struct PrefillExtra {
   int chunk;
   void* workspace;
   size_t workspace_bytes;
-  cudaEvent_t before_pass;  // recorded on the stream just before the state pass (nullable)
+  cudaEvent_t before_pass;  // recorded on the stream just before the (last) state pass (nullable)
 };
 
 cudaError_t launch_conv_update(const ConvUpdateArgs& a, cudaStream_t s);

@@ -14,9 +14,10 @@
 // Scheduling: the chunked prefill's state pass occupies one CTA per (sequence,
 // value head) -- 32 of the 152 SMs for one Qwen3-Next sequence -- for most of
 // its time. The decode rows are therefore enqueued on a side stream that waits
-// for an event recorded just before that pass, with the decode grid capped to
-// the SMs the pass leaves free; the caller's stream then waits for the side
-// stream. The side stream and its two events are created once per device, on
+// for an event recorded just before that pass (before its last piece, when the
+// prefill runs in pieces: no intra kernel runs beside it), with the decode grid
+// capped to the SMs the pass leaves free; the caller's stream then waits for
+// the side stream. The side stream and its two events are created once per device, on
 // the first mixed call that needs them (make that call before any stream
 // capture); mixed calls on one device enqueue one at a time.
 #include <mutex>

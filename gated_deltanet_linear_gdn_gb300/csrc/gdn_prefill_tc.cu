@@ -1376,11 +1376,12 @@ cudaError_t launch_tc_c(const LayerArgs& a, const PrefillExtra& p, const TcLayou
   // pass(k) before it exits, so pass(k + 1), which waits for intra(k + 1), finds the state
   // pass(k) left. The first piece is short, so that the first pass starts early, and each next
   // one half as long again: its intra kernel, on the SMs the pass leaves, keeps ahead of the
-  // pass before it. Not for the mixed step, which puts its decode rows beside the pass.
+  // pass before it. The mixed step records its event (before_pass) before the last pass, the
+  // longest, beside which no intra kernel runs: its decode rows take the SMs that pass leaves.
   // intra(0) is a programmatic dependent too, of the kernel before it (the chunk table's, or the
   // conv's), and waits for it at entry: its launch overlaps that kernel.
   int bounds[16] = {0, M}, pieces = 1;
-  if (static_cast<int64_t>(p.num_seqs) * a.Hv <= kPieceSeqHeads && !p.before_pass && M >= 16) {
+  if (static_cast<int64_t>(p.num_seqs) * a.Hv <= kPieceSeqHeads && M >= 16) {
     int n = (max(4, M / 8) + CPC - 1) / CPC * CPC, g = 0;
     pieces = 0;
     while (g < M && pieces < 15) {
@@ -1410,7 +1411,7 @@ cudaError_t launch_tc_c(const LayerArgs& a, const PrefillExtra& p, const TcLayou
                    k == 0 ? 1 : 0);
       if (e != cudaSuccess) return e;
     }
-    if (pieces == 1 && p.before_pass && (e = cudaEventRecord(p.before_pass, s)) != cudaSuccess)
+    if (k == pieces - 1 && p.before_pass && (e = cudaEventRecord(p.before_pass, s)) != cudaSuccess)
       return e;
     e = launch_k(k2, dim3(pass_ctas), kPassThreads, PassSmem<C>::kBytes, s, pieces > 1, a, p,
                  seq_ok, chunk_off, seq_order, wb, g_lo, g_hi, sx, pieces > 1 ? 1 : 0);

@@ -316,7 +316,8 @@ gdn_status gdn_chunked_prefill_noalloc(const void* mixed_qkv, const void* a, con
  * two separate calls.
  *
  * Scheduling: the decode rows run on a library-owned side stream that waits
- * for the prefill's state pass to start, on the SMs the pass leaves free; the
+ * for the prefill's state pass to start (its last piece, when a prefill of few
+ * sequences runs in pieces), on the SMs the pass leaves free; the
  * caller's stream then waits for the side stream, so the call is ordered on
  * `stream` like any other. The side stream and its events are created on the
  * first call per device that holds both parts: make it before any stream
