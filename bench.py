@@ -563,10 +563,13 @@ def prefill_cases(args):
     """The chunked-prefill workloads: one sequence (conv bypassed), then ~32k varlen tokens."""
     from gated_deltanet_linear_gdn_gb300 import inputs as gi
 
-    cases = [(f"single_{args.prefill_tokens}_bypass",
-              lambda: gi.prefill_single(args.prefill_tokens, seed=0))]
+    cases = []
+    if not args.no_single:
+        cases.append((f"single_{args.prefill_tokens}_bypass",
+                      lambda: gi.prefill_single(args.prefill_tokens, seed=0)))
     if not args.no_varlen:
-        cases.append(("varlen_8seq_conv", lambda: gi.prefill_varlen(8, 8192, seed=0)))
+        name = "varlen_8seq_conv" if args.varlen_max == 8192 else f"varlen_8seq_conv_max{args.varlen_max}"
+        cases.append((name, lambda: gi.prefill_varlen(8, args.varlen_max, seed=0)))
     return cases
 
 
@@ -699,6 +702,9 @@ def main():
     ap.add_argument("--prefill-tokens", type=int, default=4096,
                     help="length of the single-sequence prefill case")
     ap.add_argument("--no-varlen", action="store_true", help="skip the ~32k-token varlen case")
+    ap.add_argument("--no-single", action="store_true", help="skip the single-sequence prefill case")
+    ap.add_argument("--varlen-max", type=int, default=8192,
+                    help="upper bound of the varlen case's 8 sequence lengths (8192: ~32k tokens)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
