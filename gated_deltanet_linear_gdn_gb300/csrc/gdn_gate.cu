@@ -8,11 +8,16 @@
 // Per row (dv values o, the matching z):
 //   out = o / sqrt(mean(o^2) + eps) * (w + offset) * act(z)
 // in fp32 from o as stored (a bf16 output is read back as bf16, which is the
-// block's unfused arithmetic), an all-zero row with eps 0 giving zero.
+// block's unfused arithmetic), an all-zero row with eps 0 giving zero. The
+// activation takes the hardware exponential and a fast quotient (silu_fast; the
+// sigmoid likewise): the kernel is bound by instruction issue, and the prefill's
+// bound is far looser than the few fp32 ulp this moves. The decode epilogue keeps
+// the IEEE forms.
 //
 // One warp per row, dv/32 consecutive elements per lane, a 5-step xor-shuffle
-// sum of squares; a grid-stride loop over rows. HBM-bound: per row it reads o
-// and z and writes y.
+// sum of squares; a grid-stride loop over rows (kGateRows = 1: more rows in
+// flight per warp cost occupancy and measured slower). Per row it reads o and z
+// and writes y.
 #include "gdn_common.cuh"
 #include "gdn_internal.h"
 
@@ -21,6 +26,7 @@ namespace gdn {
 namespace {
 
 constexpr int kGateWarps = 8;
+constexpr int kGateRows = 1;  // consecutive rows a warp takes at a time
 
 template <int VPL>
 struct RowIO;
@@ -76,28 +82,39 @@ __global__ void __launch_bounds__(32 * kGateWarps)
   float w[VPL];
 #pragma unroll
   for (int e = 0; e < VPL; ++e) w[e] = __ldg(a.gate_w + lane * VPL + e) + a.gate_offset;
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * kGateWarps;
-  for (int64_t row = static_cast<int64_t>(blockIdx.x) * kGateWarps + (threadIdx.x >> 5); row < rows;
-       row += stride) {
-    float o[VPL], z[VPL];
-    IO::load_bf16(static_cast<const uint16_t*>(a.gate_z) + row * DV, lane, z);
-    if (a.out_f32) IO::load_f32(static_cast<const float*>(a.out) + row * DV, lane, o);
-    else IO::load_bf16(static_cast<const uint16_t*>(a.out) + row * DV, lane, o);
-    float ss = 0.0f;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * kGateWarps * kGateRows;
+  for (int64_t row0 = (static_cast<int64_t>(blockIdx.x) * kGateWarps + (threadIdx.x >> 5)) * kGateRows;
+       row0 < rows; row0 += stride) {
+    float o[kGateRows][VPL], z[kGateRows][VPL];
 #pragma unroll
-    for (int e = 0; e < VPL; ++e) ss = fmaf(o[e], o[e], ss);
-    ss = warp_sum(ss);
-    const float den = __fadd_rn(__fdiv_rn(ss, static_cast<float>(DV)), a.gate_eps);
-    const float inv = den > 0.0f ? 1.0f / sqrtf(den) : 0.0f;  // all-zero row, eps 0
-    float y[VPL];
-#pragma unroll
-    for (int e = 0; e < VPL; ++e) {
-      const float act = a.gate_act == GDN_ACT_SIGMOID ? __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-z[e])))
-                                                      : silu_f(z[e]);
-      y[e] = ((o[e] * inv) * w[e]) * act;
+    for (int k = 0; k < kGateRows; ++k) {
+      const int64_t row = row0 + k;
+      if (row >= rows) break;
+      IO::load_bf16(static_cast<const uint16_t*>(a.gate_z) + row * DV, lane, z[k]);
+      if (a.out_f32) IO::load_f32(static_cast<const float*>(a.out) + row * DV, lane, o[k]);
+      else IO::load_bf16(static_cast<const uint16_t*>(a.out) + row * DV, lane, o[k]);
     }
-    if (a.out_f32) IO::store_f32(static_cast<float*>(a.out) + row * DV, lane, y);
-    else IO::store_bf16(static_cast<uint16_t*>(a.out) + row * DV, lane, y);
+#pragma unroll
+    for (int k = 0; k < kGateRows; ++k) {
+      const int64_t row = row0 + k;
+      if (row >= rows) break;
+      float ss = 0.0f;
+#pragma unroll
+      for (int e = 0; e < VPL; ++e) ss = fmaf(o[k][e], o[k][e], ss);
+      ss = warp_sum(ss);
+      const float den = __fadd_rn(__fdiv_rn(ss, static_cast<float>(DV)), a.gate_eps);
+      const float inv = den > 0.0f ? 1.0f / sqrtf(den) : 0.0f;  // all-zero row, eps 0
+      float y[VPL];
+#pragma unroll
+      for (int e = 0; e < VPL; ++e) {
+        const float act = a.gate_act == GDN_ACT_SIGMOID
+                              ? __fdividef(1.0f, 1.0f + __expf(-z[k][e]))
+                              : silu_fast(z[k][e]);
+        y[e] = ((o[k][e] * inv) * w[e]) * act;
+      }
+      if (a.out_f32) IO::store_f32(static_cast<float*>(a.out) + row * DV, lane, y);
+      else IO::store_bf16(static_cast<uint16_t*>(a.out) + row * DV, lane, y);
+    }
   }
 }
 
@@ -108,7 +125,8 @@ cudaError_t launch_output_gate(const LayerArgs& a, int64_t rows, cudaStream_t s)
   int dev = 0, sms = 148;
   if (cudaGetDevice(&dev) == cudaSuccess)
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const int64_t want = (rows + kGateWarps - 1) / kGateWarps;
+  const int64_t per_block = static_cast<int64_t>(kGateWarps) * kGateRows;
+  const int64_t want = (rows + per_block - 1) / per_block;
   const int blocks = static_cast<int>(want < 8LL * sms ? want : 8LL * sms);
   switch (a.dv) {
     case 32: gate_rows_kernel<1><<<blocks, 32 * kGateWarps, 0, s>>>(a, rows); break;
