@@ -25,16 +25,21 @@
 // (hi*hi + hi*lo + lo*hi), one split and one exact operand two. The error per
 // product is ~1e-5 relative, well inside the prefill bound.
 //
-// Kernels (after the shared prep and conv):
-//   intra (chunks packed 128/C per CTA, k-head): KK^T and QK^T for 128 token
-//       rows at once (M = N = 128; the diagonal CxC blocks are the chunks'),
-//       then per value head: gates, A and P rows from tensor memory, the fp32
-//       triangular solve, U and W as MMAs with a block-diagonal T. Writes the
-//       pass's operand tiles, already in tensor-core layout, to workspace.
+// Kernels (after the shared chunk table and conv):
+//   intra (64 token rows = 64/C chunks of one k-head per CTA, two CTAs per SM):
+//       one MMA over the stacked [K; Q] operand (M = 128, N = 64) gives KK^T
+//       and QK^T of the 64 rows at once (the diagonal CxC blocks are the
+//       chunks'), then per value head: gates, A and P rows from tensor memory,
+//       the fp32 triangular solve, U and W as MMAs with a block-diagonal T.
+//       Writes the pass's operand tiles, already in tensor-core layout, to
+//       workspace.
 //   pass (sequence, value head): the state S lives in registers (a thread owns
-//       half a row); per chunk, bulk copies bring the chunk's tiles into shared
-//       memory, MMA group 1 forms D^T (= U^T - S W^T) and S Q^T, MMA group 2
-//       forms D^T P^T and the state update D'^T K; M = dv = 128 throughout.
+//       half a row), its bf16 hi / lo parts in tensor memory; per chunk, bulk
+//       copies bring the chunk's tiles into shared memory, MMA group 1 forms
+//       S W^T and S Q^T (the compute warps then form D^T = U^T - S W^T), MMA
+//       group 2 the state update D'^T K and then O2 = D^T P^T onto f_t O1;
+//       M = dv = 128 throughout. With few sequences the chunks run in pieces,
+//       each piece's pass beside the next piece's intra kernel.
 // Every wait is bounded (GDN_DEVERR_TIMEOUT on expiry, the CTA stops cleanly
 // and frees its tensor memory).
 #include <climits>
