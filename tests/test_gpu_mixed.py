@@ -84,6 +84,10 @@ COMPOSITIONS = [
     ("b64-three-prefills", gi.QWEN3_NEXT, 64, [130, 1, 77], 64, False),
     ("tiny-cuda-core-prefill", gi.TINY, 5, [40, 17], 16, False),
     ("b16-two-prefills-bf16-state", gi.QWEN3_NEXT, 16, [70, 129], 64, True),
+    # prefills of few sequences and at least 16 chunks run in pieces; the decode rows then run
+    # beside the last pass piece
+    ("b32-pieced-prefill", gi.QWEN3_NEXT, 32, [1500], 64, False),
+    ("b8-pieced-two-prefills-bf16-state", gi.QWEN3_NEXT, 8, [1100, 40], 64, True),
 ]
 
 

@@ -129,6 +129,22 @@ def test_prefill_more_sequences_than_ranked(geo):
         check_prefill(inp, chunk=chunk, bf16_too=False)
 
 
+@pytest.mark.parametrize("chunk", [32, 64])
+def test_prefill_pieces_with_empty_and_short_sequences(chunk):
+    """A call of few (sequence, value head) pairs and enough chunks runs in pieces: here two
+    empty sequences (one with an initial state, one without), a 3-token one that ends in the
+    first piece, and two that carry their state across pieces."""
+    lens = [0, 1500, 3, 0, 700]
+    inp = gi.make_inputs(gi.Geometry(1, 2, 128, 128), lens, 8, seed=1500 + chunk,
+                         has_init=[1, 0, 1, 0, 1])
+    m = (sum(lens) + len(lens) * (chunk - 1)) // chunk
+    assert len(lens) * 2 <= 64 and m >= 16        # the piece rule applies
+    ref, d, out = check_prefill(inp, chunk=chunk)
+    s_empty = int(inp.slot[3])                    # empty, no initial state: zero state and window
+    assert np.all(d.ssm[s_empty].cpu().numpy() == 0)
+    assert np.all(d.conv_state_host()[s_empty] == 0)
+
+
 def test_prefill_bad_cu_seqlens_sets_error():
     inp = gi.make_inputs(gi.TINY, [5, 6], 4, seed=6)
     d = Device(inp)
