@@ -229,15 +229,10 @@ def test_prefill_packing_invariance(geo, chunk, lens):
         assert torch.equal(ds.conv_state.cpu()[inv[sl]], d.conv_state.cpu()[sl])
 
 
-@pytest.mark.parametrize("chunk,state_bf16", [(64, False), (32, False), (64, True)])
-def test_prefill_pieces_bitwise(chunk, state_bf16):
-    """A long sequence alone runs its chunks in pieces (its intra kernel beside its state pass,
-    the fp32 state handed from piece to piece); packed with 44 other sequences it runs in one
-    piece. Its outputs, final state and conv window are bitwise the same either way (with a
-    bf16 state too: the state crosses piece boundaries unrounded)."""
-    geo = gi.QWEN3_NEXT
-    lens = [4096, 37, 150, 9, 200] + [5] * 40
-    inp = gi.make_inputs(geo, lens, 64, seed=12, state_bf16=state_bf16)
+def _pieces_alone_equals_packed(geo, lens, chunk, state_bf16, seed):
+    """The first sequence alone (in pieces) against the whole list packed (one piece): outputs,
+    final state and conv window bitwise. Returns the alone call's inputs."""
+    inp = gi.make_inputs(geo, lens, 64, seed=seed, state_bf16=state_bf16)
     d = Device(inp)
     full = gpu_prefill(d, chunk=chunk, out_f32=False)
     torch.cuda.synchronize()
@@ -257,6 +252,27 @@ def test_prefill_pieces_bitwise(chunk, state_bf16):
     s0 = int(inp.slot[0])
     assert torch.equal(ds.ssm.cpu()[s0], d.ssm.cpu()[s0])
     assert torch.equal(ds.conv_state.cpu()[s0], d.conv_state.cpu()[s0])
+    return sub
+
+
+@pytest.mark.parametrize("chunk,state_bf16", [(64, False), (32, False), (64, True)])
+def test_prefill_pieces_bitwise(chunk, state_bf16):
+    """A long sequence alone runs its chunks in pieces (its intra kernel beside its state pass,
+    the fp32 state handed from piece to piece); packed with 44 other sequences it runs in one
+    piece. Its outputs, final state and conv window are bitwise the same either way (with a
+    bf16 state too: the state crosses piece boundaries unrounded)."""
+    _pieces_alone_equals_packed(gi.QWEN3_NEXT, [4096, 37, 150, 9, 200] + [5] * 40, chunk,
+                                state_bf16, seed=12)
+
+
+def test_prefill_pieces_bitwise_four_value_heads_per_k_head():
+    """Hv / Hk = 4: alone, the sequence's first intra piece splits its CTAs four ways by value
+    head; packed with 14 others (120 sequence-head pairs) nothing is split. Bitwise the same,
+    and the alone call matches the oracle."""
+    geo = gi.Geometry(2, 8, 128, 128)
+    sub = _pieces_alone_equals_packed(geo, [1500, 37, 150, 9, 200] + [5] * 10, 64, False,
+                                      seed=13)
+    check_prefill(sub, chunk=64, bf16_too=False)
 
 
 def test_prefill_then_decode_continues_the_state():
