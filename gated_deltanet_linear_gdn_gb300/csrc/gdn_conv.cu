@@ -86,7 +86,8 @@ __device__ __forceinline__ void window8(const LayerArgs& a, const PrefillExtra& 
 // Per channel the taps are conv_tap_sum's (fp32 accumulator from the bias, taps in order).
 // With a bf16 cache every operand is a bf16 value, so each tap product rounded to bf16 is one
 // packed bf16 multiply of the raw input words (the exact product, rounded once to nearest
-// even, as the fp32 product -- exact for two bf16 factors -- rounded to bf16 is); with an fp32
+// even, as the fp32 product -- exact for two bf16 factors -- rounded to bf16 is), added to the
+// fp32 accumulator by a mixed-precision add that takes the bf16 half directly; with an fp32
 // cache the products are fp32 (the initial window's values need not be bf16). The SiLU is
 // silu_fast (the kernel is bound by instruction issue and memory, and its bf16 output feeds
 // the prefill, whose bound is far looser than the unit of bf16 it can move; the decode conv
@@ -103,6 +104,14 @@ __device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b) {
 }
 __device__ __forceinline__ float2 bf16x2_to_float2(uint32_t v) {
   return make_float2(__uint_as_float(v << 16), __uint_as_float(v & 0xFFFF0000u));
+}
+// acc + (lo, hi) of a bf16 pair, each sum rounded once in fp32 (the bf16 operand converts
+// exactly), as an fp32 add of the unpacked pair rounds it
+__device__ __forceinline__ float2 add_bf16x2(float2 acc, uint32_t v) {
+  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+      "add.rn.f32.bf16 %0, lo, %0;\n\tadd.rn.f32.bf16 %1, hi, %1;\n\t}"
+      : "+f"(acc.x), "+f"(acc.y) : "r"(v));
+  return acc;
 }
 
 // The W-1 taps before token t0 of channels [c0, c0 + 8) (t0 in sequence i starting at bos, a
@@ -218,7 +227,7 @@ __global__ void __launch_bounds__(kConvRunThreads)
         if (!kF32Cache) {
 #pragma unroll
           for (int j = 0; j < kConvW; ++j)
-            acc = __fadd2_rn(acc, bf16x2_to_float2(mul_bf16x2(wq[j][q], j < kConvW - 1 ? wb[j][q] : xw[q])));
+            acc = add_bf16x2(acc, mul_bf16x2(wq[j][q], j < kConvW - 1 ? wb[j][q] : xw[q]));
         } else {
           const float2 xf = bf16x2_to_float2(xw[q]);
 #pragma unroll
