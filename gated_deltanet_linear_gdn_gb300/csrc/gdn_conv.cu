@@ -44,37 +44,6 @@ __global__ void __launch_bounds__(kConvThreads) conv_update_kernel(ConvUpdateArg
   *out = pack8(h);
 }
 
-// Window tap j of token t: position p = t - (W-1) + j of its sequence; before
-// the sequence start it comes from the initial conv state (or zero).
-template <bool kF32Cache>
-__device__ __forceinline__ void window8(const LayerArgs& a, const PrefillExtra& p, int i, int bos,
-                                        int t, int c0, float (&win)[8][kConvW - 1],
-                                        float (&x8)[8]) {
-  const uint16_t* x = static_cast<const uint16_t*>(a.mixed);
-  const bool init = (p.has_init == nullptr) || (p.has_init[i] != 0);
-  const int32_t s = a.slot[i];
-  bool need_init = false;
-#pragma unroll
-  for (int j = 0; j < kConvW - 1; ++j) need_init |= (t - (kConvW - 1) + j < bos);
-  float st[8][kConvW - 1];
-  if (need_init && init) load_conv8<kF32Cache>(a.conv_state, a.conv_layout, s, a.D, c0, st);
-#pragma unroll
-  for (int j = 0; j < kConvW - 1; ++j) {
-    const int pos = t - (kConvW - 1) + j;
-    if (pos >= bos) {
-      float v[8];
-      unpack8(__ldg(reinterpret_cast<const uint4*>(x + static_cast<int64_t>(pos) * a.D + c0)), v);
-#pragma unroll
-      for (int ch = 0; ch < 8; ++ch) win[ch][j] = v[ch];
-    } else {
-      const int jj = (kConvW - 1) + (pos - bos);  // 0..W-2
-#pragma unroll
-      for (int ch = 0; ch < 8; ++ch) win[ch][j] = init ? st[ch][jj] : 0.0f;
-    }
-  }
-  unpack8(__ldg(reinterpret_cast<const uint4*>(x + static_cast<int64_t>(t) * a.D + c0)), x8);
-}
-
 // y[t, :] = conv output of token t (bf16) for every token of an active sequence (the
 // tokens of inactive ones are never read). A CTA covers a run of min(kConvRun, C) tokens
 // inside one chunk (so within one sequence, found in the chunk table) and 8 kConvRunThreads
