@@ -35,3 +35,23 @@ def test_traffic_only_for_the_captured_workload(state):
     assert bench.ncu_traffic(state, e["batch"], e["num_slots"]) == e
     assert bench.ncu_traffic(state, 1, 2) is None
     assert bench.ncu_traffic(state, e["batch"], 2 * e["num_slots"]) is None
+
+
+def _args(**kw):
+    import argparse
+    ns = dict(prefill_tokens=4096, no_varlen=False, no_single=False, varlen_max=8192)
+    ns.update(kw)
+    return argparse.Namespace(**ns)
+
+
+def test_prefill_cases_default_and_small_varlen():
+    """The default cases are the two the bench line reports; --no-single and --varlen-max
+    select the small varlen case the prefill profile is captured on."""
+    names = [n for n, _ in bench.prefill_cases(_args())]
+    assert names == ["single_4096_bypass", "varlen_8seq_conv"]
+    cases = bench.prefill_cases(_args(no_single=True, varlen_max=2048))
+    assert [n for n, _ in cases] == ["varlen_8seq_conv_max2048"]
+    inp = cases[0][1]()
+    lens = inp.cu_seqlens[1:] - inp.cu_seqlens[:-1]
+    assert lens.size == 8 and lens.max() <= 2048 and inp.conv_w is not None
+    assert bench.prefill_cases(_args(no_single=True, no_varlen=True)) == []
