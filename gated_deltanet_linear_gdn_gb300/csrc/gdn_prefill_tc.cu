@@ -859,6 +859,9 @@ __global__ void __launch_bounds__(kPassThreads, 1)
   }
   const int nch = c1 - c0;
   const bool from_slot = c0 == cs, to_slot = c1 == ce;
+  // tensor memory first: no return follows, and no other CTA that uses it shares this SM (shared
+  // memory excludes the intra kernel's), so the allocation does not wait on the kernels before
+  if (warp == 0) tc::tmem_alloc(&s_tmem, kTmemCols);
   if (pdl) grid_dep_wait();  // the piece's intra tiles, and the state the piece before left in sx
   const int32_t slot = a.slot[i];
   const bool init = (p.has_init == nullptr) || (p.has_init[i] != 0);
@@ -920,7 +923,6 @@ __global__ void __launch_bounds__(kPassThreads, 1)
     bulk_g2s(smem_addr(sm + S::oU), ut, static_cast<uint32_t>(kD * C * 4), fullU);
   };
 
-  if (warp == 0) tc::tmem_alloc(&s_tmem, kTmemCols);
   if (copy_warp && lane == 0) {
     for (int k = 0; k < 5; ++k) mbar_init(smem_addr(&s_bar[k]), 1);
     mbar_init(dead, 1);
@@ -934,12 +936,15 @@ __global__ void __launch_bounds__(kPassThreads, 1)
   const int64_t soff = (static_cast<int64_t>(slot) * a.Hv + h) * (kD * kD) + r * kD + half * 64;
   float* Sg = a.ssm + soff;                                          // fp32 state
   uint16_t* Sb = reinterpret_cast<uint16_t*>(a.ssm) + soff;          // bf16 state
-  float* Sx = sx ? sx + ((static_cast<int64_t>(i) * a.Hv + h) * kD + r) * kD + half * 64 : nullptr;
+  // the state between pieces: per (sequence, value head) 64 KB of fp32, float4 piece j of row r at
+  // [j][r] (j = 0 .. 31 along dk), so that a warp's 32 rows read or write 512 contiguous bytes
+  float* Sx = sx ? sx + (static_cast<int64_t>(i) * a.Hv + h) * (kD * kD) + (half * 16 * 128 + r) * 4
+                 : nullptr;
   float Sr[64];
   if (compute && !from_slot) {
 #pragma unroll
     for (int e = 0; e < 64; e += 4) {
-      const float4 v = *reinterpret_cast<const float4*>(Sx + e);
+      const float4 v = *reinterpret_cast<const float4*>(Sx + e / 4 * 128 * 4);
       Sr[e] = v.x; Sr[e + 1] = v.y; Sr[e + 2] = v.z; Sr[e + 3] = v.w;
     }
   } else if (compute) {
@@ -1300,7 +1305,7 @@ __global__ void __launch_bounds__(kPassThreads, 1)
     if (compute && !to_slot) {  // the next piece takes the state from here, unrounded
 #pragma unroll
       for (int e = 0; e < 64; e += 4)
-        *reinterpret_cast<float4*>(Sx + e) = make_float4(Sr[e], Sr[e + 1], Sr[e + 2], Sr[e + 3]);
+        *reinterpret_cast<float4*>(Sx + e / 4 * 128 * 4) = make_float4(Sr[e], Sr[e + 1], Sr[e + 2], Sr[e + 3]);
     } else if (compute) {
       if (a.ssm_bf16) {  // rounded to bf16 only here, at the write-back
 #pragma unroll
