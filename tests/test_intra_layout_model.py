@@ -157,3 +157,31 @@ def test_intra_writes_cover_each_piece_once(C):
         got = [16 * i for u in range(nthr) for i in range(u, slice_pieces, nthr)]
         pieces_once(got, C * KD * 2, f"q / k workspace tile, chunk {ci}")
         assert (ci + 1) * C * KD * 2 <= L["K"][1]
+
+
+def test_pass_state_handoff_layout():
+    """The state pass hands a (sequence, value head)'s fp32 state to the next piece through a 64 KB
+    block: compute thread (row r = 32 (w % 4) + lane, half = w // 4) stores and loads float4 piece j
+    (dk columns 4 (16 half + j) .. + 3) at float offset ((16 half + j) * 128 + r) * 4. Every element
+    once, inside the block, at the same place for the store and the load; and at each step j a
+    warp's 32 rows cover 512 contiguous bytes."""
+    seen = {}
+    for w in range(8):
+        half = w >> 2
+        steps = {}
+        for lane in range(32):
+            r = 32 * (w & 3) + lane
+            for j in range(16):
+                off = ((half * 16 + j) * 128 + r) * 4
+                assert 0 <= off and off + 4 <= 128 * 128
+                for e in range(4):
+                    elem = (r, 4 * (half * 16 + j) + e)
+                    assert off + e not in seen, "two elements at one place"
+                    seen[off + e] = elem
+                steps.setdefault(j, []).append(off * 4)
+        for j, byte_offs in steps.items():
+            byte_offs.sort()
+            assert byte_offs[-1] - byte_offs[0] == 31 * 16       # 32 rows, 16 bytes each, contiguous
+            assert all(b - a == 16 for a, b in zip(byte_offs, byte_offs[1:]))
+    assert len(seen) == 128 * 128
+    assert sorted(seen.values()) == [(r, c) for r in range(128) for c in range(128)]
